@@ -1,0 +1,178 @@
+"""Seeded synthetic inputs for the attention forward workloads.
+
+This module is the only code shared by the fp64 oracle side and the CUDA side.
+It draws numbers and lays them out; it holds none of the attention arithmetic.
+
+Every tensor is drawn with numpy's PCG64 generator from a SeedSequence keyed by
+(seed, tensor id, sequence index), so one sequence's block can be regenerated
+alone (the oracle checks sampled sequences of the full-size workloads without
+drawing the whole KV cache) and the bits are identical on any machine.
+Standard-normal float32 draws are rounded to bfloat16 with round-to-nearest-even.
+
+Workloads (the shapes the FlashAttention pages benchmark: dense/causal GQA
+prefill, a large head dim, varlen packing with a sliding window and the
+(192,128) head shape, and split-KV decode over a KV cache):
+
+  tiny     B=1  Hq=Hkv=2  Sq=Sk=128  D=64, dense
+  causal   B=2  Hq=32 Hkv=4  Sq=Sk=4096  D=128, causal
+  large    B=1  Hq=16 Hkv=2  Sq=Sk=8192  D=256, dense and causal, scale 1/16
+  varlen   16 sequences, lengths uniform in [256, 8192], Hq=Hkv=16,
+           Dqk=192, Dv=128, causal, window_left=1024
+  decode   Sq=1, B=64, Hq=32, Hkv=8, D=128, KV cache capacity 16384,
+           seqused_k uniform in [1024, 16384]
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+# tensor ids inside a workload's SeedSequence
+_Q, _K, _V = 0, 1, 2
+
+# bfloat16 bit pattern of a quiet NaN; written into KV-cache slots past
+# seqused_k so that any read of them that reaches the arithmetic shows up.
+BF16_NAN_BITS = 0x7FC0
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Widen bfloat16 bits to float32 exactly."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16(seed: int, tensor_id: int, index: int, shape) -> np.ndarray:
+    """N(0,1) draws for one sequence block, rounded to bf16 bits."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tensor_id, index])))
+    return f32_to_bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
+
+
+def uniform_lengths(seed: int, n: int, lo: int, hi: int) -> np.ndarray:
+    """n integers uniform in [lo, hi] inclusive (int32)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed])))
+    return rng.integers(lo, hi + 1, size=n).astype(np.int32)
+
+
+@dataclasses.dataclass
+class Workload:
+    """Host-side (numpy) inputs; bf16 tensors are uint16 bit arrays."""
+    name: str
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    num_heads_q: int
+    num_heads_kv: int
+    head_dim_qk: int
+    head_dim_v: int
+    softmax_scale: float
+    causal: bool = False
+    window_left: int = -1
+    window_right: int = -1
+    batch: int = 1
+    seqlen_q: int = 0          # batched layout only
+    seqlen_k: int = 0          # batched layout: K/V capacity per sequence
+    cu_seqlens_q: Optional[np.ndarray] = None   # int32 [B+1], varlen layout
+    cu_seqlens_k: Optional[np.ndarray] = None
+    seqused_k: Optional[np.ndarray] = None      # int32 [B]
+    max_seqlen_q: int = 0
+    max_seqlen_k: int = 0
+    seed: int = 0
+
+    @property
+    def varlen(self) -> bool:
+        return self.cu_seqlens_q is not None
+
+
+def batched(name, seed, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale=None, causal=False,
+            window_left=-1, window_right=-1, seqused_k=None, pad_bits=BF16_NAN_BITS):
+    """Batched layout: q (B,Sq,Hq,Dqk), k (B,Sk,Hkv,Dqk), v (B,Sk,Hkv,Dv).
+
+    Sequence b's block of each tensor comes from its own stream. With seqused_k,
+    only the first seqused_k[b] cache rows are drawn; the rest are filled with
+    `pad_bits` (a NaN by default), which a correct kernel never lets reach O.
+    """
+    q = np.empty((B, Sq, Hq, Dqk), np.uint16)
+    k = np.empty((B, Sk, Hkv, Dqk), np.uint16)
+    v = np.empty((B, Sk, Hkv, Dv), np.uint16)
+    for b in range(B):
+        q[b] = normal_bf16(seed, _Q, b, (Sq, Hq, Dqk))
+        n = Sk if seqused_k is None else int(seqused_k[b])
+        k[b, :n] = normal_bf16(seed, _K, b, (n, Hkv, Dqk))
+        v[b, :n] = normal_bf16(seed, _V, b, (n, Hkv, Dv))
+        if n < Sk:
+            k[b, n:] = pad_bits
+            v[b, n:] = pad_bits
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(Dqk))
+    return Workload(name=name, q=q, k=k, v=v, num_heads_q=Hq, num_heads_kv=Hkv,
+                    head_dim_qk=Dqk, head_dim_v=Dv, softmax_scale=scale, causal=causal,
+                    window_left=window_left, window_right=window_right, batch=B,
+                    seqlen_q=Sq, seqlen_k=Sk,
+                    seqused_k=None if seqused_k is None else np.asarray(seqused_k, np.int32),
+                    max_seqlen_q=Sq, max_seqlen_k=Sk, seed=seed)
+
+
+def packed(name, seed, lens_q, lens_k, Hq, Hkv, Dqk, Dv, scale=None, causal=False,
+           window_left=-1, window_right=-1):
+    """Varlen packed layout: q (Tq,Hq,Dqk), k (Tk,Hkv,Dqk), v (Tk,Hkv,Dv)."""
+    lens_q = np.asarray(lens_q, np.int64)
+    lens_k = np.asarray(lens_k, np.int64)
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)]).astype(np.int32)
+    q = np.empty((int(cu_q[-1]), Hq, Dqk), np.uint16)
+    k = np.empty((int(cu_k[-1]), Hkv, Dqk), np.uint16)
+    v = np.empty((int(cu_k[-1]), Hkv, Dv), np.uint16)
+    for b in range(len(lens_q)):
+        q[cu_q[b]:cu_q[b + 1]] = normal_bf16(seed, _Q, b, (int(lens_q[b]), Hq, Dqk))
+        k[cu_k[b]:cu_k[b + 1]] = normal_bf16(seed, _K, b, (int(lens_k[b]), Hkv, Dqk))
+        v[cu_k[b]:cu_k[b + 1]] = normal_bf16(seed, _V, b, (int(lens_k[b]), Hkv, Dv))
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(Dqk))
+    return Workload(name=name, q=q, k=k, v=v, num_heads_q=Hq, num_heads_kv=Hkv,
+                    head_dim_qk=Dqk, head_dim_v=Dv, softmax_scale=scale, causal=causal,
+                    window_left=window_left, window_right=window_right, batch=len(lens_q),
+                    cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+                    max_seqlen_q=int(lens_q.max()) if len(lens_q) else 0,
+                    max_seqlen_k=int(lens_k.max()) if len(lens_k) else 0, seed=seed)
+
+
+# ---- the named workloads -----------------------------------------------------
+
+VARLEN_LENGTH_SEED = 40
+DECODE_SEQUSED_SEED = 50
+
+
+def varlen_lengths() -> np.ndarray:
+    return uniform_lengths(VARLEN_LENGTH_SEED, 16, 256, 8192)
+
+
+def decode_seqused() -> np.ndarray:
+    return uniform_lengths(DECODE_SEQUSED_SEED, 64, 1024, 16384)
+
+
+def workload(name: str) -> Workload:
+    if name == "tiny":
+        return batched("tiny", 1, 1, 128, 128, 2, 2, 64, 64)
+    if name == "causal":
+        return batched("causal", 2, 2, 4096, 4096, 32, 4, 128, 128, causal=True)
+    if name in ("large_dense", "large_causal"):
+        return batched(name, 3, 1, 8192, 8192, 16, 2, 256, 256, scale=1.0 / 16,
+                       causal=(name == "large_causal"))
+    if name == "varlen":
+        lens = varlen_lengths()
+        return packed("varlen", 4, lens, lens, 16, 16, 192, 128, causal=True,
+                      window_left=1024, window_right=0)
+    if name == "decode":
+        return batched("decode", 5, 64, 1, 16384, 32, 8, 128, 128, seqused_k=decode_seqused())
+    raise KeyError(name)
+
+
+WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode")
