@@ -1,0 +1,429 @@
+// fa_api.cu - the C ABI of libfa.so: argument checks, TMA descriptor
+// encoding, the split policy, and routing between the prefill, decode and
+// combine kernels. All checks mirror `_flash_attn_fwd` on the FlashAttention
+// interface page ("mslk/attention/flash_attn/interface.py"): Hq % Hkv == 0,
+// head dims <= 256 and multiples of 8, int32 contiguous cu_seqlens/seqused,
+// num_splits <= 256 (`_flash_attn_fwd_combine`).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+
+namespace fa {
+namespace {
+
+__device__ int g_status[1];
+
+std::atomic<unsigned long long> g_timeout_ns{4000000000ull};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+int* status_ptr() {
+  // one address per device (the symbol lives in every device's image)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  static int* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// 4-D bf16 map (d, rows, heads, batch) with a box of (64, box_rows, 1, 1) and
+// 128-byte swizzle; out-of-range rows read as zero.
+bool make_map(CUtensorMap* m, const void* base, int64_t d, int64_t rows, int64_t heads, int64_t batch,
+              int64_t row_stride, int64_t head_stride, int64_t batch_stride, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
+  cuuint64_t strides[3] = {(cuuint64_t)(row_stride * 2), (cuuint64_t)(head_stride * 2),
+                           (cuuint64_t)(batch_stride * 2)};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0; }
+
+struct Resolved {
+  bool varlen;
+  int rows_q;       // batched: seqlen_q; varlen: max_seqlen_q
+  int kmax;         // batched: seqlen_k; varlen: max_seqlen_k
+  int r;
+  float scale;
+  int wl, wr;
+};
+
+int check_args(const fa_fwd_args* a, Resolved* out) {
+  if (!a) return FA_ERR_INVALID_ARG;
+  const bool varlen = a->cu_seqlens_q != nullptr || a->cu_seqlens_k != nullptr;
+  if (varlen && (a->cu_seqlens_q == nullptr || a->cu_seqlens_k == nullptr)) return FA_ERR_UNSUPPORTED;
+  if (a->batch < 0 || a->num_heads_q <= 0 || a->num_heads_kv <= 0) return FA_ERR_INVALID_ARG;
+  if (a->num_heads_q % a->num_heads_kv != 0) return FA_ERR_INVALID_ARG;
+  if (a->head_dim_qk <= 0 || a->head_dim_v <= 0 || a->head_dim_qk > 256 || a->head_dim_v > 256)
+    return FA_ERR_INVALID_ARG;
+  if (a->head_dim_qk % 8 != 0 || a->head_dim_v % 8 != 0) return FA_ERR_INVALID_ARG;
+  if (!prefill_supported(a->head_dim_qk, a->head_dim_v)) return FA_ERR_UNSUPPORTED;
+  if (a->window_left < -1 || a->window_right < -1) return FA_ERR_INVALID_ARG;
+  if (a->num_splits < 0 || a->num_splits > 256) return FA_ERR_INVALID_ARG;
+  if (varlen) {
+    if (a->total_q < 0 || a->total_k < 0 || a->max_seqlen_q < 0 || a->max_seqlen_k < 0) return FA_ERR_INVALID_ARG;
+  } else {
+    if (a->seqlen_q < 0 || a->seqlen_k < 0) return FA_ERR_INVALID_ARG;
+  }
+  Resolved r;
+  r.varlen = varlen;
+  r.rows_q = varlen ? a->max_seqlen_q : a->seqlen_q;
+  r.kmax = varlen ? a->max_seqlen_k : a->seqlen_k;
+  r.r = a->num_heads_q / a->num_heads_kv;
+  r.scale = (a->softmax_scale > 0.f && std::isfinite(a->softmax_scale))
+                ? a->softmax_scale
+                : 1.0f / std::sqrt(static_cast<float>(a->head_dim_qk));
+  r.wl = a->window_left;
+  r.wr = a->causal ? 0 : a->window_right;
+  if (out) *out = r;
+  return FA_OK;
+}
+
+int check_tensors(const fa_fwd_args* a, bool need_out) {
+  if (!a->q || !a->k || !a->v) return FA_ERR_INVALID_ARG;
+  if (need_out && !a->out) return FA_ERR_INVALID_ARG;
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || (need_out && !aligned16(a->out)))
+    return FA_ERR_ALIGNMENT;
+  const bool varlen = a->cu_seqlens_q != nullptr;
+  if (!stride_ok(a->q_row_stride) || !stride_ok(a->q_head_stride) || !stride_ok(a->k_row_stride) ||
+      !stride_ok(a->k_head_stride) || !stride_ok(a->v_row_stride) || !stride_ok(a->v_head_stride))
+    return FA_ERR_ALIGNMENT;
+  if (need_out && (!stride_ok(a->o_row_stride) || !stride_ok(a->o_head_stride))) return FA_ERR_ALIGNMENT;
+  if (!varlen) {
+    if (!stride_ok(a->q_batch_stride) || !stride_ok(a->k_batch_stride) || !stride_ok(a->v_batch_stride))
+      return FA_ERR_ALIGNMENT;
+    if (need_out && !stride_ok(a->o_batch_stride)) return FA_ERR_ALIGNMENT;
+  }
+  return FA_OK;
+}
+
+bool decode_shaped(const fa_fwd_args* a, const Resolved& r) {
+  return static_cast<long long>(r.rows_q) * r.r <= decode_max_rows();
+}
+
+int resolve_splits(const fa_fwd_args* a, const Resolved& r, int num_sms) {
+  if (a->num_splits > 0) return a->num_splits;
+  if (!decode_shaped(a, r) || r.kmax <= 0) return 1;
+  if (num_sms <= 0) num_sms = device_sms();
+  constexpr int kTarget = 2048;
+  int ns = (r.kmax + kTarget - 1) / kTarget;
+  const long long chunks = (static_cast<long long>(r.rows_q) * r.r + decode_max_rows() - 1) / decode_max_rows();
+  const long long units = static_cast<long long>(a->batch) * a->num_heads_kv * (chunks > 0 ? chunks : 1);
+  while (ns < 128 && units * ns < 2LL * num_sms && r.kmax / (2 * ns) >= 512) ns *= 2;
+  if (ns < 1) ns = 1;
+  if (ns > 128) ns = 128;
+  return ns;
+}
+
+int split_len_for(int kmax, int ns) {
+  if (ns <= 1) return INT32_MAX / 2;   // one split holds every key
+  const int per = (kmax + ns - 1) / ns;
+  const int l = ((per + 63) / 64) * 64;
+  return l > 0 ? l : 64;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t prefix_off, prefix_bytes;
+  size_t opart_off, opart_bytes;
+  size_t lpart_off, lpart_bytes;
+  size_t total;
+};
+
+WsLayout ws_layout(const fa_fwd_args* a, const Resolved& r, int ns) {
+  WsLayout w{};
+  size_t off = 0;
+  const bool prefill = ns <= 1 && !decode_shaped(a, r);
+  if (prefill && r.varlen) {
+    w.prefix_off = off;
+    w.prefix_bytes = align256(sizeof(int) * (static_cast<size_t>(a->batch) + 1));
+    off += w.prefix_bytes;
+  }
+  if (ns > 1) {
+    const size_t rows = r.varlen ? static_cast<size_t>(a->total_q)
+                                 : static_cast<size_t>(a->batch) * static_cast<size_t>(a->seqlen_q);
+    w.opart_off = off;
+    w.opart_bytes = align256(sizeof(float) * ns * rows * a->num_heads_q * a->head_dim_v);
+    off += w.opart_bytes;
+    w.lpart_off = off;
+    w.lpart_bytes = align256(sizeof(float) * ns * rows * a->num_heads_q);
+    off += w.lpart_bytes;
+  }
+  w.total = off;
+  return w;
+}
+
+void fill_common(FwdParams* p, const fa_fwd_args* a, const Resolved& r) {
+  std::memset(p, 0, sizeof(*p));
+  p->q = a->q;
+  p->out = a->out;
+  p->lse = a->lse;
+  p->q_bs = a->q_batch_stride;
+  p->q_rs = a->q_row_stride;
+  p->q_hs = a->q_head_stride;
+  p->o_bs = a->o_batch_stride;
+  p->o_rs = a->o_row_stride;
+  p->o_hs = a->o_head_stride;
+  p->cu_seqlens_q = a->cu_seqlens_q;
+  p->cu_seqlens_k = a->cu_seqlens_k;
+  p->seqused_k = a->seqused_k;
+  p->batch = a->batch;
+  p->seqlen_q = r.varlen ? 0 : a->seqlen_q;
+  p->seqlen_k = r.varlen ? 0 : a->seqlen_k;
+  p->total_q = r.varlen ? a->total_q : 0;
+  p->max_seqlen_q = r.rows_q;
+  p->hq = a->num_heads_q;
+  p->hkv = a->num_heads_kv;
+  p->r = r.r;
+  p->scale_log2 = static_cast<float>(static_cast<double>(r.scale) * 1.4426950408889634);
+  p->wl = r.wl;
+  p->wr = r.wr;
+  p->num_splits = 1;
+  p->split_len = INT32_MAX / 2;
+  p->write_partial = 0;
+  p->status = status_ptr();
+  p->timeout_ns = g_timeout_ns.load();
+}
+
+bool kv_maps(const fa_fwd_args* a, const Resolved& r, int box_rows, CUtensorMap* mk, CUtensorMap* mv) {
+  const int64_t rows = r.varlen ? a->total_k : a->seqlen_k;
+  const int64_t nb = r.varlen ? 1 : a->batch;
+  const int64_t kbs = r.varlen ? a->k_row_stride * (rows > 0 ? rows : 1) : a->k_batch_stride;
+  const int64_t vbs = r.varlen ? a->v_row_stride * (rows > 0 ? rows : 1) : a->v_batch_stride;
+  return make_map(mk, a->k, a->head_dim_qk, rows, a->num_heads_kv, nb, a->k_row_stride, a->k_head_stride,
+                  kbs > 0 ? kbs : 8, box_rows) &&
+         make_map(mv, a->v, a->head_dim_v, rows, a->num_heads_kv, nb, a->v_row_stride, a->v_head_stride,
+                  vbs > 0 ? vbs : 8, box_rows);
+}
+
+int run_decode(const fa_fwd_args* a, const Resolved& r, int ns, float* opart, float* lpart, cudaStream_t st) {
+  FwdParams p;
+  fill_common(&p, a, r);
+  p.num_splits = ns;
+  p.split_len = split_len_for(r.kmax, ns);
+  p.write_partial = opart != nullptr ? 1 : 0;
+  p.out_partial = opart;
+  p.lse_partial = lpart;
+  if (!p.status) return FA_ERR_CUDA;
+  CUtensorMap mk, mv;
+  if (!kv_maps(a, r, 64, &mk, &mv)) return FA_ERR_CUDA;
+  cudaError_t e = launch_decode(p, a->head_dim_qk, a->head_dim_v, mk, mv, st);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int run_prefill(const fa_fwd_args* a, const Resolved& r, void* ws, const WsLayout& w, cudaStream_t st) {
+  FwdParams p;
+  fill_common(&p, a, r);
+  if (!p.status) return FA_ERR_CUDA;
+  const int rpt = prefill_rows_per_tile(a->head_dim_qk, a->head_dim_v);
+  if (r.varlen) {
+    p.tile_prefix = reinterpret_cast<int*>(static_cast<char*>(ws) + w.prefix_off);
+    cudaError_t e = launch_varlen_prepare(p, rpt, st);
+    if (e != cudaSuccess) return FA_ERR_LAUNCH;
+  } else {
+    p.m_blocks = (a->seqlen_q + rpt - 1) / rpt;
+    p.num_tiles = p.m_blocks * a->num_heads_q * a->batch;
+  }
+  CUtensorMap mq, mk, mv;
+  const int64_t qrows = r.varlen ? a->total_q : a->seqlen_q;
+  const int64_t qb = r.varlen ? 1 : a->batch;
+  const int64_t qbs = r.varlen ? a->q_row_stride * (qrows > 0 ? qrows : 1) : a->q_batch_stride;
+  if (!make_map(&mq, a->q, a->head_dim_qk, qrows, a->num_heads_q, qb, a->q_row_stride, a->q_head_stride,
+                qbs > 0 ? qbs : 8, 128))
+    return FA_ERR_CUDA;
+  if (!kv_maps(a, r, 128, &mk, &mv)) return FA_ERR_CUDA;
+  const int sms = device_sms();
+  if (sms <= 0) return FA_ERR_CUDA;
+  cudaError_t e = launch_prefill(p, a->head_dim_qk, a->head_dim_v, mq, mk, mv, sms, st);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+bool no_work(const fa_fwd_args* a, const Resolved& r) {
+  if (a->batch == 0) return true;
+  if (r.varlen) return a->total_q == 0;
+  return a->seqlen_q == 0;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_abi_version(void) { return 100; }
+
+const char* fa_status_string(int s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_LAUNCH: return "kernel launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+    case FA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+void fa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 1); }
+
+int fa_num_splits(const fa_fwd_args* a, int num_sms) {
+  Resolved r;
+  if (check_args(a, &r) != FA_OK) return 1;
+  fa_fwd_args b = *a;
+  b.num_splits = 0;
+  return resolve_splits(&b, r, num_sms);
+}
+
+int fa_split_len(const fa_fwd_args* a, int num_splits) {
+  Resolved r;
+  if (check_args(a, &r) != FA_OK) return 0;
+  return split_len_for(r.kmax, num_splits);
+}
+
+size_t fa_workspace_size(const fa_fwd_args* a) {
+  Resolved r;
+  if (check_args(a, &r) != FA_OK) return 0;
+  const int ns = resolve_splits(a, r, 0);
+  return ws_layout(a, r, ns).total;
+}
+
+int fa_fwd(const fa_fwd_args* a, void* workspace, size_t workspace_bytes, void* stream) {
+  Resolved r;
+  int rc = check_args(a, &r);
+  if (rc != FA_OK) return rc;
+  if (no_work(a, r)) return FA_OK;
+  rc = check_tensors(a, true);
+  if (rc != FA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ns = resolve_splits(a, r, 0);
+  const WsLayout w = ws_layout(a, r, ns);
+  if (w.total > 0 && (workspace == nullptr || workspace_bytes < w.total)) return FA_ERR_WORKSPACE;
+  if (w.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
+  if (ns > 1) {
+    float* opart = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.opart_off);
+    float* lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lpart_off);
+    rc = run_decode(a, r, ns, opart, lpart, st);
+    if (rc != FA_OK) return rc;
+    return fa_combine(opart, lpart, ns, a->batch, r.varlen ? 0 : a->seqlen_q, a->num_heads_q, a->head_dim_v,
+                      a->cu_seqlens_q, r.varlen ? a->total_q : 0, a->out, a->o_batch_stride, a->o_row_stride,
+                      a->o_head_stride, a->lse, stream);
+  }
+  if (decode_shaped(a, r)) return run_decode(a, r, 1, nullptr, nullptr, st);
+  return run_prefill(a, r, workspace, w, st);
+}
+
+int fa_fwd_splitkv(const fa_fwd_args* a, int num_splits, float* out_partial, float* lse_partial,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  Resolved r;
+  int rc = check_args(a, &r);
+  if (rc != FA_OK) return rc;
+  if (num_splits < 1 || num_splits > 256) return FA_ERR_INVALID_ARG;
+  if (no_work(a, r)) return FA_OK;
+  rc = check_tensors(a, false);
+  if (rc != FA_OK) return rc;
+  if (!out_partial || !lse_partial) return FA_ERR_INVALID_ARG;
+  if (!aligned16(out_partial) || (reinterpret_cast<uintptr_t>(lse_partial) & 3u)) return FA_ERR_ALIGNMENT;
+  fa_fwd_args b = *a;
+  b.out = nullptr;
+  b.lse = nullptr;
+  return run_decode(&b, r, num_splits, out_partial, lse_partial, static_cast<cudaStream_t>(stream));
+}
+
+int fa_combine(const float* out_partial, const float* lse_partial, int num_splits, int batch, int seqlen_q,
+               int num_heads, int head_dim_v, const int32_t* cu_seqlens_q, int total_q, void* out,
+               int64_t o_batch_stride, int64_t o_row_stride, int64_t o_head_stride, float* lse, void* stream) {
+  if (num_splits < 1 || num_splits > 256) return FA_ERR_INVALID_ARG;
+  if (batch < 0 || num_heads <= 0 || seqlen_q < 0 || total_q < 0) return FA_ERR_INVALID_ARG;
+  if (head_dim_v != 64 && head_dim_v != 128 && head_dim_v != 256) return FA_ERR_UNSUPPORTED;
+  const bool varlen = cu_seqlens_q != nullptr;
+  const long long rows = varlen ? total_q : static_cast<long long>(batch) * seqlen_q;
+  if (rows == 0) return FA_OK;
+  if (!out_partial || !lse_partial || !out) return FA_ERR_INVALID_ARG;
+  if (!aligned16(out_partial) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse_partial) & 3u))
+    return FA_ERR_ALIGNMENT;
+  if (!stride_ok(o_row_stride) || !stride_ok(o_head_stride) || (!varlen && !stride_ok(o_batch_stride)))
+    return FA_ERR_ALIGNMENT;
+  CombineParams p;
+  p.out_partial = out_partial;
+  p.lse_partial = lse_partial;
+  p.out = out;
+  p.lse = lse;
+  p.o_bs = o_batch_stride;
+  p.o_rs = o_row_stride;
+  p.o_hs = o_head_stride;
+  p.num_splits = num_splits;
+  p.batch = batch;
+  p.seqlen_q = varlen ? 0 : seqlen_q;
+  p.hq = num_heads;
+  p.dv = head_dim_v;
+  p.varlen = varlen ? 1 : 0;
+  p.total_q = varlen ? total_q : 0;
+  cudaError_t e = launch_combine(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_get_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_DEVICE_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

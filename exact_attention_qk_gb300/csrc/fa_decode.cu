@@ -1,0 +1,501 @@
+// fa_decode.cu - split-KV decode forward and the LSE-weighted combine.
+//
+// Decode ("mslk/attention/fmha/triton_splitk.py", split-K forward; and
+// "mslk/attention/flash_attn/interface.py", `_flash_attn_fwd` with
+// num_splits > 1): few query rows against a long KV cache. Reading K and V
+// once from HBM is the whole cost, so the kernel is built for bandwidth:
+//   * one CTA per (split, KV head x row chunk, sequence); the Hq/Hkv query heads
+//     that share a KV head are packed as rows of one CTA (the triton page's
+//     head-swapping trick), so K/V bytes are read once per KV head;
+//   * a producer warp streams 64-key K/V tiles with TMA (128-byte swizzle) into
+//     an NSTAGE-deep mbarrier ring; cache rows at or past seqused_k are never
+//     used in arithmetic;
+//   * four compute warps take 16 keys each per tile: QK^T with 16-byte swizzled
+//     shared loads (conflict-free), online softmax in base 2 with the scale
+//     folded into q, and P.V with per-lane output columns;
+//   * the four warps' (m, l, O) states merge in shared memory at the end and the
+//     CTA writes either the final bf16 O / fp32 LSE or the fp32 split partials.
+#include <cuda_bf16.h>
+
+#include "fa_kernels.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kDecWarps = 4;            // compute warps
+constexpr int kDecThreads = (kDecWarps + 1) * 32;
+constexpr int kTileKeys = 64;
+constexpr int kBoxBytes = kTileKeys * 128;   // one 64-element x 64-key box
+
+template <int DK, int DV, int NR>
+struct DecodeCfg {
+  static constexpr int KCH = DK / 64;
+  static constexpr int VCH = DV / 64;
+  static constexpr int STAGE_BYTES = (KCH + VCH) * kBoxBytes;
+  static constexpr int NSTAGE = (STAGE_BYTES <= 32768) ? 3 : 2;
+  static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
+  static constexpr int Q_BYTES = NR * DK * 4;
+  static constexpr int P_BYTES = kDecWarps * 16 * NR * 4;
+  static constexpr int MERGE_BYTES = kDecWarps * NR * (DV + 2) * 4;
+  static constexpr int OFF_Q = RING_BYTES;
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + 16 + 1024;   // + alignment slack
+  static constexpr int E = DV / 32;                                   // output columns per lane
+  static_assert(MERGE_BYTES <= RING_BYTES, "merge area reuses the ring");
+  static_assert(NR * E <= 64, "accumulator budget");
+};
+
+template <int DK, int DV, int NR>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                  const FwdParams p) {
+  using C = DecodeCfg<DK, DV, NR>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
+  float* p_s = reinterpret_cast<float*>(smem + C::OFF_P);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::NSTAGE;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::NSTAGE);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x;
+  const int g = blockIdx.y % p.hkv;
+  const int chunk = blockIdx.y / p.hkv;
+  const int b = blockIdx.z;
+
+  // ---- sequence geometry --------------------------------------------------------------
+  const bool varlen = p.cu_seqlens_q != nullptr;
+  int q_row0 = 0, k_row0 = 0, sq = p.seqlen_q, sk = p.seqlen_k;
+  if (varlen) {
+    q_row0 = p.cu_seqlens_q[b];
+    sq = p.cu_seqlens_q[b + 1] - q_row0;
+    k_row0 = p.cu_seqlens_k[b];
+    sk = p.cu_seqlens_k[b + 1] - k_row0;
+  }
+  if (p.seqused_k) sk = p.seqused_k[b];
+  const int rows = sq * p.r;                       // packed rows of this KV head
+  const int prow0 = chunk * NR;
+  if (prow0 >= rows) return;                       // chunk past this sequence's rows
+  const int off = sk - sq;
+  const bool split_mode = p.write_partial != 0;
+  const int s_lo = min(sk, split * p.split_len);
+  const int s_hi = min(sk, (split + 1) * p.split_len);
+
+  // per-row visible key interval [lo, hi] (inclusive) inside this split
+  int lo[NR], hi[NR];
+  int klo = INT32_MAX, khi = -1;
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) {
+    const int pr = prow0 + rr;
+    lo[rr] = 1;
+    hi[rr] = 0;
+    if (pr < rows) {
+      const int i = pr / p.r;
+      int l = s_lo, h = s_hi - 1;
+      if (p.wl >= 0) l = max(l, i + off - p.wl);
+      if (p.wr >= 0) h = min(h, i + off + p.wr);
+      l = max(l, 0);
+      if (l <= h) {
+        lo[rr] = l;
+        hi[rr] = h;
+        klo = min(klo, l);
+        khi = max(khi, h + 1);
+      }
+    }
+  }
+
+  auto row_out = [&](int rr, int& i, int& h) {
+    const int pr = prow0 + rr;
+    i = pr / p.r;
+    h = g * p.r + pr % p.r;
+  };
+  auto write_row = [&](int rr, int d, float o, float lse_v, bool write_lse) {
+    int i, h;
+    row_out(rr, i, h);
+    if (split_mode) {
+      const int64_t rows_total = varlen ? p.total_q : int64_t(p.batch) * p.seqlen_q;
+      const int64_t ri = varlen ? int64_t(q_row0 + i) : int64_t(b) * p.seqlen_q + i;
+      p.out_partial[((int64_t(split) * rows_total + ri) * p.hq + h) * DV + d] = o;
+      if (write_lse) {
+        const int64_t li = varlen ? (int64_t(split) * p.hq + h) * p.total_q + q_row0 + i
+                                  : ((int64_t(split) * p.batch + b) * p.hq + h) * p.seqlen_q + i;
+        p.lse_partial[li] = lse_v;
+      }
+    } else {
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+      out[(varlen ? 0 : int64_t(b) * p.o_bs) + int64_t(q_row0 + i) * p.o_rs + int64_t(h) * p.o_hs + d] =
+          __float2bfloat16_rn(o);
+      if (write_lse && p.lse) {
+        const int64_t li = varlen ? int64_t(h) * p.total_q + q_row0 + i
+                                  : (int64_t(b) * p.hq + h) * p.seqlen_q + i;
+        p.lse[li] = lse_v;
+      }
+    }
+  };
+
+  if (khi <= klo) {   // nothing visible in this split for any row: O = 0, LSE = -inf
+    for (int idx = tid; idx < NR * DV; idx += blockDim.x) {
+      const int rr = idx / DV, d = idx % DV;
+      if (prow0 + rr < rows) write_row(rr, d, 0.f, -INFINITY, d == 0);
+    }
+    return;
+  }
+
+  const int key_base = (klo / kTileKeys) * kTileKeys;
+  const int ntiles = (khi - key_base + kTileKeys - 1) / kTileKeys;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDecWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // q rows -> fp32 with the softmax scale (base 2) folded in
+  for (int idx = tid; idx < NR * DK; idx += blockDim.x) {
+    const int rr = idx / DK, d = idx % DK;
+    float v = 0.f;
+    if (prow0 + rr < rows) {
+      int i, h;
+      row_out(rr, i, h);
+      const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q);
+      v = __bfloat162float(q[(varlen ? 0 : int64_t(b) * p.q_bs) + int64_t(q_row0 + i) * p.q_rs +
+                             int64_t(h) * p.q_hs + d]) *
+          p.scale_log2;
+    }
+    q_s[idx] = v;
+  }
+  __syncthreads();
+
+  const WaitGuard guard{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == kDecWarps) {
+    // ---------------- producer warp ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      const int kb = varlen ? 0 : b;
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        const int st = t % C::NSTAGE;
+        if (t >= C::NSTAGE && !mbar_wait(&empty[st], ((t / C::NSTAGE) - 1) & 1, guard)) break;
+        uint8_t* dst = smem + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+        const int row = k_row0 + key_base + t * kTileKeys;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c) tma_load_4d(dst + c * kBoxBytes, &mapK, &full[st], c * 64, row, g, kb);
+#pragma unroll
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_4d(dst + (C::KCH + c) * kBoxBytes, &mapV, &full[st], c * 64, row, g, kb);
+      }
+      // drain: never leave a copy in flight into shared memory of an exiting CTA
+      const WaitGuard drain{abort_flag, p.status, p.timeout_ns};
+      for (int u = max(0, t - C::NSTAGE); u < t; ++u) {
+        const uint32_t a = smem_u32(&full[u % C::NSTAGE]);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, (u / C::NSTAGE) & 1) && global_timer_ns() - t0 < drain.timeout_ns) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- compute warps ----------------
+  const int kk = lane & 15, hf = lane >> 4;
+  const int kw = warp * 16 + kk;                 // this lane's key inside a tile
+  constexpr int E = C::E;
+  float o[NR][E];
+  float m_run[NR], l_run[NR];
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) {
+    m_run[rr] = -INFINITY;
+    l_run[rr] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[rr][e] = 0.f;
+  }
+  float* pw = p_s + warp * 16 * NR;
+  const int e0 = lane * E;                       // first output column of this lane
+  const int vbox = e0 / 64, vch = (e0 % 64) / 8, vbyte = (e0 % 8) * 2;
+  const int key_end = min(sk, s_hi);             // keys at or past this are never used
+
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % C::NSTAGE;
+    if (!mbar_wait(&full[st], (t / C::NSTAGE) & 1, guard)) {
+      ok = false;
+      break;
+    }
+    const uint8_t* stage = smem + st * C::STAGE_BYTES;
+    const int tkey0 = key_base + t * kTileKeys;
+
+    // ---- S = q K^T for this lane's key over its half of the dims ----
+    float acc[NR];
+#pragma unroll
+    for (int rr = 0; rr < NR; ++rr) acc[rr] = 0.f;
+#pragma unroll
+    for (int c = 0; c < DK / 16; ++c) {
+      const int gc = hf * (DK / 16) + c;
+      const uint4 kv = *reinterpret_cast<const uint4*>(stage + (gc >> 3) * kBoxBytes + kw * 128 +
+                                                       (((gc & 7) ^ (kw & 7)) << 4));
+      float kf[8];
+      kf[0] = bf16lo_to_f32(kv.x); kf[1] = bf16hi_to_f32(kv.x);
+      kf[2] = bf16lo_to_f32(kv.y); kf[3] = bf16hi_to_f32(kv.y);
+      kf[4] = bf16lo_to_f32(kv.z); kf[5] = bf16hi_to_f32(kv.z);
+      kf[6] = bf16lo_to_f32(kv.w); kf[7] = bf16hi_to_f32(kv.w);
+#pragma unroll
+      for (int rr = 0; rr < NR; ++rr) {
+        const float4 qa = *reinterpret_cast<const float4*>(q_s + rr * DK + gc * 8);
+        const float4 qb = *reinterpret_cast<const float4*>(q_s + rr * DK + gc * 8 + 4);
+        float a = acc[rr];
+        a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
+        a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
+        a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
+        a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
+        acc[rr] = a;
+      }
+    }
+    const int j = tkey0 + kw;
+#pragma unroll
+    for (int rr = 0; rr < NR; ++rr) {
+      acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], 16);
+      acc[rr] = (j >= lo[rr] && j <= hi[rr]) ? acc[rr] : -INFINITY;
+    }
+    // ---- online softmax over this warp's 16 keys (base 2) ----
+#pragma unroll
+    for (int rr = 0; rr < NR; ++rr) {
+      float bm = acc[rr];
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      const float m_new = fmaxf(m_run[rr], bm);
+      float factor = 1.f, pv = 0.f;
+      if (m_new != -INFINITY) {
+        factor = ex2_approx(m_run[rr] - m_new);
+        pv = ex2_approx(acc[rr] - m_new);
+      }
+      m_run[rr] = m_new;
+      l_run[rr] = l_run[rr] * factor + pv;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[rr][e] *= factor;
+      if (hf == 0) pw[kk * NR + rr] = pv;
+    }
+    __syncwarp();
+    // ---- O += P V over the keys this warp owns that exist ----
+    const int wkey0 = tkey0 + warp * 16;
+    const int kbeg = max(0, klo - wkey0);
+    const int kend = min(16, key_end - wkey0);
+    for (int k2 = kbeg; k2 < kend; ++k2) {
+      const int key = warp * 16 + k2;
+      const uint8_t* vp = stage + (C::KCH + vbox) * kBoxBytes + key * 128 + (((vch ^ (key & 7)) << 4) + vbyte);
+      float vf[E];
+      if constexpr (E == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
+        vf[0] = bf16lo_to_f32(w); vf[1] = bf16hi_to_f32(w);
+      } else if constexpr (E == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(vp);
+        vf[0] = bf16lo_to_f32(w.x); vf[1] = bf16hi_to_f32(w.x);
+        vf[2] = bf16lo_to_f32(w.y); vf[3] = bf16hi_to_f32(w.y);
+      } else {
+        const uint4 w = *reinterpret_cast<const uint4*>(vp);
+        vf[0] = bf16lo_to_f32(w.x); vf[1] = bf16hi_to_f32(w.x);
+        vf[2] = bf16lo_to_f32(w.y); vf[3] = bf16hi_to_f32(w.y);
+        vf[4] = bf16lo_to_f32(w.z); vf[5] = bf16hi_to_f32(w.z);
+        vf[6] = bf16lo_to_f32(w.w); vf[7] = bf16hi_to_f32(w.w);
+      }
+#pragma unroll
+      for (int rr = 0; rr < NR; ++rr) {
+        const float pr = pw[k2 * NR + rr];
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[rr][e] = fmaf(pr, vf[e], o[rr][e]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+
+  // ---- merge the four warps' states ----
+  float lsum[NR];
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) {
+    float l = hf == 0 ? l_run[rr] : 0.f;
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    lsum[rr] = l;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");   // ring no longer read
+  float* mg = reinterpret_cast<float*>(smem);          // [warp][rr][DV + 2]
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) {
+    float* row = mg + (warp * NR + rr) * (DV + 2);
+#pragma unroll
+    for (int e = 0; e < E; ++e) row[e0 + e] = o[rr][e];
+    if (lane == 0) {
+      row[DV] = m_run[rr];
+      row[DV + 1] = lsum[rr];
+    }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+  if (!ok || *abort_flag) return;
+  for (int idx = tid; idx < NR * DV; idx += kDecWarps * 32) {
+    const int rr = idx / DV, d = idx % DV;
+    if (prow0 + rr >= rows) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mg[(w * NR + rr) * (DV + 2) + DV]);
+    float L = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float* row = mg + (w * NR + rr) * (DV + 2);
+        const float sc = ex2_approx(row[DV] - M);
+        L += row[DV + 1] * sc;
+        acc += row[d] * sc;
+      }
+    }
+    const bool empty_row = !(L > 0.f);
+    const float ov = empty_row ? 0.f : acc / L;
+    const float lse_v = empty_row ? -INFINITY : (M + log2f(L)) * 0.69314718055994530942f;
+    write_row(rr, d, ov, lse_v, d == 0);
+  }
+}
+
+// ---- combine ----------------------------------------------------------------------------
+constexpr int kCombineWarps = 8;
+
+template <int DV>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
+  constexpr int E = DV / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t rows_total = p.varlen ? p.total_q : int64_t(p.batch) * p.seqlen_q;
+  const int64_t gw = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+  if (gw >= rows_total * p.hq) return;
+  const int64_t ri = gw / p.hq;
+  const int h = static_cast<int>(gw % p.hq);
+  int64_t lse_base, lse_split_stride;
+  if (p.varlen) {
+    lse_base = int64_t(h) * p.total_q + ri;
+    lse_split_stride = int64_t(p.hq) * p.total_q;
+  } else {
+    const int64_t b = ri / p.seqlen_q, i = ri % p.seqlen_q;
+    lse_base = (b * p.hq + h) * p.seqlen_q + i;
+    lse_split_stride = int64_t(p.batch) * p.hq * p.seqlen_q;
+  }
+  constexpr float kLog2e = 1.4426950408889634f;
+  float M = -INFINITY;
+  for (int s = lane; s < p.num_splits; s += 32) M = fmaxf(M, p.lse_partial[lse_base + s * lse_split_stride]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float sum = 0.f;
+  if (M != -INFINITY)
+    for (int s = lane; s < p.num_splits; s += 32) {
+      const float l = p.lse_partial[lse_base + s * lse_split_stride];
+      if (l != -INFINITY) sum += ex2_approx((l - M) * kLog2e);
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const bool empty_row = (M == -INFINITY) || !(sum > 0.f);
+  const float lse = empty_row ? -INFINITY : M + logf(sum);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  if (!empty_row) {
+    for (int s = 0; s < p.num_splits; ++s) {
+      const float l = p.lse_partial[lse_base + s * lse_split_stride];
+      if (l == -INFINITY) continue;
+      const float w = ex2_approx((l - lse) * kLog2e);
+      const float* src = p.out_partial + ((int64_t(s) * rows_total + ri) * p.hq + h) * DV + lane * E;
+      if constexpr (E == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src + e);
+          acc[e] = fmaf(w, v.x, acc[e]); acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+          acc[e + 2] = fmaf(w, v.z, acc[e + 2]); acc[e + 3] = fmaf(w, v.w, acc[e + 3]);
+        }
+      }
+    }
+  }
+  int64_t obase;
+  if (p.varlen) {
+    obase = ri * p.o_rs + int64_t(h) * p.o_hs;
+  } else {
+    const int64_t b = ri / p.seqlen_q, i = ri % p.seqlen_q;
+    obase = b * p.o_bs + i * p.o_rs + int64_t(h) * p.o_hs;
+  }
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + obase + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    *reinterpret_cast<__nv_bfloat162*>(out + e) = __floats2bfloat162_rn(acc[e], acc[e + 1]);
+  }
+  if (p.lse && lane == 0) p.lse[lse_base] = lse;
+}
+
+template <int DK, int DV, int NR>
+cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
+                            cudaStream_t stream) {
+  using C = DecodeCfg<DK, DV, NR>;
+  auto kern = decode_kernel<DK, DV, NR>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int rows = p.max_seqlen_q * p.r;
+  const int chunks = (rows + NR - 1) / NR;
+  dim3 grid(p.num_splits, p.hkv * chunks, p.batch);
+  kern<<<grid, kDecThreads, C::SMEM, stream>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
+template <int DK, int DV>
+cudaError_t launch_decode_nr(const FwdParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
+                             cudaStream_t stream) {
+  const int rows = p.max_seqlen_q * p.r;
+  constexpr int NRMAX = (DV == 256) ? 8 : 16;
+  if (rows <= 1) return launch_decode_t<DK, DV, 1>(p, mk, mv, stream);
+  if (rows <= 2) return launch_decode_t<DK, DV, 2>(p, mk, mv, stream);
+  if (rows <= 4) return launch_decode_t<DK, DV, 4>(p, mk, mv, stream);
+  if (rows <= 8 || NRMAX == 8) return launch_decode_t<DK, DV, 8>(p, mk, mv, stream);
+  return launch_decode_t<DK, DV, NRMAX>(p, mk, mv, stream);
+}
+
+}  // namespace
+
+bool decode_supported(int dk, int dv) {
+  return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128) ||
+         (dk == 256 && dv == 256);
+}
+
+int decode_max_rows() { return 16; }
+
+cudaError_t launch_decode(const FwdParams& p, int dk, int dv, const CUtensorMap& mk, const CUtensorMap& mv,
+                          cudaStream_t stream) {
+  if (dk == 64 && dv == 64) return launch_decode_nr<64, 64>(p, mk, mv, stream);
+  if (dk == 128 && dv == 128) return launch_decode_nr<128, 128>(p, mk, mv, stream);
+  if (dk == 192 && dv == 128) return launch_decode_nr<192, 128>(p, mk, mv, stream);
+  if (dk == 256 && dv == 256) return launch_decode_nr<256, 256>(p, mk, mv, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+  const int64_t rows_total = p.varlen ? p.total_q : int64_t(p.batch) * p.seqlen_q;
+  const int64_t warps = rows_total * p.hq;
+  if (warps == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>((warps + kCombineWarps - 1) / kCombineWarps);
+  switch (p.dv) {
+    case 64: combine_kernel<64><<<blocks, kCombineWarps * 32, 0, stream>>>(p); break;
+    case 128: combine_kernel<128><<<blocks, kCombineWarps * 32, 0, stream>>>(p); break;
+    case 256: combine_kernel<256><<<blocks, kCombineWarps * 32, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,64 @@
+// fa_kernels.h - parameter blocks and launchers shared by the host API
+// (fa_api.cu) and the kernel translation units. Internal to libfa.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Everything a forward kernel needs besides the tensor maps. Strides are in
+// elements. `wr` is already 0 when the call was causal.
+struct FwdParams {
+  const void* q;
+  void* out;
+  float* lse;                    // final LSE or NULL
+  float* out_partial;            // split mode: fp32 partial O
+  float* lse_partial;            // split mode: fp32 partial LSE
+  int64_t q_bs, q_rs, q_hs;
+  int64_t o_bs, o_rs, o_hs;
+  const int* cu_seqlens_q;
+  const int* cu_seqlens_k;
+  const int* seqused_k;
+  int* tile_prefix;              // varlen prefill: [batch+1] tile prefix sums (workspace)
+  int batch, seqlen_q, seqlen_k; // batched sizes (seqlen_k = capacity)
+  int total_q;                   // varlen rows (LSE row stride)
+  int max_seqlen_q;
+  int hq, hkv, r;                // r = hq / hkv
+  float scale_log2;              // softmax_scale * log2(e)
+  int wl, wr;                    // -1 = unbounded
+  int num_splits;                // decode grid extent over key splits (>= 1)
+  int split_len;                 // keys per split (covers every key when num_splits == 1)
+  int write_partial;             // decode: 1 = fp32 partials at [split], 0 = final bf16 O / LSE
+  int m_blocks;                  // batched prefill: ceil(seqlen_q / tile rows)
+  int num_tiles;                 // batched prefill: total work tiles
+  int* status;                   // device status word
+  unsigned long long timeout_ns;
+};
+
+// Launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_prefill(const FwdParams& p, int dk, int dv, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, int num_sms, cudaStream_t stream);
+cudaError_t launch_varlen_prepare(const FwdParams& p, int rows_per_tile, cudaStream_t stream);
+int prefill_rows_per_tile(int dk, int dv);
+bool prefill_supported(int dk, int dv);
+
+cudaError_t launch_decode(const FwdParams& p, int dk, int dv, const CUtensorMap& mk, const CUtensorMap& mv,
+                          cudaStream_t stream);
+bool decode_supported(int dk, int dv);
+int decode_max_rows();
+
+struct CombineParams {
+  const float* out_partial;
+  const float* lse_partial;
+  void* out;
+  float* lse;
+  int64_t o_bs, o_rs, o_hs;
+  int num_splits;
+  int batch, seqlen_q, hq, dv;
+  int varlen, total_q;
+};
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+}  // namespace fa

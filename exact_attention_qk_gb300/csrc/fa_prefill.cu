@@ -1,0 +1,692 @@
+// fa_prefill.cu - persistent, warp-specialised tcgen05 attention forward.
+//
+// The FlashAttention forward of "mslk/attention/flash_attn/interface.py"
+// (`_flash_attn_fwd`, FlashAttentionForwardSm100: 128x128 tiles, q_stage 2,
+// persistent when dense) re-designed here for sm_103a from the Blackwell idioms
+// the backward page ("mslk/attention/flash_attn/flash_bwd_sm100.py") shows:
+// TMA loads into 128B-swizzled shared memory, mbarrier pipelines, a single
+// MMA-issuing thread, tcgen05 accumulators in tensor memory, the P operand of
+// P.V read straight from tensor memory, and exp2 with the scale folded in.
+//
+// One CTA per SM loops over work tiles (m-block, q head, sequence); causal
+// tiles come longest first. A tile is NQ x 128 query rows:
+//   NQ = 2 (head dims 64, 128, 192/128): two 128-row Q tiles share each K/V
+//     tile; softmax warpgroup s owns Q tile s, and the MMA warp ping-pongs
+//       PV(n,0) S(n-1,0) PV(n,1) S(n-1,1) ...
+//     so each softmax overlaps the other tile's GEMMs.
+//     TMEM: S0 [0,128) S1 [128,256) O0 [256,256+DV) O1 [256+DV,256+2DV).
+//   NQ = 1 (head dim 256): one Q tile, S double-buffered (slots alternate by
+//     block), O in [256,512).
+// P (bf16) overwrites the first 64 columns of its S slot. Key blocks run from
+// the diagonal downwards so the masked blocks come first. The running max is
+// rescaled lazily: O and l are only rescaled when the row max grows by more
+// than 4 (base-2 units), the threshold of the FA4 notes on the sm_120 page.
+//
+// Warps: [0, 4*NSM) softmax (NSM = NQ warpgroups), then one MMA warp, one
+// Q+K TMA warp and one V TMA warp. Every mbarrier wait is bounded; on a
+// timeout the CTA raises a shared abort flag, records the failure in the
+// device status word, drains its copies and MMAs, frees TMEM and exits.
+#include <cuda_bf16.h>
+
+#include "fa_kernels.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;                 // query rows per Q tile
+constexpr int kBN = 128;                 // keys per K/V block
+constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle-128B column chunk)
+constexpr float kRescaleThreshold = 4.f;
+
+template <int DK_, int DV_>
+struct PrefillCfg {
+  static constexpr int DK = DK_, DV = DV_;
+  static constexpr int NQ = (DV <= 128) ? 2 : 1;
+  static constexpr int NSM = NQ;                         // softmax warpgroups
+  static constexpr int KST = (DK == 64) ? 3 : (DK == 192 || DK == 256) ? (DK == 256 ? 1 : 2) : 2;
+  static constexpr int VST = (DK == 64) ? 3 : (DK == 192 || DK == 256) ? 1 : 2;
+  static constexpr int KCH = DK / 64, VCH = DV / 64;
+  static constexpr int Q_BYTES = KCH * kChunkBytes;
+  static constexpr int K_BYTES = KCH * kChunkBytes;
+  static constexpr int V_BYTES = VCH * kChunkBytes;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + KST * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VST * V_BYTES;
+  static constexpr int NBAR = 2 * 2 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2 + 1;
+  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
+  // at least half the SM's shared memory, so one CTA (the one that owns all
+  // 512 TMEM columns) is resident per SM
+  static constexpr int SMEM = (SMEM_USED + 1024 < 120 * 1024) ? 120 * 1024 : SMEM_USED + 1024;
+  static constexpr int MMA_WARP = 4 * NSM;
+  static constexpr int TMA_QK_WARP = MMA_WARP + 1;
+  static constexpr int TMA_V_WARP = MMA_WARP + 2;
+  static constexpr int THREADS = 32 * (MMA_WARP + 3);
+  static constexpr int ROWS_PER_TILE = NQ * kBM;
+  static constexpr int O_COL = 256;
+  static_assert(NQ == 2 ? (256 + 2 * DV <= 512) : (256 + DV <= 512), "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct Tile {
+  int b, h, g, mb;
+  int q_row0, k_row0;   // first row of the sequence in q's / k's row axis
+  int sq, sk;
+};
+
+struct Range {
+  int r0;       // first query row of this Q tile inside the sequence
+  bool active;  // the Q tile has rows
+  int nlo, nhi; // key blocks [nlo, nhi) hold visible keys; empty when nhi <= nlo
+};
+
+template <int ROWS_PER_TILE>
+__device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
+  if (p.cu_seqlens_q == nullptr) {
+    if (t >= p.num_tiles) return false;
+    const int per = p.hq * p.batch;
+    const int mbi = t / per, rem = t - mbi * per;
+    T.mb = p.m_blocks - 1 - mbi;   // longest-first for causal; a fixed order otherwise
+    T.h = rem % p.hq;
+    T.b = rem / p.hq;
+    T.q_row0 = 0;
+    T.k_row0 = 0;
+    T.sq = p.seqlen_q;
+    T.sk = p.seqused_k ? p.seqused_k[T.b] : p.seqlen_k;
+  } else {
+    const int total = p.tile_prefix[p.batch];
+    if (t >= total) return false;
+    int lo = 0, hi = p.batch - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.tile_prefix[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    T.b = lo;
+    const int local = t - p.tile_prefix[lo];
+    const int nmb = (p.tile_prefix[lo + 1] - p.tile_prefix[lo]) / p.hq;
+    T.mb = nmb - 1 - local / p.hq;
+    T.h = local % p.hq;
+    T.q_row0 = p.cu_seqlens_q[lo];
+    T.sq = p.cu_seqlens_q[lo + 1] - T.q_row0;
+    T.k_row0 = p.cu_seqlens_k[lo];
+    T.sk = p.seqused_k ? p.seqused_k[lo] : p.cu_seqlens_k[lo + 1] - T.k_row0;
+  }
+  T.g = T.h / p.r;
+  return true;
+}
+
+__device__ __forceinline__ Range stage_range(const FwdParams& p, const Tile& T, int r0) {
+  Range R;
+  R.r0 = r0;
+  R.active = r0 < T.sq;
+  R.nlo = R.nhi = 0;
+  if (!R.active) return R;
+  const int ilast = min(r0 + kBM - 1, T.sq - 1), off = T.sk - T.sq;
+  int klo = 0, khi = T.sk;
+  if (p.wl >= 0) klo = max(klo, r0 + off - p.wl);
+  if (p.wr >= 0) khi = min(khi, ilast + off + p.wr + 1);
+  if (khi > klo) {
+    R.nlo = klo / kBN;
+    R.nhi = (khi + kBN - 1) / kBN;
+  }
+  return R;
+}
+
+__device__ __forceinline__ bool has_work(const Range& R) { return R.nhi > R.nlo; }
+__device__ __forceinline__ bool part(const Range& R, int n) { return R.nhi > R.nlo && n >= R.nlo && n < R.nhi; }
+
+// true when some (row, key) of Q tile R x key block n is not visible
+__device__ __forceinline__ bool needs_mask(const FwdParams& p, const Tile& T, const Range& R, int n) {
+  const int off = T.sk - T.sq;
+  const bool full = ((n + 1) * kBN <= T.sk) && (p.wr < 0 || (n + 1) * kBN - 1 <= R.r0 + off + p.wr) &&
+                    (p.wl < 0 || n * kBN >= R.r0 + kBM - 1 + off - p.wl);
+  return !full;
+}
+
+struct Bars {
+  uint64_t* q_full;    // [2]
+  uint64_t* q_empty;   // [2]
+  uint64_t* k_full;    // [KST]
+  uint64_t* k_empty;
+  uint64_t* v_full;    // [VST]
+  uint64_t* v_empty;
+  uint64_t* s_full;    // [2] per S slot
+  uint64_t* p_full;    // [2] per S slot
+  uint64_t* o_bar;     // [2] per O: one phase per P.V
+  uint64_t* o_empty;   // [2] per O: epilogue done reading
+  uint64_t* drain;
+};
+
+template <class Cfg>
+__device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+  Bars B;
+  B.q_full = b; b += 2;
+  B.q_empty = b; b += 2;
+  B.k_full = b; b += Cfg::KST;
+  B.k_empty = b; b += Cfg::KST;
+  B.v_full = b; b += Cfg::VST;
+  B.v_empty = b; b += Cfg::VST;
+  B.s_full = b; b += 2;
+  B.p_full = b; b += 2;
+  B.o_bar = b; b += 2;
+  B.o_empty = b; b += 2;
+  B.drain = b; b += 1;
+  return B;
+}
+
+// Spin (bounded, ignoring the abort flag) until the given phase completed:
+// used to drain copies / MMAs in flight before the CTA exits.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity) && global_timer_ns() - t0 < timeout_ns) {
+  }
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                   const __grid_constant__ CUtensorMap mapV, const FwdParams p) {
+  using Cfg = PrefillCfg<DK, DV>;
+  constexpr int NQ = Cfg::NQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars B = carve_bars<Cfg>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_BAR + Cfg::NBAR * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool varlen = p.cu_seqlens_q != nullptr;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.q_full[i], 1);
+      mbar_init(&B.q_empty[i], 1);
+      mbar_init(&B.s_full[i], 1);
+      mbar_init(&B.p_full[i], kBM);
+      mbar_init(&B.o_bar[i], 1);
+      mbar_init(&B.o_empty[i], kBM);
+    }
+    for (int i = 0; i < Cfg::KST; ++i) {
+      mbar_init(&B.k_full[i], 1);
+      mbar_init(&B.k_empty[i], 1);
+    }
+    for (int i = 0; i < Cfg::VST; ++i) {
+      mbar_init(&B.v_full[i], 1);
+      mbar_init(&B.v_empty[i], 1);
+    }
+    mbar_init(B.drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == Cfg::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitGuard guard{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == Cfg::TMA_QK_WARP || warp == Cfg::TMA_V_WARP) {
+    // ================= TMA producers =================
+    if (lane == 0) {
+      const bool is_k = warp == Cfg::TMA_QK_WARP;
+      if (is_k) {
+        tma_prefetch_desc(&mapQ);
+        tma_prefetch_desc(&mapK);
+      } else {
+        tma_prefetch_desc(&mapV);
+      }
+      uint32_t kc = 0, qc[2] = {0, 0};
+      bool ok = true;
+      for (int t = blockIdx.x; ok; t += gridDim.x) {
+        Tile T;
+        if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, t, T)) break;
+        Range R[NQ];
+        int nlo = INT32_MAX, nhi = INT32_MIN;
+#pragma unroll
+        for (int s = 0; s < NQ; ++s) {
+          R[s] = stage_range(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
+          if (has_work(R[s])) {
+            nlo = min(nlo, R[s].nlo);
+            nhi = max(nhi, R[s].nhi);
+          }
+        }
+        if (nhi <= nlo) continue;
+        const int cb = varlen ? 0 : T.b;
+        if (is_k) {
+#pragma unroll
+          for (int s = 0; s < NQ; ++s) {
+            if (!has_work(R[s])) continue;
+            if (qc[s] > 0 && !mbar_wait(&B.q_empty[s], (qc[s] - 1) & 1, guard)) { ok = false; break; }
+            uint8_t* dst = smem + Cfg::OFF_Q + s * Cfg::Q_BYTES;
+            mbar_arrive_expect_tx(&B.q_full[s], Cfg::Q_BYTES);
+#pragma unroll
+            for (int c = 0; c < Cfg::KCH; ++c)
+              tma_load_4d(dst + c * kChunkBytes, &mapQ, &B.q_full[s], c * 64, T.q_row0 + R[s].r0, T.h, cb);
+            ++qc[s];
+          }
+          for (int n = nhi - 1; ok && n >= nlo; --n) {
+            const int st = kc % Cfg::KST;
+            if (kc >= Cfg::KST && !mbar_wait(&B.k_empty[st], ((kc / Cfg::KST) - 1) & 1, guard)) { ok = false; break; }
+            uint8_t* dst = smem + Cfg::OFF_K + st * Cfg::K_BYTES;
+            mbar_arrive_expect_tx(&B.k_full[st], Cfg::K_BYTES);
+#pragma unroll
+            for (int c = 0; c < Cfg::KCH; ++c)
+              tma_load_4d(dst + c * kChunkBytes, &mapK, &B.k_full[st], c * 64, T.k_row0 + n * kBN, T.g, cb);
+            ++kc;
+          }
+        } else {
+          for (int n = nhi - 1; ok && n >= nlo; --n) {
+            const int st = kc % Cfg::VST;
+            if (kc >= Cfg::VST && !mbar_wait(&B.v_empty[st], ((kc / Cfg::VST) - 1) & 1, guard)) { ok = false; break; }
+            uint8_t* dst = smem + Cfg::OFF_V + st * Cfg::V_BYTES;
+            mbar_arrive_expect_tx(&B.v_full[st], Cfg::V_BYTES);
+#pragma unroll
+            for (int c = 0; c < Cfg::VCH; ++c)
+              tma_load_4d(dst + c * kChunkBytes, &mapV, &B.v_full[st], c * 64, T.k_row0 + n * kBN, T.g, cb);
+            ++kc;
+          }
+        }
+      }
+      // drain the copies still in flight (only after an abort can any be)
+      if (is_k) {
+        const int nst = Cfg::KST;
+        for (uint32_t u = (kc > (uint32_t)nst ? kc - nst : 0); u < kc; ++u)
+          drain_wait(&B.k_full[u % nst], (u / nst) & 1, p.timeout_ns);
+        for (int s = 0; s < NQ; ++s)
+          if (qc[s] > 0) drain_wait(&B.q_full[s], (qc[s] - 1) & 1, p.timeout_ns);
+      } else {
+        const int nst = Cfg::VST;
+        for (uint32_t u = (kc > (uint32_t)nst ? kc - nst : 0); u < kc; ++u)
+          drain_wait(&B.v_full[u % nst], (u / nst) & 1, p.timeout_ns);
+      }
+    }
+  } else if (warp == Cfg::MMA_WARP) {
+    // ================= MMA issuer (one thread) =================
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(kBM, DV, false, true);
+      const uint32_t q_base = smem_u32(smem + Cfg::OFF_Q);
+      const uint32_t k_base = smem_u32(smem + Cfg::OFF_K);
+      const uint32_t v_base = smem_u32(smem + Cfg::OFF_V);
+
+      // S[slot] = Q[qs] K[kst]^T, K-major operands, 16 deep per instruction
+      auto issue_s = [&](int qs, int slot, int kst) {
+        const uint32_t d = tmem + slot * 128;
+        const uint32_t qa = q_base + qs * Cfg::Q_BYTES, ka = k_base + kst * Cfg::K_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+          mma_bf16_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+        }
+      };
+      // O[o] (+)= P[slot] V[vst]; P from TMEM, V MN-major (64-column chunks 16 KB apart)
+      auto issue_pv = [&](int o, int slot, int vst, bool acc) {
+        const uint32_t d = tmem + Cfg::O_COL + o * DV;
+        const uint32_t va = v_base + vst * Cfg::V_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(d, tmem + slot * 128 + kk * 8, sdesc_sw128(va + kk * 16 * 128, kChunkBytes, 1024), IDESC_PV,
+                      (kk > 0 || acc) ? 1u : 0u);
+      };
+
+      uint32_t kc = 0, vc = 0, qw[2] = {0, 0}, pw[2] = {0, 0}, ou[2] = {0, 0};
+      uint32_t jc = 0;   // NQ == 1: jobs so far (S slot = job parity)
+      bool ok = true;
+      for (int t = blockIdx.x; ok; t += gridDim.x) {
+        Tile T;
+        if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, t, T)) break;
+        Range R[NQ];
+        int nlo = INT32_MAX, nhi = INT32_MIN;
+#pragma unroll
+        for (int s = 0; s < NQ; ++s) {
+          R[s] = stage_range(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
+          if (has_work(R[s])) {
+            nlo = min(nlo, R[s].nlo);
+            nhi = max(nhi, R[s].nhi);
+          }
+        }
+        if (nhi <= nlo) continue;
+        bool first_s[2] = {true, true}, first_pv[2] = {true, true};
+
+        auto wait_q = [&](int s) -> bool {
+          if (!first_s[s]) return true;
+          first_s[s] = false;
+          const bool r = mbar_wait(&B.q_full[s], qw[s] & 1, guard);
+          ++qw[s];
+          return r;
+        };
+        auto before_pv = [&](int o) -> bool {   // O[o] free for the tile's first P.V
+          if (!first_pv[o]) return true;
+          first_pv[o] = false;
+          bool r = true;
+          if (ou[o] > 0) r = mbar_wait(&B.o_empty[o], (ou[o] - 1) & 1, guard);
+          ++ou[o];
+          return r;
+        };
+
+        if constexpr (NQ == 2) {
+          // prologue: S for the first block of each participating Q tile
+          {
+            const int n0 = nhi - 1, st = kc % Cfg::KST;
+            if (!mbar_wait(&B.k_full[st], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
+            for (int s = 0; s < 2; ++s) {
+              if (!part(R[s], n0)) continue;
+              if (!wait_q(s)) { ok = false; break; }
+              issue_s(s, s, st);
+              mma_commit(&B.s_full[s]);
+              if (n0 == R[s].nlo) mma_commit(&B.q_empty[s]);
+            }
+            if (!ok) break;
+            mma_commit(&B.k_empty[st]);
+            ++kc;
+          }
+          for (int n = nhi - 1; n >= nlo; --n) {
+            const int vst = vc % Cfg::VST;
+            if (!mbar_wait(&B.v_full[vst], (vc / Cfg::VST) & 1, guard)) { ok = false; break; }
+            const bool has_next = n - 1 >= nlo;
+            const int kst = kc % Cfg::KST;
+            bool k_ready = false;
+            for (int s = 0; s < 2; ++s) {
+              if (part(R[s], n)) {
+                if (!mbar_wait(&B.p_full[s], pw[s] & 1, guard)) { ok = false; break; }
+                ++pw[s];
+                tc_fence_after();
+                const bool acc = !first_pv[s];
+                if (!before_pv(s)) { ok = false; break; }
+                issue_pv(s, s, vst, acc);
+                mma_commit(&B.o_bar[s]);
+              }
+              if (has_next && part(R[s], n - 1)) {
+                if (!k_ready) {
+                  if (!mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
+                  k_ready = true;
+                }
+                if (!wait_q(s)) { ok = false; break; }
+                issue_s(s, s, kst);
+                mma_commit(&B.s_full[s]);
+                if (n - 1 == R[s].nlo) mma_commit(&B.q_empty[s]);
+              }
+            }
+            if (!ok) break;
+            mma_commit(&B.v_empty[vst]);
+            ++vc;
+            if (has_next) {
+              if (!k_ready && !mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
+              mma_commit(&B.k_empty[kst]);
+              ++kc;
+            }
+          }
+        } else {
+          // one Q tile, S slots alternate: S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ...
+          const int cnt = nhi - nlo;
+          auto do_s = [&](int i) -> bool {
+            const int st = kc % Cfg::KST;
+            if (!mbar_wait(&B.k_full[st], (kc / Cfg::KST) & 1, guard)) return false;
+            if (!wait_q(0)) return false;
+            const int slot = (jc + i) & 1;
+            issue_s(0, slot, st);
+            mma_commit(&B.s_full[slot]);
+            if (i == cnt - 1) mma_commit(&B.q_empty[0]);
+            mma_commit(&B.k_empty[st]);
+            ++kc;
+            return true;
+          };
+          for (int i = 0; ok && i < min(2, cnt); ++i) ok = do_s(i);
+          for (int i = 0; ok && i < cnt; ++i) {
+            const int slot = (jc + i) & 1;
+            const int vst = vc % Cfg::VST;
+            if (!mbar_wait(&B.v_full[vst], (vc / Cfg::VST) & 1, guard)) { ok = false; break; }
+            if (!mbar_wait(&B.p_full[slot], pw[slot] & 1, guard)) { ok = false; break; }
+            ++pw[slot];
+            tc_fence_after();
+            const bool acc = i > 0;
+            if (!before_pv(0)) { ok = false; break; }
+            issue_pv(0, slot, vst, acc);
+            mma_commit(&B.o_bar[0]);
+            mma_commit(&B.v_empty[vst]);
+            ++vc;
+            if (i + 2 < cnt) ok = do_s(i + 2);
+          }
+          jc += cnt;
+        }
+      }
+      // wait for every MMA this thread issued before TMEM is released
+      mma_commit(B.drain);
+      drain_wait(B.drain, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax warpgroups =================
+    const int wg = warp >> 2;                 // Q tile (NQ == 2) or 0
+    const int row_local = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int o_idx = (NQ == 2) ? wg : 0;
+    const uint32_t o_addr = tmem + lane_off + Cfg::O_COL + o_idx * DV;
+    uint32_t sw[2] = {0, 0};   // S waits per slot
+    uint32_t ow = 0;           // o_bar phases consumed (one per P.V of this O, in order)
+    uint32_t jc = 0;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+    bool ok = true;
+    for (int t = blockIdx.x; ok; t += gridDim.x) {
+      Tile T;
+      if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, t, T)) break;
+      const Range R = stage_range(p, T, T.mb * Cfg::ROWS_PER_TILE + wg * kBM);
+      if (!R.active) continue;
+      const int i = R.r0 + row_local;
+      const bool valid = i < T.sq;
+      const int64_t orow = (varlen ? 0 : int64_t(T.b) * p.o_bs) + int64_t(T.q_row0 + i) * p.o_rs +
+                           int64_t(T.h) * p.o_hs;
+      const int64_t lrow = varlen ? int64_t(T.h) * p.total_q + T.q_row0 + i
+                                  : (int64_t(T.b) * p.hq + T.h) * p.seqlen_q + i;
+      if (!has_work(R)) {
+        if (valid) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < DV / 8; ++c) *reinterpret_cast<uint4*>(out + orow + c * 8) = z;
+          if (p.lse) p.lse[lrow] = -INFINITY;
+        }
+        continue;
+      }
+      const int off = T.sk - T.sq;
+      float m = -INFINITY, l = 0.f;
+      for (int n = R.nhi - 1; n >= R.nlo; --n) {
+        const int slot = (NQ == 2) ? wg : (jc & 1);
+        if (!mbar_wait(&B.s_full[slot], sw[slot] & 1, guard)) { ok = false; break; }
+        ++sw[slot];
+        tc_fence_after();
+        uint32_t r[128];
+        tmem_ld128(tmem + lane_off + slot * 128, r);
+        float* s = reinterpret_cast<float*>(r);
+        if (needs_mask(p, T, R, n)) {
+          const int jb = n * kBN;
+          const int c_lo = (p.wl >= 0) ? i + off - p.wl - jb : INT32_MIN / 2;
+          int c_hi = T.sk - 1 - jb;
+          if (p.wr >= 0) c_hi = min(c_hi, i + off + p.wr - jb);
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (c < c_lo || c > c_hi) ? -INFINITY : s[c];
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float bmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+        const float m_new = fmaxf(m, bmax);
+        // The previous P.V of this O (if any in this tile) has a phase on o_bar
+        // that is consumed exactly once: before O is rescaled, or else just
+        // before this block's P is published (so the next P.V cannot run ahead).
+        bool pending = n != R.nhi - 1;
+        if (n == R.nhi - 1) {
+          m = m_new;
+        } else {
+          const bool need = m_new > m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) { ok = false; break; }
+            ++ow;
+            pending = false;
+            tc_fence_after();
+            const float f = need ? ex2_approx(m - m_new) : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < DV / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + c * 32, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+              tmem_st32(o_addr + c * 32, o);
+            }
+            tmem_st_wait();
+            if (need) {
+              l *= f;
+              m = m_new;
+            }
+          }
+        }
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          s[c] = ex2_approx(fmaf(s[c], p.scale_log2, -mu));
+          s[c + 1] = ex2_approx(fmaf(s[c + 1], p.scale_log2, -mu));
+          s[c + 2] = ex2_approx(fmaf(s[c + 2], p.scale_log2, -mu));
+          s[c + 3] = ex2_approx(fmaf(s[c + 3], p.scale_log2, -mu));
+          l0 += s[c];
+          l1 += s[c + 1];
+          l2 += s[c + 2];
+          l3 += s[c + 3];
+        }
+        l += (l0 + l1) + (l2 + l3);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+        tmem_st64(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[64]>(r));
+        tmem_st_wait();
+        if (pending) {
+          if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) { ok = false; break; }
+          ++ow;
+        }
+        tc_fence_before();
+        mbar_arrive(&B.p_full[slot]);
+        ++jc;
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16, LSE (natural log) ----
+      if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) { ok = false; break; }
+      ++ow;
+      tc_fence_after();
+      const bool empty_row = !(l > 0.f);
+      const float inv_l = empty_row ? 0.f : 1.f / l;
+#pragma unroll 1
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + c * 32, o);
+        if (valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(out + orow + c * 32);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
+      }
+      if (valid && p.lse) p.lse[lrow] = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+      tc_fence_before();
+      mbar_arrive(&B.o_empty[o_idx]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Cfg::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void varlen_prepare_kernel(const int* cu_seqlens_q, int batch, int rows_per_tile, int hq,
+                                      int* prefix) {
+  __shared__ int part[1024];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int per = (batch + nt - 1) / nt;
+  const int b0 = min(batch, tid * per), b1 = min(batch, b0 + per);
+  int sum = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int sq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    sum += ((sq + rows_per_tile - 1) / rows_per_tile) * hq;
+  }
+  part[tid] = sum;
+  __syncthreads();
+  for (int o = 1; o < nt; o <<= 1) {
+    const int v = tid >= o ? part[tid - o] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  int run = part[tid] - sum;
+  for (int b = b0; b < b1; ++b) {
+    prefix[b] = run;
+    const int sq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    run += ((sq + rows_per_tile - 1) / rows_per_tile) * hq;
+  }
+  if (tid == nt - 1) prefix[batch] = part[tid];
+}
+
+template <int DK, int DV>
+cudaError_t launch_prefill_t(const FwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
+                             const CUtensorMap& mv, int num_sms, cudaStream_t stream) {
+  using Cfg = PrefillCfg<DK, DV>;
+  auto kern = prefill_kernel<DK, DV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  if (e != cudaSuccess) return e;
+  long long tiles;
+  if (p.cu_seqlens_q == nullptr) {
+    tiles = p.num_tiles;
+  } else {
+    tiles = (long long)p.batch * p.hq * ((p.max_seqlen_q + Cfg::ROWS_PER_TILE - 1) / Cfg::ROWS_PER_TILE);
+  }
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_supported(int dk, int dv) {
+  return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128) ||
+         (dk == 256 && dv == 256);
+}
+
+int prefill_rows_per_tile(int dk, int dv) {
+  if (dk == 64 && dv == 64) return PrefillCfg<64, 64>::ROWS_PER_TILE;
+  if (dk == 128 && dv == 128) return PrefillCfg<128, 128>::ROWS_PER_TILE;
+  if (dk == 192 && dv == 128) return PrefillCfg<192, 128>::ROWS_PER_TILE;
+  if (dk == 256 && dv == 256) return PrefillCfg<256, 256>::ROWS_PER_TILE;
+  return 0;
+}
+
+cudaError_t launch_prefill(const FwdParams& p, int dk, int dv, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, int num_sms, cudaStream_t stream) {
+  if (dk == 64 && dv == 64) return launch_prefill_t<64, 64>(p, mq, mk, mv, num_sms, stream);
+  if (dk == 128 && dv == 128) return launch_prefill_t<128, 128>(p, mq, mk, mv, num_sms, stream);
+  if (dk == 192 && dv == 128) return launch_prefill_t<192, 128>(p, mq, mk, mv, num_sms, stream);
+  if (dk == 256 && dv == 256) return launch_prefill_t<256, 256>(p, mq, mk, mv, num_sms, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_varlen_prepare(const FwdParams& p, int rows_per_tile, cudaStream_t stream) {
+  varlen_prepare_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens_q, p.batch, rows_per_tile, p.hq, p.tile_prefix);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

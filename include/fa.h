@@ -1,0 +1,191 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact attention forward library (libfa.so).
+ *
+ * The operation is the exact scaled-dot-product attention forward with a
+ * per-row log-sum-exp, as defined by the FlashAttention pages:
+ *
+ *   "mslk/attention/flash_attn/interface.py", `_flash_attn_fwd`:
+ *       O = softmax(scale * Q K^T + mask) V,  LSE = log sum_j exp(scale q.k_j)
+ *       over visible keys; default scale 1/sqrt(head_dim_qk); O has q's layout
+ *       with head_dim_v; LSE is fp32 (B,Hq,Sq), or (Hq,Tq) for packed varlen;
+ *       causal means window_right = 0; GQA head h reads KV head h / (Hq/Hkv).
+ *   "mslk/attention/flash_attn/flash_bwd_sm100.py", causal block bound:
+ *       the causal diagonal is bottom-right aligned (offset Sk - Sq), and the
+ *       window [i + off - window_left, i + off + window_right] is taken about it.
+ *   "mslk/attention/flash_attn/interface.py", `_flash_attn_fwd_combine` and
+ *   "mslk/attention/fmha/triton_splitk.py", `merge_attentions`:
+ *       split-KV partials (fp32 O and LSE per split) merge by LSE weights.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers; the library allocates nothing.
+ *     The caller owns every buffer, including workspace, and the stream.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous on that stream; inputs must stay alive and
+ *     unmodified until the stream reaches the call.
+ *   - bf16 tensors have a contiguous last dimension; the other strides are
+ *     given in ELEMENTS. Base pointers must be 16-byte aligned and strides
+ *     multiples of 8 elements (16 bytes), else FA_ERR_ALIGNMENT.
+ *   - Arguments are checked before any launch: a non-zero status means that
+ *     nothing was launched (except FA_ERR_LAUNCH / FA_ERR_CUDA, reported after
+ *     a failed launch). No error crosses the ABI as an exception.
+ *   - Device-side waits are bounded; a wait that runs out sets a device status
+ *     word instead of hanging. fa_get_status() reads and clears it.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* shape / dtype-rule / null-pointer violation          */
+  FA_ERR_UNSUPPORTED = 2,     /* legal input outside the compiled kernel set           */
+  FA_ERR_ALIGNMENT = 3,       /* base pointer or stride not 16-byte aligned            */
+  FA_ERR_WORKSPACE = 4,       /* workspace NULL or smaller than fa_workspace_size()   */
+  FA_ERR_LAUNCH = 5,          /* a kernel launch failed (cudaGetLastError)            */
+  FA_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device wait ran out (from fa_get_status)   */
+  FA_ERR_CUDA = 7,            /* another CUDA runtime error (no device, bad stream)   */
+};
+
+/*
+ * Arguments of one attention forward.
+ *
+ * Batched layout (cu_seqlens_q == NULL):
+ *   q   (batch, seqlen_q, num_heads_q,  head_dim_qk)
+ *   k   (batch, seqlen_k, num_heads_kv, head_dim_qk)   seqlen_k = cache capacity
+ *   v   (batch, seqlen_k, num_heads_kv, head_dim_v)
+ *   out (batch, seqlen_q, num_heads_q,  head_dim_v)    bf16, written
+ *   lse (batch, num_heads_q, seqlen_q)                 fp32 contiguous, written; may be NULL
+ * Packed varlen layout (cu_seqlens_q and cu_seqlens_k both non-NULL, int32 [batch+1],
+ * prefix sums starting at 0; the *_batch_stride fields are ignored):
+ *   q   (total_q, num_heads_q, head_dim_qk)   k, v (total_k, num_heads_kv, ...)
+ *   out (total_q, num_heads_q, head_dim_v)    lse (num_heads_q, total_q)
+ * seqused_k (int32 [batch], optional): only keys [0, seqused_k[b]) of sequence b
+ *   exist; it overrides seqlen_k / the cu_seqlens_k length. The decode path never
+ *   reads cache rows past seqused_k[b]. The prefill path reads whole 128-key tiles,
+ *   so rows up to the next multiple of 128 past seqused_k[b] must hold finite values.
+ * Masks: causal != 0 forces window_right = 0. window_left / window_right = -1
+ *   means unbounded on that side. Key j is visible from query row i of a
+ *   sequence with Sq query rows and Sk keys iff
+ *     j < Sk and (wl < 0 or j >= i + Sk - Sq - wl) and (wr < 0 or j <= i + Sk - Sq + wr).
+ *   A row with no visible key gets O = 0 and LSE = -inf.
+ * softmax_scale <= 0 (or NaN) selects 1/sqrt(head_dim_qk).
+ * num_splits: 0 = let the library choose (fa_num_splits), 1 = no split,
+ *   > 1 = split-KV with that many splits followed by the combine (<= 256).
+ * Supported (head_dim_qk, head_dim_v): (64,64), (128,128), (192,128), (256,256).
+ * Element type: bf16 for q, k, v and out.
+ */
+typedef struct fa_fwd_args {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  int64_t q_batch_stride, q_row_stride, q_head_stride;
+  int64_t k_batch_stride, k_row_stride, k_head_stride;
+  int64_t v_batch_stride, v_row_stride, v_head_stride;
+  int64_t o_batch_stride, o_row_stride, o_head_stride;
+  int32_t batch;
+  int32_t seqlen_q;        /* batched: query rows per sequence                 */
+  int32_t seqlen_k;        /* batched: key rows (capacity) per sequence        */
+  int32_t num_heads_q;
+  int32_t num_heads_kv;
+  int32_t head_dim_qk;
+  int32_t head_dim_v;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  const int32_t* seqused_k;
+  int32_t total_q;         /* varlen: rows of q / out                           */
+  int32_t total_k;         /* varlen: rows of k / v                             */
+  int32_t max_seqlen_q;    /* varlen: upper bound on any query length           */
+  int32_t max_seqlen_k;    /* varlen: upper bound on any key length             */
+  float softmax_scale;
+  int32_t causal;
+  int32_t window_left;
+  int32_t window_right;
+  int32_t num_splits;
+} fa_fwd_args;
+
+/*
+ * fa_fwd - O and LSE for args (the whole forward: split-KV plus combine when the
+ * resolved split count is > 1, otherwise one kernel).
+ * workspace: device buffer of at least fa_workspace_size(args) bytes, 256-byte
+ * aligned; may be NULL when that size is 0. Its contents are scratch.
+ * Returns FA_OK or an error code (see the enum); asynchronous on `stream`.
+ */
+int fa_fwd(const fa_fwd_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_fwd_splitkv - the split-KV pass alone ("interface.py", `_flash_attn_fwd`
+ * with num_splits > 1: fp32 out_partial and lse_partial).
+ * Split s covers key positions [s*L, (s+1)*L) of every sequence, with
+ * L = fa_split_len(args, num_splits). An empty split writes O = 0, LSE = -inf.
+ *   out_partial fp32 (num_splits, batch, seqlen_q, num_heads_q, head_dim_v)
+ *               or   (num_splits, total_q, num_heads_q, head_dim_v), contiguous
+ *   lse_partial fp32 (num_splits, batch, num_heads_q, seqlen_q)
+ *               or   (num_splits, num_heads_q, total_q), contiguous
+ * args->out / args->lse / args->num_splits are ignored. 1 <= num_splits <= 256.
+ * workspace: as for fa_fwd (this pass needs none today; pass NULL, 0).
+ */
+int fa_fwd_splitkv(const fa_fwd_args* args, int num_splits, float* out_partial,
+                   float* lse_partial, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_combine - merge split partials by LSE weights ("interface.py",
+ * `_flash_attn_fwd_combine`; "triton_splitk.py", `merge_attentions`):
+ *   M = max_s LSE_s;  LSE = M + log sum_s exp(LSE_s - M);  O = sum_s exp(LSE_s - LSE) O_s
+ * Splits with LSE_s = -inf are skipped (their O_s is never read); if every split
+ * is empty the row gets O = 0 and LSE = -inf.
+ * Layouts: partials as in fa_fwd_splitkv (cu_seqlens_q != NULL selects the
+ * packed layout with total_q rows; only its presence matters). out is bf16
+ * with the given strides (elements; batch stride ignored when packed); lse is
+ * fp32 (batch, num_heads, seqlen_q) or (num_heads, total_q), may be NULL.
+ * head_dim_v in {64, 128, 256}; 1 <= num_splits <= 256.
+ */
+int fa_combine(const float* out_partial, const float* lse_partial, int num_splits,
+               int batch, int seqlen_q, int num_heads, int head_dim_v,
+               const int32_t* cu_seqlens_q, int total_q,
+               void* out, int64_t o_batch_stride, int64_t o_row_stride, int64_t o_head_stride,
+               float* lse, void* stream);
+
+/* Bytes of workspace fa_fwd needs for args (with args->num_splits resolved as fa_fwd does). */
+size_t fa_workspace_size(const fa_fwd_args* args);
+
+/*
+ * Split count fa_fwd uses when args->num_splits == 0. Decode-shaped problems
+ * (seqlen_q * Hq/Hkv <= 16) are split into chunks of about 2048 keys so that
+ * sequences of very different length spread over the SMs; others are not split.
+ * num_sms <= 0 queries the current device.
+ */
+int fa_num_splits(const fa_fwd_args* args, int num_sms);
+
+/* Keys per split, L = 64 * ceil(ceil(Kmax / num_splits) / 64), Kmax = seqlen_k
+ * (batched) or max_seqlen_k (varlen). */
+int fa_split_len(const fa_fwd_args* args, int num_splits);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device status word of the
+ * current device. Returns FA_OK, or FA_ERR_DEVICE_TIMEOUT if some kernel's
+ * bounded wait ran out since the last call (that kernel's outputs are invalid).
+ */
+int fa_get_status(void* stream);
+
+/* Limit for every device-side wait, in nanoseconds (default 4e9 = 4 s). */
+void fa_set_wait_timeout_ns(uint64_t ns);
+
+/* Static text for a status code. */
+const char* fa_status_string(int status);
+
+/* ABI version (major*100 + minor). */
+int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,139 @@
+"""The C ABI without a GPU: libfa.so loads, exports every entry point that
+include/fa.h declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+LIB = os.path.join(ROOT, "exact_attention_qk_gb300", "libfa.so")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not os.path.exists(LIB):
+        from exact_attention_qk_gb300 import build
+        build.build(selftest=False)
+    import torch  # noqa: F401  (provides the CUDA runtime the library links)
+    from exact_attention_qk_gb300 import fa as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["fa_fwd", "fa_fwd_splitkv", "fa_combine", "fa_workspace_size", "fa_num_splits",
+              "fa_split_len", "fa_get_status", "fa_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(fa):
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (fa_[a-z_0-9]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = fa.lib()
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_struct_layout_matches_header(fa, tmp_path):
+    """Compile a C probe against include/fa.h and compare every field offset."""
+    fields = [f[0] for f in fa.FwdArgs._fields_]
+    src = tmp_path / "probe.c"
+    body = "\n".join(f'  printf("%s %zu\\n", "{n}", offsetof(fa_fwd_args, {n}));' for n in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "fa.h"\nint main(void){\n'
+                   '  printf("sizeof %zu\\n", sizeof(fa_fwd_args));\n' + body + "\n  return 0;\n}\n")
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                        check=True).stdout.splitlines())
+    assert int(got["sizeof"]) == ctypes.sizeof(fa.FwdArgs)
+    for n in fields:
+        assert int(got[n]) == getattr(fa.FwdArgs, n).offset, n
+    assert fa.fa_abi_version() == 100
+
+
+def _args(fa, **over):
+    a = fa.FwdArgs()
+    a.q, a.k, a.v, a.out = 0x10000, 0x20000, 0x30000, 0x40000
+    a.batch, a.seqlen_q, a.seqlen_k = 2, 300, 300
+    a.num_heads_q, a.num_heads_kv, a.head_dim_qk, a.head_dim_v = 8, 2, 128, 128
+    a.q_batch_stride, a.q_row_stride, a.q_head_stride = 300 * 8 * 128, 8 * 128, 128
+    a.k_batch_stride, a.k_row_stride, a.k_head_stride = 300 * 2 * 128, 2 * 128, 128
+    a.v_batch_stride, a.v_row_stride, a.v_head_stride = 300 * 2 * 128, 2 * 128, 128
+    a.o_batch_stride, a.o_row_stride, a.o_head_stride = 300 * 8 * 128, 8 * 128, 128
+    a.window_left, a.window_right = -1, -1
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(num_heads_q=6, num_heads_kv=4), 1),            # Hq % Hkv
+    (dict(head_dim_qk=264), 1),                           # > 256
+    (dict(head_dim_qk=100), 1),                           # not a multiple of 8
+    (dict(head_dim_qk=96, head_dim_v=96), 2),             # legal but not compiled
+    (dict(head_dim_qk=128, head_dim_v=64), 2),
+    (dict(window_left=-2), 1),
+    (dict(num_splits=257), 1),
+    (dict(batch=-1), 1),
+    (dict(q=0x10008), 3),                                 # 8-byte aligned only
+    (dict(k_row_stride=2 * 128 + 4), 3),                  # stride not a multiple of 8 elements
+    (dict(out=0), 1),
+    (dict(q=0), 1),
+])
+def test_rejections_before_launch(fa, over, code):
+    a = _args(fa, **over)
+    assert fa.lib().fa_fwd(ctypes.byref(a), None, 0, None) == code
+
+
+def test_varlen_needs_both_cu_seqlens(fa):
+    a = _args(fa, cu_seqlens_q=0x50000)
+    assert fa.lib().fa_fwd(ctypes.byref(a), None, 0, None) == 2
+
+
+def test_empty_problem_is_a_no_op(fa):
+    a = _args(fa, batch=0)
+    assert fa.lib().fa_fwd(ctypes.byref(a), None, 0, None) == 0
+    a = _args(fa, seqlen_q=0)
+    assert fa.lib().fa_fwd(ctypes.byref(a), None, 0, None) == 0
+
+
+def test_combine_rejections(fa):
+    L = fa.lib()
+    assert L.fa_combine(0x1000, 0x2000, 0, 1, 1, 1, 128, None, 0, 0x3000, 0, 0, 0, None, None) == 1
+    assert L.fa_combine(0x1000, 0x2000, 257, 1, 1, 1, 128, None, 0, 0x3000, 0, 0, 0, None, None) == 1
+    assert L.fa_combine(0x1000, 0x2000, 2, 1, 1, 1, 96, None, 0, 0x3000, 0, 0, 0, None, None) == 2
+    assert L.fa_combine(0x1008, 0x2000, 2, 1, 1, 1, 128, None, 0, 0x3000, 128, 128, 128, None, None) == 3
+    assert L.fa_combine(0x1000, 0x2000, 2, 0, 1, 1, 128, None, 0, 0x3000, 0, 0, 0, None, None) == 0
+
+
+def test_split_policy(fa):
+    # decode shape of the benchmark: Kmax 16384 -> 8 splits of 2048 keys
+    a = _args(fa, batch=64, seqlen_q=1, seqlen_k=16384, num_heads_q=32, num_heads_kv=8)
+    assert fa.fa_num_splits(a, 152) == 8
+    assert fa.fa_split_len(a, 8) == 2048
+    assert fa.fa_split_len(a, 3) == 64 * -(-(-(-16384 // 3)) // 64)
+    # few units: more splits to fill the SMs
+    a = _args(fa, batch=1, seqlen_q=1, seqlen_k=16384, num_heads_q=8, num_heads_kv=8)
+    assert fa.fa_num_splits(a, 152) == 32
+    # prefill shapes are not split by default
+    a = _args(fa)
+    assert fa.fa_num_splits(a, 152) == 1
+    a = _args(fa, num_splits=5)
+    assert fa.fa_num_splits(a, 152) == 5 or fa.fa_num_splits(a, 152) == 1
+
+
+def test_status_strings(fa):
+    for c in range(8):
+        assert fa.fa_status_string(c)
+    assert "unknown" in fa.fa_status_string(99)
