@@ -1,0 +1,524 @@
+"""Benchmark of the exact attention forward on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload causal|large_dense|large_causal|varlen|decode|tiny] [--only]
+
+One step is one forward of the named workload (inputs resident in HBM): for the
+prefill workloads one persistent tcgen05 kernel (plus the varlen prepare
+kernel), for decode the split-KV kernel plus the combine kernel. The headline
+line is the causal GQA prefill (B=2, Hq=32, Hkv=4, Sq=Sk=4096, D=128) in
+TFLOP/s with the standard attention FLOP count 2*(Dqk+Dv)*#visible(i,j); the
+other workloads are measured in the same run and reported under "workloads"
+(decode in GB/s of algorithmic bytes: Q + visible K/V rows + O + LSE).
+
+Timing: W untimed steps, then K steps each bracketed by CUDA events on the
+launching stream, with an L2 flush (a 512 MB write) before every timed step
+and a barrier + synchronize around the timed region; max over ranks.
+`--impl reference` times the fp64 CPU oracle on a bounded sample instead.
+With N > 1 (torchrun), every rank runs an independent replica of the
+workload (the path needs no exchange); value = all ranks' work / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_qk_gb300 import inputs  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+# ---------------------------------------------------------------- accounting --
+def visible_pairs(sq: int, sk: int, causal: bool, wl: int, wr: int) -> int:
+    """#(i, j) with key j visible from row i (bottom-right aligned diagonal)."""
+    if sq <= 0 or sk <= 0:
+        return 0
+    if causal:
+        wr = 0
+    off = sk - sq
+    i = np.arange(sq, dtype=np.int64)
+    lo = np.zeros(sq, np.int64) if wl < 0 else np.maximum(0, i + off - wl)
+    hi = np.full(sq, sk - 1, np.int64) if wr < 0 else np.minimum(sk - 1, i + off + wr)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
+def seq_lengths(w):
+    if w.varlen:
+        lq = np.diff(w.cu_seqlens_q)
+        lk = np.diff(w.cu_seqlens_k) if w.seqused_k is None else w.seqused_k
+        return list(zip(lq.tolist(), lk.tolist()))
+    lk = [w.seqlen_k] * w.batch if w.seqused_k is None else w.seqused_k.tolist()
+    return [(w.seqlen_q, k) for k in lk]
+
+
+def flops(w) -> float:
+    pairs = sum(visible_pairs(sq, sk, w.causal, w.window_left, w.window_right) for sq, sk in seq_lengths(w))
+    return 2.0 * (w.head_dim_qk + w.head_dim_v) * pairs * w.num_heads_q
+
+
+def decode_bytes(w) -> float:
+    rows = sum(sq for sq, _ in seq_lengths(w))
+    keys = sum(sk for _, sk in seq_lengths(w))
+    q = rows * w.num_heads_q * w.head_dim_qk * 2
+    kv = keys * w.num_heads_kv * (w.head_dim_qk + w.head_dim_v) * 2
+    o = rows * w.num_heads_q * w.head_dim_v * 2
+    lse = rows * w.num_heads_q * 4
+    return float(q + kv + o + lse)
+
+
+def is_decode(name):
+    return name == "decode"
+
+
+# ------------------------------------------------------------------- peaks ----
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBs")
+            bf = d.get("bf16_tflops")
+            bfs = d.get("bf16_tflops_sustained") or bf
+            if hbm and bf:
+                return dict(hbm=float(hbm), bf16=float(bf), bf16_sustained=float(bfs), source="measured")
+        except Exception:
+            pass
+    return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sustained=FALLBACK_BF16_TFLOPS_SUSTAINED,
+                source="fallback")
+
+
+# ------------------------------------------------------------------ clocks ----
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- GPU timing ------
+class Runner:
+    """Device-resident inputs and pre-marshalled C-ABI calls for one workload."""
+
+    def __init__(self, name, dev):
+        import torch
+        from exact_attention_qk_gb300 import fa
+        self.torch, self.fa = torch, fa
+        self.name = name
+        self.w = w = inputs.workload(name)
+        self.dev = dev
+
+        def up(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        self.q, self.k, self.v = up(w.q), up(w.k), up(w.v)
+        self.extra = {}
+        if w.varlen:
+            self.extra = dict(cu_seqlens_q=torch.from_numpy(w.cu_seqlens_q).to(dev),
+                              cu_seqlens_k=torch.from_numpy(w.cu_seqlens_k).to(dev),
+                              max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k)
+        if w.seqused_k is not None:
+            self.extra["seqused_k"] = torch.from_numpy(w.seqused_k).to(dev)
+        self.kw = dict(softmax_scale=w.softmax_scale, causal=w.causal, window_left=w.window_left,
+                       window_right=w.window_right)
+        hq = w.num_heads_q
+        self.out = torch.empty(w.q.shape[:-1] + (w.head_dim_v,), dtype=torch.bfloat16, device=dev)
+        lshape = (hq, w.q.shape[0]) if w.varlen else (w.batch, hq, w.seqlen_q)
+        self.lse = torch.empty(lshape, dtype=torch.float32, device=dev)
+        self.args = fa.make_args(self.q, self.k, self.v, self.out, self.lse, **self.kw, **self.extra)
+        self.ws_bytes = fa.fa_workspace_size(self.args)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.decode = is_decode(name)
+        if self.decode:
+            self.ns = fa.fa_num_splits(self.args, 0)
+            rows = w.q.shape[:-2] if not w.varlen else w.q.shape[:1]
+            self.opart = torch.empty((self.ns,) + tuple(rows) + (hq, w.head_dim_v), dtype=torch.float32,
+                                     device=dev)
+            self.lpart = torch.empty((self.ns,) + tuple(lshape), dtype=torch.float32, device=dev)
+        self.work = decode_bytes(w) if self.decode else flops(w)
+        self.launches_per_step = 2 if (self.decode or w.varlen) else 1
+
+    def stream_ptr(self):
+        import ctypes
+        return ctypes.c_void_p(self.torch.cuda.current_stream().cuda_stream)
+
+    def step(self):
+        import ctypes
+        rc = self.fa.lib().fa_fwd(ctypes.byref(self.args), self.ws.data_ptr(), self.ws_bytes, self.stream_ptr())
+        if rc != 0:
+            raise RuntimeError(f"fa_fwd: {self.fa.fa_status_string(rc)}")
+
+    def step_split(self):
+        """decode as its two kernels, returning the events around the split-KV kernel."""
+        import ctypes
+        t = self.torch
+        e0, e1 = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        e0.record()
+        rc = self.fa.lib().fa_fwd_splitkv(ctypes.byref(self.args), self.ns, self.opart.data_ptr(),
+                                          self.lpart.data_ptr(), None, 0, self.stream_ptr())
+        e1.record()
+        if rc != 0:
+            raise RuntimeError(f"fa_fwd_splitkv: {self.fa.fa_status_string(rc)}")
+        w = self.w
+        o_bs, o_rs, o_hs = (0, self.out.stride(0), self.out.stride(1)) if w.varlen else \
+            (self.out.stride(0), self.out.stride(1), self.out.stride(2))
+        rc = self.fa.lib().fa_combine(
+            self.opart.data_ptr(), self.lpart.data_ptr(), self.ns, w.batch, 0 if w.varlen else w.seqlen_q,
+            w.num_heads_q, w.head_dim_v, self.extra["cu_seqlens_q"].data_ptr() if w.varlen else None,
+            w.q.shape[0] if w.varlen else 0, self.out.data_ptr(), o_bs, o_rs, o_hs, self.lse.data_ptr(),
+            self.stream_ptr())
+        if rc != 0:
+            raise RuntimeError(f"fa_combine: {self.fa.fa_status_string(rc)}")
+        return e0, e1
+
+
+def l2_flush_buffer(torch, dev):
+    return torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+
+def time_steps(r: Runner, steps: int, warmup: int, flush):
+    """Returns per-step ms and per-step ms of the dominant kernel."""
+    torch = r.torch
+    for _ in range(warmup):
+        if r.decode:
+            r.step_split()
+        else:
+            r.step()
+    torch.cuda.synchronize()
+    st = r.fa.fa_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    step_ms, kern_ms = [], []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        if r.decode:
+            e0, e1 = r.step_split()
+        else:
+            r.step()
+        b.record()
+        torch.cuda.synchronize()
+        step_ms.append(a.elapsed_time(b))
+        kern_ms.append(e0.elapsed_time(e1) if r.decode else step_ms[-1])
+    st = r.fa.fa_get_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after timing")
+    return step_ms, kern_ms
+
+
+def time_e2e(r: Runner, steps: int, warmup: int):
+    """Public API end to end: pinned host inputs -> H2D, fa_fwd, O and LSE -> host."""
+    torch, fa = r.torch, r.fa
+    w = r.w
+    hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory()
+    hk = torch.from_numpy(np.ascontiguousarray(w.k).view(np.int16)).pin_memory()
+    hv = torch.from_numpy(np.ascontiguousarray(w.v).view(np.int16)).pin_memory()
+    ho = torch.empty(r.out.shape, dtype=torch.int16).pin_memory()
+    hl = torch.empty(r.lse.shape, dtype=torch.float32).pin_memory()
+    dq = r.q.view(torch.int16)
+    dk = r.k.view(torch.int16)
+    dv = r.v.view(torch.int16)
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    d2h = ho.numel() * 2 + hl.numel() * 4
+
+    def one():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        fa.fa_fwd(r.q, r.k, r.v, out=r.out, lse=r.lse, workspace=r.ws, **r.kw, **r.extra)
+        ho.copy_(r.out.view(torch.int16), non_blocking=True)
+        hl.copy_(r.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+# --------------------------------------------------------------- CPU oracle ---
+def oracle_sample(w, budget_s: float, max_pairs=None):
+    """Time the fp64 oracle on whole (sequence, head) pairs until ~budget_s.
+
+    Returns (work units done, seconds, description)."""
+    import oracle
+    seqs = oracle.sequences(w.q.shape, w.k.shape, w.cu_seqlens_q, w.cu_seqlens_k, w.seqused_k)
+    r = w.num_heads_q // w.num_heads_kv
+    done_work, t_total, pairs = 0.0, 0.0, 0
+    order = [(b, h) for b in range(len(seqs)) for h in range(w.num_heads_q)]
+    for b, h in order:
+        s = seqs[b]
+        if s.sq == 0:
+            continue
+        if w.varlen:
+            q = w.q[s.q_start:s.q_start + s.sq, h][:, None, None, :].transpose(1, 0, 2, 3)
+            k = w.k[s.k_start:s.k_start + s.sk, h // r][None, :, None, :]
+            v = w.v[s.k_start:s.k_start + s.sk, h // r][None, :, None, :]
+        else:
+            q = w.q[b:b + 1, :, h:h + 1]
+            k = w.k[b:b + 1, :s.sk, h // r:h // r + 1]
+            v = w.v[b:b + 1, :s.sk, h // r:h // r + 1]
+        t0 = time.perf_counter()
+        oracle.attention_forward(q, k, v, scale=w.softmax_scale, causal=w.causal, window_left=w.window_left,
+                                 window_right=w.window_right)
+        t_total += time.perf_counter() - t0
+        pairs += 1
+        if is_decode(w.name):
+            done_work += s.sq * w.head_dim_qk * 2 + s.sk * (w.head_dim_qk + w.head_dim_v) * 2 / r + \
+                s.sq * (w.head_dim_v * 2 + 4)
+        else:
+            done_work += 2.0 * (w.head_dim_qk + w.head_dim_v) * visible_pairs(
+                s.sq, s.sk, w.causal, w.window_left, w.window_right)
+        if t_total >= budget_s or (max_pairs and pairs >= max_pairs):
+            break
+    desc = f"{pairs} (sequence, q-head) pairs of the {w.name} workload, full rows, fp64"
+    return done_work, t_total, desc
+
+
+def unit_of(name):
+    return "GB/s" if is_decode(name) else "TFLOP/s"
+
+
+def rate(work, ms, name):
+    return work / (ms * 1e-3) / (1e9 if is_decode(name) else 1e12)
+
+
+# -------------------------------------------------------------------- main ----
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="causal", choices=list(inputs.WORKLOADS))
+    ap.add_argument("--only", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    flush = l2_flush_buffer(torch, dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode")
+                                                      if n != args.workload])
+    results = {}
+    clocks = None
+    for n in names:
+        r = Runner(n, dev)
+        primary = n == args.workload
+        sampler = ClockSampler(local_rank) if primary else None
+        barrier()
+        if sampler:
+            sampler.start()
+        step_ms, kern_ms = time_steps(r, args.steps, args.warmup, flush)
+        barrier()
+        if sampler:
+            clocks = sampler.stop()
+        total_ms = max_over_ranks(sum(step_ms))
+        ms_step = total_ms / args.steps
+        kern_avg = max_over_ranks(sum(kern_ms) / len(kern_ms))
+        value = rate(r.work * world, ms_step, n)
+        if r.decode:
+            roof = {"bound": "hbm", "achieved": rate(r.work, kern_avg, n), "peak": peaks["hbm"], "unit": "GB/s"}
+        else:
+            roof = {"bound": "tensor", "achieved": rate(r.work, kern_avg, n), "peak": peaks["bf16"],
+                    "unit": "TFLOP/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["peak_source"] = peaks["source"] + (" (HBM copy)" if r.decode else " (dense bf16 burst)")
+        roof["traffic"] = None
+        res = {"value": value, "unit": unit_of(n), "ms_per_step": ms_step, "kernel_ms": kern_avg,
+               "work_per_step": r.work, "roofline": roof, "launches_per_step": r.launches_per_step,
+               "median_step_ms": statistics.median(step_ms)}
+        if r.decode:
+            res["num_splits"] = r.ns
+        if primary:
+            e2e_ms, h2d, d2h = time_e2e(r, max(3, args.steps // 4), 2)
+            e2e_ms = max_over_ranks(e2e_ms)
+            res["e2e"] = {"value": rate(r.work * world, e2e_ms, n), "unit": unit_of(n),
+                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        results[n] = res
+        del r
+        torch.cuda.empty_cache()
+
+    p = results[args.workload]
+    w0 = inputs.workload(args.workload)
+    cpu = None
+    if rank == 0:
+        work, secs, desc = oracle_sample(w0, args.cpu_budget)
+        cpu = {"value": rate(work, secs * 1e3, args.workload), "unit": unit_of(args.workload),
+               "cores": os.cpu_count(), "kind": "oracle", "sample": desc, "seconds": secs}
+    if rank == 0:
+        metric = ("attn fwd TFLOP/s (prefill, causal GQA B=2 Hq=32 Hkv=4 S=4096 D=128)"
+                  if not is_decode(args.workload) else "split-KV decode KV GB/s")
+        line = {
+            "metric": metric,
+            "value": p["value"],
+            "unit": p["unit"],
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": p["ms_per_step"],
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, numpy PCG64)",
+            "config": {"workload": args.workload, "shape": workload_desc(w0), "l2": "flushed between steps",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": p["roofline"],
+            "cpu_baseline": cpu,
+            "e2e": p["e2e"],
+            "gpu_launches": p["launches_per_step"] * args.steps,
+            "clocks": clocks,
+            "workloads": {n: {k: v for k, v in res.items() if k != "e2e"} for n, res in results.items()
+                          if n != args.workload},
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def workload_desc(w):
+    d = {"Hq": w.num_heads_q, "Hkv": w.num_heads_kv, "Dqk": w.head_dim_qk, "Dv": w.head_dim_v,
+         "causal": w.causal, "window": [w.window_left, w.window_right], "scale": w.softmax_scale}
+    if w.varlen:
+        d.update(batch=w.batch, total_q=int(w.cu_seqlens_q[-1]), varlen=True)
+    else:
+        d.update(batch=w.batch, seqlen_q=w.seqlen_q, seqlen_k=w.seqlen_k)
+    if w.seqused_k is not None:
+        d["seqused_k"] = "uniform [1024, 16384], seeded"
+    return d
+
+
+def run_reference(args):
+    """The fp64 CPU oracle on the host cores, one bounded sample per step."""
+    w = inputs.workload(args.workload)
+    per_step_budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step_budget, max_pairs=1)
+    works, secs = 0.0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        wk, s, desc = oracle_sample(w, per_step_budget, max_pairs=1)
+        works += wk
+        secs += s
+    value = rate(works, secs * 1e3, args.workload)
+    line = {
+        "impl": "reference",
+        "metric": ("attn fwd TFLOP/s (prefill, causal GQA B=2 Hq=32 Hkv=4 S=4096 D=128)"
+                   if not is_decode(args.workload) else "split-KV decode KV GB/s"),
+        "value": value,
+        "unit": unit_of(args.workload),
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": secs * 1e3 / max(1, args.steps),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16, numpy PCG64)",
+        "config": {"workload": args.workload, "shape": workload_desc(w)},
+        "cpu_baseline": {"value": value, "unit": unit_of(args.workload), "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": value, "unit": unit_of(args.workload), "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
