@@ -80,7 +80,7 @@ def decode_bytes(w) -> float:
 
 
 def is_decode(name):
-    return name == "decode"
+    return name.startswith("decode")
 
 
 # ------------------------------------------------------------------- peaks ----

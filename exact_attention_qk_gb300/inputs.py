@@ -172,7 +172,10 @@ def workload(name: str) -> Workload:
                       window_left=1024, window_right=0)
     if name == "decode":
         return batched("decode", 5, 64, 1, 16384, 32, 8, 128, 128, seqused_k=decode_seqused())
+    if name == "decode_small":
+        # the decode shape with 16 sequences (about 1 GB of cache): a profiling case
+        return batched("decode_small", 5, 16, 1, 16384, 32, 8, 128, 128, seqused_k=decode_seqused()[:16])
     raise KeyError(name)
 
 
-WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode")
+WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode", "decode_small")
