@@ -284,6 +284,26 @@ int run_prefill(const fa_fwd_args* a, const Resolved& r, void* ws, const WsLayou
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// Scratch for fa_fwd_decode_noalloc: split partials of callers that cannot
+// allocate. One copy per device that loads the library; shared by every call.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in for it).
+void* noalloc_scratch_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  static void* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
 bool no_work(const fa_fwd_args* a, const Resolved& r) {
   if (a->batch == 0) return true;
   if (r.varlen) return a->total_q == 0;
@@ -411,6 +431,32 @@ int fa_combine(const float* out_partial, const float* lse_partial, int num_split
   p.total_q = varlen ? total_q : 0;
   cudaError_t e = launch_combine(p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd_decode_noalloc(const fa_fwd_args* a, void* stream) {
+  Resolved r;
+  int rc = check_args(a, &r);
+  if (rc != FA_OK) return rc;
+  if (no_work(a, r)) return FA_OK;
+  rc = check_tensors(a, true);
+  if (rc != FA_OK) return rc;
+  const int ns = resolve_splits(a, r, 0);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (ns <= 1) return run_decode(a, r, 1, nullptr, nullptr, st);
+  const size_t rows = r.varlen ? static_cast<size_t>(a->total_q)
+                               : static_cast<size_t>(a->batch) * static_cast<size_t>(a->seqlen_q);
+  const size_t obytes = align256(sizeof(float) * ns * rows * a->num_heads_q * a->head_dim_v);
+  const size_t lbytes = align256(sizeof(float) * ns * rows * a->num_heads_q);
+  if (obytes + lbytes > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  char* base = static_cast<char*>(noalloc_scratch_ptr());
+  if (!base) return FA_ERR_CUDA;
+  float* opart = reinterpret_cast<float*>(base);
+  float* lpart = reinterpret_cast<float*>(base + obytes);
+  rc = run_decode(a, r, ns, opart, lpart, st);
+  if (rc != FA_OK) return rc;
+  return fa_combine(opart, lpart, ns, a->batch, r.varlen ? 0 : a->seqlen_q, a->num_heads_q, a->head_dim_v,
+                    a->cu_seqlens_q, r.varlen ? a->total_q : 0, a->out, a->o_batch_stride, a->o_row_stride,
+                    a->o_head_stride, a->lse, stream);
 }
 
 int fa_get_status(void* stream) {

@@ -81,6 +81,8 @@ _lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
 _lib.fa_set_wait_timeout_ns.restype = None
 _lib.fa_status_string.argtypes = [ctypes.c_int]
 _lib.fa_status_string.restype = ctypes.c_char_p
+_lib.fa_fwd_decode_noalloc.argtypes = [_P, _vp]
+_lib.fa_fwd_decode_noalloc.restype = ctypes.c_int
 _lib.fa_abi_version.argtypes = []
 _lib.fa_abi_version.restype = ctypes.c_int
 
@@ -228,3 +230,18 @@ def fa_combine(out_partial, lse_partial, out=None, lse=None, *, cu_seqlens_q=Non
 
 def default_scale(head_dim_qk: int) -> float:
     return 1.0 / math.sqrt(head_dim_qk)
+
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def fa_fwd_decode_noalloc(q, k, v, out, lse=None, *, stream=None, **kw):
+    """Split-KV decode + combine with the library's fixed scratch (no workspace).
+
+    For callers that cannot allocate device memory at the call: `out` (and
+    `lse`, if wanted) must already exist. See fa.h for the limits and the
+    sharing rules of the scratch array.
+    """
+    args = make_args(q, k, v, out, lse, **kw)
+    _check(_lib.fa_fwd_decode_noalloc(ctypes.byref(args), _vp(_stream_handle(stream))), "fa_fwd_decode_noalloc")
+    return out, lse

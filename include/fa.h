@@ -153,6 +153,31 @@ int fa_combine(const float* out_partial, const float* lse_partial, int num_split
                void* out, int64_t o_batch_stride, int64_t o_row_stride, int64_t o_head_stride,
                float* lse, void* stream);
 
+/*
+ * fa_fwd_decode_noalloc - split-KV decode plus combine, like fa_fwd on a
+ * decode-shaped problem, but with no workspace argument: the fp32 split
+ * partials live in a fixed array inside the library (FA_NOALLOC_SCRATCH_BYTES
+ * per GPU, reserved when the library is loaded and held until the process
+ * exits). The pages have no counterpart of this entry point; it exists for
+ * callers that cannot allocate device memory at the point of the call, for
+ * example code running while its stream is captured into a CUDA graph (where
+ * cudaMalloc is not allowed), engines whose device memory is owned by another
+ * allocator they cannot reach, and latency-critical paths that must not take
+ * the driver's allocation locks or its implicit synchronisation.
+ * The caller still passes q/k/v/out/lse in args; args->num_splits is resolved as
+ * in fa_fwd. Problems whose partials (num_splits * rows * Hq * (head_dim_v + 1)
+ * floats) exceed the array return FA_ERR_WORKSPACE before anything is launched.
+ * No call allocates: it calls no cudaMalloc/cudaFree or allocating library routine.
+ * The first call on each device looks up the array's device address there (the
+ * device must be current); make that first call before any stream capture.
+ * Every call on a device shares the one array: calls whose work overlaps on the
+ * GPU (different streams without ordering between them) race and give wrong
+ * results. Nothing in the array needs clearing: each call writes every partial
+ * it later reads.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
+
 /* Bytes of workspace fa_fwd needs for args (with args->num_splits resolved as fa_fwd does). */
 size_t fa_workspace_size(const fa_fwd_args* args);
 
