@@ -205,17 +205,21 @@ __global__ void __launch_bounds__(kDecThreads)
   }
 
   // ---------------- compute warps ----------------
-  const int kk = lane & 15, hf = lane >> 4;
-  const int kw = warp * 16 + kk;                 // this lane's key inside a tile
+  // Lane = (key slot kq in 0..7, dim quarter qp in 0..3); each lane takes keys
+  // kq and kq + 8 of its warp's 16, so every q load feeds two keys. Products
+  // run as packed fp32 pairs (FFMA2); a 2-level shuffle sums the quarters.
+  const int kq = lane & 7, qp = lane >> 3;
+  const int kw0 = warp * 16 + kq, kw1 = kw0 + 8;   // keys inside a tile
   constexpr int E = C::E;
-  float o[NR][E];
+  constexpr int QCH = DK / 32;                     // 8-dim chunks per quarter
+  float2 o[NR][E / 2];
   float m_run[NR], l_run[NR];
 #pragma unroll
   for (int rr = 0; rr < NR; ++rr) {
     m_run[rr] = -INFINITY;
     l_run[rr] = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) o[rr][e] = 0.f;
+    for (int e = 0; e < E / 2; ++e) o[rr][e] = make_float2(0.f, 0.f);
   }
   float* pw = p_s + warp * 16 * NR;
   const int e0 = lane * E;                       // first output column of this lane
@@ -232,57 +236,78 @@ __global__ void __launch_bounds__(kDecThreads)
     const uint8_t* stage = smem + st * C::STAGE_BYTES;
     const int tkey0 = key_base + t * kTileKeys;
 
-    // ---- S = q K^T for this lane's key over its half of the dims ----
-    float acc[NR];
+    // ---- S = q K^T for two keys over this lane's quarter of the dims ----
+    float2 acc0[NR], acc1[NR];
 #pragma unroll
-    for (int rr = 0; rr < NR; ++rr) acc[rr] = 0.f;
+    for (int rr = 0; rr < NR; ++rr) {
+      acc0[rr] = make_float2(0.f, 0.f);
+      acc1[rr] = make_float2(0.f, 0.f);
+    }
 #pragma unroll
-    for (int c = 0; c < DK / 16; ++c) {
-      const int gc = hf * (DK / 16) + c;
-      const uint4 kv = *reinterpret_cast<const uint4*>(stage + (gc >> 3) * kBoxBytes + kw * 128 +
-                                                       (((gc & 7) ^ (kw & 7)) << 4));
-      float kf[8];
-      kf[0] = bf16lo_to_f32(kv.x); kf[1] = bf16hi_to_f32(kv.x);
-      kf[2] = bf16lo_to_f32(kv.y); kf[3] = bf16hi_to_f32(kv.y);
-      kf[4] = bf16lo_to_f32(kv.z); kf[5] = bf16hi_to_f32(kv.z);
-      kf[6] = bf16lo_to_f32(kv.w); kf[7] = bf16hi_to_f32(kv.w);
+    for (int c = 0; c < QCH; ++c) {
+      const int gc = qp * QCH + c;
+      const uint8_t* kb = stage + (gc >> 3) * kBoxBytes;
+      const uint4 ka = *reinterpret_cast<const uint4*>(kb + kw0 * 128 + (((gc & 7) ^ (kw0 & 7)) << 4));
+      const uint4 kc = *reinterpret_cast<const uint4*>(kb + kw1 * 128 + (((gc & 7) ^ (kw1 & 7)) << 4));
+      const float2 a0 = make_float2(bf16lo_to_f32(ka.x), bf16hi_to_f32(ka.x));
+      const float2 a1 = make_float2(bf16lo_to_f32(ka.y), bf16hi_to_f32(ka.y));
+      const float2 a2 = make_float2(bf16lo_to_f32(ka.z), bf16hi_to_f32(ka.z));
+      const float2 a3 = make_float2(bf16lo_to_f32(ka.w), bf16hi_to_f32(ka.w));
+      const float2 b0 = make_float2(bf16lo_to_f32(kc.x), bf16hi_to_f32(kc.x));
+      const float2 b1 = make_float2(bf16lo_to_f32(kc.y), bf16hi_to_f32(kc.y));
+      const float2 b2 = make_float2(bf16lo_to_f32(kc.z), bf16hi_to_f32(kc.z));
+      const float2 b3 = make_float2(bf16lo_to_f32(kc.w), bf16hi_to_f32(kc.w));
 #pragma unroll
       for (int rr = 0; rr < NR; ++rr) {
         const float4 qa = *reinterpret_cast<const float4*>(q_s + rr * DK + gc * 8);
         const float4 qb = *reinterpret_cast<const float4*>(q_s + rr * DK + gc * 8 + 4);
-        float a = acc[rr];
-        a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
-        a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
-        a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
-        a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
-        acc[rr] = a;
+        const float2 q0 = make_float2(qa.x, qa.y), q1 = make_float2(qa.z, qa.w);
+        const float2 q2 = make_float2(qb.x, qb.y), q3 = make_float2(qb.z, qb.w);
+        acc0[rr] = __ffma2_rn(q0, a0, acc0[rr]);
+        acc0[rr] = __ffma2_rn(q1, a1, acc0[rr]);
+        acc0[rr] = __ffma2_rn(q2, a2, acc0[rr]);
+        acc0[rr] = __ffma2_rn(q3, a3, acc0[rr]);
+        acc1[rr] = __ffma2_rn(q0, b0, acc1[rr]);
+        acc1[rr] = __ffma2_rn(q1, b1, acc1[rr]);
+        acc1[rr] = __ffma2_rn(q2, b2, acc1[rr]);
+        acc1[rr] = __ffma2_rn(q3, b3, acc1[rr]);
       }
     }
-    const int j = tkey0 + kw;
+    const int j0 = tkey0 + kw0, j1 = tkey0 + kw1;
+    float s0[NR], s1[NR];
 #pragma unroll
     for (int rr = 0; rr < NR; ++rr) {
-      acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], 16);
-      acc[rr] = (j >= lo[rr] && j <= hi[rr]) ? acc[rr] : -INFINITY;
+      float x0 = acc0[rr].x + acc0[rr].y, x1 = acc1[rr].x + acc1[rr].y;
+      x0 += __shfl_xor_sync(0xffffffffu, x0, 8);
+      x1 += __shfl_xor_sync(0xffffffffu, x1, 8);
+      x0 += __shfl_xor_sync(0xffffffffu, x0, 16);
+      x1 += __shfl_xor_sync(0xffffffffu, x1, 16);
+      s0[rr] = (j0 >= lo[rr] && j0 <= hi[rr]) ? x0 : -INFINITY;
+      s1[rr] = (j1 >= lo[rr] && j1 <= hi[rr]) ? x1 : -INFINITY;
     }
     // ---- online softmax over this warp's 16 keys (base 2) ----
 #pragma unroll
     for (int rr = 0; rr < NR; ++rr) {
-      float bm = acc[rr];
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+      float bm = fmaxf(s0[rr], s1[rr]);
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
       const float m_new = fmaxf(m_run[rr], bm);
-      float factor = 1.f, pv = 0.f;
+      float factor = 1.f, p0 = 0.f, p1 = 0.f;
       if (m_new != -INFINITY) {
         factor = ex2_approx(m_run[rr] - m_new);
-        pv = ex2_approx(acc[rr] - m_new);
+        p0 = ex2_approx(s0[rr] - m_new);
+        p1 = ex2_approx(s1[rr] - m_new);
       }
       m_run[rr] = m_new;
-      l_run[rr] = l_run[rr] * factor + pv;
+      l_run[rr] = l_run[rr] * factor + (p0 + p1);
+      const float2 f2 = make_float2(factor, factor);
 #pragma unroll
-      for (int e = 0; e < E; ++e) o[rr][e] *= factor;
-      if (hf == 0) pw[kk * NR + rr] = pv;
+      for (int e = 0; e < E / 2; ++e) o[rr][e] = __fmul2_rn(o[rr][e], f2);
+      if (qp == 0) {
+        pw[kq * NR + rr] = p0;
+        pw[(kq + 8) * NR + rr] = p1;
+      }
     }
     __syncwarp();
     // ---- O += P V over the keys this warp owns that exist ----
@@ -292,26 +317,27 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int k2 = kbeg; k2 < kend; ++k2) {
       const int key = warp * 16 + k2;
       const uint8_t* vp = stage + (C::KCH + vbox) * kBoxBytes + key * 128 + (((vch ^ (key & 7)) << 4) + vbyte);
-      float vf[E];
+      float2 vf[E / 2];
       if constexpr (E == 2) {
         const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
-        vf[0] = bf16lo_to_f32(w); vf[1] = bf16hi_to_f32(w);
+        vf[0] = make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
       } else if constexpr (E == 4) {
         const uint2 w = *reinterpret_cast<const uint2*>(vp);
-        vf[0] = bf16lo_to_f32(w.x); vf[1] = bf16hi_to_f32(w.x);
-        vf[2] = bf16lo_to_f32(w.y); vf[3] = bf16hi_to_f32(w.y);
+        vf[0] = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+        vf[1] = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
       } else {
         const uint4 w = *reinterpret_cast<const uint4*>(vp);
-        vf[0] = bf16lo_to_f32(w.x); vf[1] = bf16hi_to_f32(w.x);
-        vf[2] = bf16lo_to_f32(w.y); vf[3] = bf16hi_to_f32(w.y);
-        vf[4] = bf16lo_to_f32(w.z); vf[5] = bf16hi_to_f32(w.z);
-        vf[6] = bf16lo_to_f32(w.w); vf[7] = bf16hi_to_f32(w.w);
+        vf[0] = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
+        vf[1] = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+        vf[2] = make_float2(bf16lo_to_f32(w.z), bf16hi_to_f32(w.z));
+        vf[3] = make_float2(bf16lo_to_f32(w.w), bf16hi_to_f32(w.w));
       }
 #pragma unroll
       for (int rr = 0; rr < NR; ++rr) {
         const float pr = pw[k2 * NR + rr];
+        const float2 p2 = make_float2(pr, pr);
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[rr][e] = fmaf(pr, vf[e], o[rr][e]);
+        for (int e = 0; e < E / 2; ++e) o[rr][e] = __ffma2_rn(p2, vf[e], o[rr][e]);
       }
     }
     __syncwarp();
@@ -322,7 +348,7 @@ __global__ void __launch_bounds__(kDecThreads)
   float lsum[NR];
 #pragma unroll
   for (int rr = 0; rr < NR; ++rr) {
-    float l = hf == 0 ? l_run[rr] : 0.f;
+    float l = qp == 0 ? l_run[rr] : 0.f;
     l += __shfl_xor_sync(0xffffffffu, l, 16);
     l += __shfl_xor_sync(0xffffffffu, l, 8);
     l += __shfl_xor_sync(0xffffffffu, l, 4);
@@ -336,7 +362,10 @@ __global__ void __launch_bounds__(kDecThreads)
   for (int rr = 0; rr < NR; ++rr) {
     float* row = mg + (warp * NR + rr) * (DV + 2);
 #pragma unroll
-    for (int e = 0; e < E; ++e) row[e0 + e] = o[rr][e];
+    for (int e = 0; e < E / 2; ++e) {
+      row[e0 + 2 * e] = o[rr][e].x;
+      row[e0 + 2 * e + 1] = o[rr][e].y;
+    }
     if (lane == 0) {
       row[DV] = m_run[rr];
       row[DV + 1] = lsum[rr];
@@ -457,13 +486,13 @@ cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& mk, const CUt
 template <int DK, int DV>
 cudaError_t launch_decode_nr(const FwdParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                              cudaStream_t stream) {
+  // rows per CTA: up to 8 (more would spill the accumulators); larger row
+  // counts are split into chunks of 8 over grid.y
   const int rows = p.max_seqlen_q * p.r;
-  constexpr int NRMAX = (DV == 256) ? 8 : 16;
   if (rows <= 1) return launch_decode_t<DK, DV, 1>(p, mk, mv, stream);
   if (rows <= 2) return launch_decode_t<DK, DV, 2>(p, mk, mv, stream);
   if (rows <= 4) return launch_decode_t<DK, DV, 4>(p, mk, mv, stream);
-  if (rows <= 8 || NRMAX == 8) return launch_decode_t<DK, DV, 8>(p, mk, mv, stream);
-  return launch_decode_t<DK, DV, NRMAX>(p, mk, mv, stream);
+  return launch_decode_t<DK, DV, 8>(p, mk, mv, stream);
 }
 
 }  // namespace

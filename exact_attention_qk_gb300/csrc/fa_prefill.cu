@@ -59,10 +59,15 @@ struct PrefillCfg {
   // at least half the SM's shared memory, so one CTA (the one that owns all
   // 512 TMEM columns) is resident per SM
   static constexpr int SMEM = (SMEM_USED + 1024 < 120 * 1024) ? 120 * 1024 : SMEM_USED + 1024;
+  // warpgroups: NSM softmax warpgroups, then one holding the MMA warp, the two
+  // TMA warps and one idle warp (whole warpgroups, for setmaxnreg)
   static constexpr int MMA_WARP = 4 * NSM;
   static constexpr int TMA_QK_WARP = MMA_WARP + 1;
   static constexpr int TMA_V_WARP = MMA_WARP + 2;
-  static constexpr int THREADS = 32 * (MMA_WARP + 3);
+  static constexpr int THREADS = 32 * 4 * (NSM + 1);
+  // register split (NQ == 2): 256 x 200 + 128 x 104 (or 256 x 192 + 128 x 120) = 384 x 168 at launch
+  static constexpr int REG_SOFTMAX = (DK == 192) ? 192 : 200;
+  static constexpr int REG_OTHER = (DK == 192) ? 120 : 104;
   static constexpr int ROWS_PER_TILE = NQ * kBM;
   static constexpr int O_COL = 256;
   static_assert(NQ == 2 ? (256 + 2 * DV <= 512) : (256 + DV <= 512), "TMEM budget");
@@ -205,9 +210,9 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       mbar_init(&B.q_full[i], 1);
       mbar_init(&B.q_empty[i], 1);
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.p_full[i], kBM);
+      mbar_init(&B.p_full[i], 4);      // one arrival per softmax warp
       mbar_init(&B.o_bar[i], 1);
-      mbar_init(&B.o_empty[i], kBM);
+      mbar_init(&B.o_empty[i], 4);
     }
     for (int i = 0; i < Cfg::KST; ++i) {
       mbar_init(&B.k_full[i], 1);
@@ -230,7 +235,9 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitGuard guard{abort_flag, p.status, p.timeout_ns};
-
+  if (warp >= Cfg::MMA_WARP) {
+  // the warpgroup of the MMA, TMA and idle warps gives registers away ...
+  if constexpr (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::REG_OTHER));
   if (warp == Cfg::TMA_QK_WARP || warp == Cfg::TMA_V_WARP) {
     // ================= TMA producers =================
     if (lane == 0) {
@@ -375,13 +382,15 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           {
             const int n0 = nhi - 1, st = kc % Cfg::KST;
             if (!mbar_wait(&B.k_full[st], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
-            for (int s = 0; s < 2; ++s) {
-              if (!part(R[s], n0)) continue;
-              if (!wait_q(s)) { ok = false; break; }
+            auto first_s_of = [&](int s) -> bool {
+              if (!part(R[s], n0)) return true;
+              if (!wait_q(s)) return false;
               issue_s(s, s, st);
               mma_commit(&B.s_full[s]);
               if (n0 == R[s].nlo) mma_commit(&B.q_empty[s]);
-            }
+              return true;
+            };
+            ok = first_s_of(0) && first_s_of(1);
             if (!ok) break;
             mma_commit(&B.k_empty[st]);
             ++kc;
@@ -392,27 +401,30 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             const bool has_next = n - 1 >= nlo;
             const int kst = kc % Cfg::KST;
             bool k_ready = false;
-            for (int s = 0; s < 2; ++s) {
+            // P.V of this block for Q tile s, then S of the next block for it
+            auto pv_then_s = [&](int s) -> bool {
               if (part(R[s], n)) {
-                if (!mbar_wait(&B.p_full[s], pw[s] & 1, guard)) { ok = false; break; }
+                if (!mbar_wait(&B.p_full[s], pw[s] & 1, guard)) return false;
                 ++pw[s];
                 tc_fence_after();
                 const bool acc = !first_pv[s];
-                if (!before_pv(s)) { ok = false; break; }
+                if (!before_pv(s)) return false;
                 issue_pv(s, s, vst, acc);
                 mma_commit(&B.o_bar[s]);
               }
               if (has_next && part(R[s], n - 1)) {
                 if (!k_ready) {
-                  if (!mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
+                  if (!mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) return false;
                   k_ready = true;
                 }
-                if (!wait_q(s)) { ok = false; break; }
+                if (!wait_q(s)) return false;
                 issue_s(s, s, kst);
                 mma_commit(&B.s_full[s]);
                 if (n - 1 == R[s].nlo) mma_commit(&B.q_empty[s]);
               }
-            }
+              return true;
+            };
+            ok = pv_then_s(0) && pv_then_s(1);
             if (!ok) break;
             mma_commit(&B.v_empty[vst]);
             ++vc;
@@ -442,8 +454,9 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             const int slot = (jc + i) & 1;
             const int vst = vc % Cfg::VST;
             if (!mbar_wait(&B.v_full[vst], (vc / Cfg::VST) & 1, guard)) { ok = false; break; }
-            if (!mbar_wait(&B.p_full[slot], pw[slot] & 1, guard)) { ok = false; break; }
-            ++pw[slot];
+            const uint32_t pwc = slot ? pw[1] : pw[0];
+            if (!mbar_wait(&B.p_full[slot], pwc & 1, guard)) { ok = false; break; }
+            if (slot) ++pw[1]; else ++pw[0];
             tc_fence_after();
             const bool acc = i > 0;
             if (!before_pv(0)) { ok = false; break; }
@@ -461,14 +474,17 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       drain_wait(B.drain, 0, p.timeout_ns);
     }
     __syncwarp();
+  }
   } else {
+    // ... and the softmax warpgroups take them
+    if constexpr (NQ == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::REG_SOFTMAX));
     // ================= softmax warpgroups =================
     const int wg = warp >> 2;                 // Q tile (NQ == 2) or 0
     const int row_local = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int o_idx = (NQ == 2) ? wg : 0;
     const uint32_t o_addr = tmem + lane_off + Cfg::O_COL + o_idx * DV;
-    uint32_t sw[2] = {0, 0};   // S waits per slot
+    uint32_t sw0 = 0, sw1 = 0;  // S waits per slot
     uint32_t ow = 0;           // o_bar phases consumed (one per P.V of this O, in order)
     uint32_t jc = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -497,8 +513,8 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       float m = -INFINITY, l = 0.f;
       for (int n = R.nhi - 1; n >= R.nlo; --n) {
         const int slot = (NQ == 2) ? wg : (jc & 1);
-        if (!mbar_wait(&B.s_full[slot], sw[slot] & 1, guard)) { ok = false; break; }
-        ++sw[slot];
+        if (!mbar_wait(&B.s_full[slot], (slot ? sw1 : sw0) & 1, guard)) { ok = false; break; }
+        if (slot) ++sw1; else ++sw0;
         tc_fence_after();
         uint32_t r[128];
         tmem_ld128(tmem + lane_off + slot * 128, r);
@@ -511,15 +527,17 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < c_lo || c > c_hi) ? -INFINITY : s[c];
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // row max: eight independent chains of 3-input max
+        float mx[8];
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int j = 0; j < 8; ++j) mx[j] = s[j];
+#pragma unroll
+        for (int c = 8; c < 128; c += 16) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mx[j] = fmax3(mx[j], s[c + j], s[c + 8 + j]);
         }
-        const float bmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+        const float bmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+                           p.scale_log2;
         const float m_new = fmaxf(m, bmax);
         // The previous P.V of this O (if any in this tile) has a phase on o_bar
         // that is consumed exactly once: before O is rescaled, or else just
@@ -551,19 +569,20 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           }
         }
         const float mu = (m == -INFINITY) ? 0.f : m;
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm2 = make_float2(-mu, -mu);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          s[c] = ex2_approx(fmaf(s[c], p.scale_log2, -mu));
-          s[c + 1] = ex2_approx(fmaf(s[c + 1], p.scale_log2, -mu));
-          s[c + 2] = ex2_approx(fmaf(s[c + 2], p.scale_log2, -mu));
-          s[c + 3] = ex2_approx(fmaf(s[c + 3], p.scale_log2, -mu));
-          l0 += s[c];
-          l1 += s[c + 1];
-          l2 += s[c + 2];
-          l3 += s[c + 3];
+        for (int c = 0; c < 128; c += 2) {
+          const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+          s[c] = ex2_approx(x.x);
+          s[c + 1] = ex2_approx(x.y);
+          acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
         }
-        l += (l0 + l1) + (l2 + l3);
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        l += a.x + a.y;
 #pragma unroll
         for (int c = 0; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
         tmem_st64(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[64]>(r));
@@ -573,7 +592,8 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           ++ow;
         }
         tc_fence_before();
-        mbar_arrive(&B.p_full[slot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.p_full[slot]);
         ++jc;
       }
       if (!ok) break;
@@ -601,7 +621,8 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       }
       if (valid && p.lse) p.lse[lrow] = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
       tc_fence_before();
-      mbar_arrive(&B.o_empty[o_idx]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.o_empty[o_idx]);
     }
   }
 
