@@ -54,7 +54,8 @@ struct PrefillCfg {
   static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KST * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + VST * V_BYTES;
-  static constexpr int NBAR = 2 * 2 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2 + 1;
+  static constexpr int REL = (KST > VST) ? KST : VST;
+  static constexpr int NBAR = 2 * 2 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2 + REL + 1;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // at least half the SM's shared memory, so one CTA (the one that owns all
   // 512 TMEM columns) is resident per SM
@@ -160,6 +161,7 @@ struct Bars {
   uint64_t* p_full;    // [2] per S slot
   uint64_t* o_bar;     // [2] per O: one phase per P.V
   uint64_t* o_empty;   // [2] per O: epilogue done reading
+  uint64_t* kv_rel;    // [REL] NQ == 2: K and V of a block released together
   uint64_t* drain;
 };
 
@@ -177,6 +179,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   B.p_full = b; b += 2;
   B.o_bar = b; b += 2;
   B.o_empty = b; b += 2;
+  B.kv_rel = b; b += Cfg::REL;
   B.drain = b; b += 1;
   return B;
 }
@@ -222,6 +225,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       mbar_init(&B.v_full[i], 1);
       mbar_init(&B.v_empty[i], 1);
     }
+    for (int i = 0; i < Cfg::REL; ++i) mbar_init(&B.kv_rel[i], 1);
     mbar_init(B.drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -250,6 +254,16 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       }
       uint32_t kc = 0, qc[2] = {0, 0};
       bool ok = true;
+      // Block j's K and V tiles may be overwritten once block j is released:
+      // NQ == 2 releases K(j) and V(j) together (one commit, barrier ring of
+      // REL slots); NQ == 1 releases K and V separately on their own rings.
+      auto wait_release = [&](uint32_t j, uint64_t* own_ring, int own_depth) -> bool {
+        if constexpr (NQ == 2) {
+          return mbar_wait(&B.kv_rel[j % Cfg::REL], (j / Cfg::REL) & 1, guard);
+        } else {
+          return mbar_wait(&own_ring[j % own_depth], (j / own_depth) & 1, guard);
+        }
+      };
       for (int t = blockIdx.x; ok; t += gridDim.x) {
         Tile T;
         if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, t, T)) break;
@@ -279,7 +293,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           }
           for (int n = nhi - 1; ok && n >= nlo; --n) {
             const int st = kc % Cfg::KST;
-            if (kc >= Cfg::KST && !mbar_wait(&B.k_empty[st], ((kc / Cfg::KST) - 1) & 1, guard)) { ok = false; break; }
+            if (kc >= Cfg::KST && !wait_release(kc - Cfg::KST, B.k_empty, Cfg::KST)) { ok = false; break; }
             uint8_t* dst = smem + Cfg::OFF_K + st * Cfg::K_BYTES;
             mbar_arrive_expect_tx(&B.k_full[st], Cfg::K_BYTES);
 #pragma unroll
@@ -290,7 +304,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         } else {
           for (int n = nhi - 1; ok && n >= nlo; --n) {
             const int st = kc % Cfg::VST;
-            if (kc >= Cfg::VST && !mbar_wait(&B.v_empty[st], ((kc / Cfg::VST) - 1) & 1, guard)) { ok = false; break; }
+            if (kc >= Cfg::VST && !wait_release(kc - Cfg::VST, B.v_empty, Cfg::VST)) { ok = false; break; }
             uint8_t* dst = smem + Cfg::OFF_V + st * Cfg::V_BYTES;
             mbar_arrive_expect_tx(&B.v_full[st], Cfg::V_BYTES);
 #pragma unroll
@@ -323,26 +337,30 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       const uint32_t v_base = smem_u32(smem + Cfg::OFF_V);
 
       // S[slot] = Q[qs] K[kst]^T, K-major operands, 16 deep per instruction
+      // Descriptors are built once per operand; a K step only moves the start
+      // address, which lives in the low bits (no carry: addresses < 256 KB).
       auto issue_s = [&](int qs, int slot, int kst) {
         const uint32_t d = tmem + slot * 128;
-        const uint32_t qa = q_base + qs * Cfg::Q_BYTES, ka = k_base + kst * Cfg::K_BYTES;
+        const uint64_t qd = sdesc_sw128(q_base + qs * Cfg::Q_BYTES, 16, 1024);
+        const uint64_t kd = sdesc_sw128(k_base + kst * Cfg::K_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DK / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-          mma_bf16_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), IDESC_S, kk > 0);
+          const uint32_t off = ((kk >> 2) * kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(d, qd + off, kd + off, IDESC_S, kk > 0);
         }
       };
       // O[o] (+)= P[slot] V[vst]; P from TMEM, V MN-major (64-column chunks 16 KB apart)
       auto issue_pv = [&](int o, int slot, int vst, bool acc) {
         const uint32_t d = tmem + Cfg::O_COL + o * DV;
-        const uint32_t va = v_base + vst * Cfg::V_BYTES;
+        const uint64_t vd = sdesc_sw128(v_base + vst * Cfg::V_BYTES, kChunkBytes, 1024);
+        const uint32_t pa = tmem + slot * 128;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ts(d, tmem + slot * 128 + kk * 8, sdesc_sw128(va + kk * 16 * 128, kChunkBytes, 1024), IDESC_PV,
-                      (kk > 0 || acc) ? 1u : 0u);
+          mma_bf16_ts(d, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
       };
 
       uint32_t kc = 0, vc = 0, qw[2] = {0, 0}, pw[2] = {0, 0}, ou[2] = {0, 0};
+      uint32_t rel = 0;   // NQ == 2: blocks released so far
       uint32_t jc = 0;   // NQ == 1: jobs so far (S slot = job parity)
       bool ok = true;
       for (int t = blockIdx.x; ok; t += gridDim.x) {
@@ -392,7 +410,6 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             };
             ok = first_s_of(0) && first_s_of(1);
             if (!ok) break;
-            mma_commit(&B.k_empty[st]);
             ++kc;
           }
           for (int n = nhi - 1; n >= nlo; --n) {
@@ -410,7 +427,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
                 const bool acc = !first_pv[s];
                 if (!before_pv(s)) return false;
                 issue_pv(s, s, vst, acc);
-                mma_commit(&B.o_bar[s]);
+                if (n == R[s].nlo) mma_commit(&B.o_bar[s]);   // O[s] complete for this tile
               }
               if (has_next && part(R[s], n - 1)) {
                 if (!k_ready) {
@@ -426,11 +443,12 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             };
             ok = pv_then_s(0) && pv_then_s(1);
             if (!ok) break;
-            mma_commit(&B.v_empty[vst]);
+            // every MMA reading K(n) and V(n) is issued: release block n
+            mma_commit(&B.kv_rel[rel % Cfg::REL]);
+            ++rel;
             ++vc;
             if (has_next) {
               if (!k_ready && !mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
-              mma_commit(&B.k_empty[kst]);
               ++kc;
             }
           }
@@ -542,15 +560,19 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         // The previous P.V of this O (if any in this tile) has a phase on o_bar
         // that is consumed exactly once: before O is rescaled, or else just
         // before this block's P is published (so the next P.V cannot run ahead).
-        bool pending = n != R.nhi - 1;
+        // NQ == 1 only: with NQ == 2, S(n) completing implies every earlier
+        // P.V of this O completed (same issuing thread, issued before it).
+        bool pending = (NQ == 1) && (n != R.nhi - 1);
         if (n == R.nhi - 1) {
           m = m_new;
         } else {
           const bool need = m_new > m + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
-            if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) { ok = false; break; }
-            ++ow;
-            pending = false;
+            if (NQ == 1) {
+              if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) { ok = false; break; }
+              ++ow;
+              pending = false;
+            }
             tc_fence_after();
             const float f = need ? ex2_approx(m - m_new) : 1.f;
 #pragma unroll 1
