@@ -87,6 +87,14 @@ struct Range {
   int nlo, nhi; // key blocks [nlo, nhi) hold visible keys; empty when nhi <= nlo
 };
 
+// The k-th tile of this CTA in a persistent grid: tiles are sorted longest
+// first, and the CTA order reverses every round ("snake"), so a CTA that got a
+// long tile in one round gets a short one in the next.
+__device__ __forceinline__ int tile_of(int k) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return k * g + ((k & 1) ? g - 1 - c : c);
+}
+
 template <int ROWS_PER_TILE>
 __device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
   if (p.cu_seqlens_q == nullptr) {
@@ -264,9 +272,9 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           return mbar_wait(&own_ring[j % own_depth], (j / own_depth) & 1, guard);
         }
       };
-      for (int t = blockIdx.x; ok; t += gridDim.x) {
+      for (int k = 0; ok; ++k) {
         Tile T;
-        if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, t, T)) break;
+        if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, tile_of(k), T)) break;
         Range R[NQ];
         int nlo = INT32_MAX, nhi = INT32_MIN;
 #pragma unroll
@@ -363,9 +371,9 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       uint32_t rel = 0;   // NQ == 2: blocks released so far
       uint32_t jc = 0;   // NQ == 1: jobs so far (S slot = job parity)
       bool ok = true;
-      for (int t = blockIdx.x; ok; t += gridDim.x) {
+      for (int k = 0; ok; ++k) {
         Tile T;
-        if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, t, T)) break;
+        if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, tile_of(k), T)) break;
         Range R[NQ];
         int nlo = INT32_MAX, nhi = INT32_MIN;
 #pragma unroll
@@ -507,9 +515,9 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
     uint32_t jc = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
     bool ok = true;
-    for (int t = blockIdx.x; ok; t += gridDim.x) {
+    for (int k = 0; ok; ++k) {
       Tile T;
-      if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, t, T)) break;
+      if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, tile_of(k), T)) break;
       const Range R = stage_range(p, T, T.mb * Cfg::ROWS_PER_TILE + wg * kBM);
       if (!R.active) continue;
       const int i = R.r0 + row_local;
@@ -550,10 +558,12 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) mx[j] = s[j];
 #pragma unroll
-        for (int c = 8; c < 128; c += 16) {
+        for (int c = 8; c + 16 <= 128; c += 16) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) mx[j] = fmax3(mx[j], s[c + j], s[c + 8 + j]);
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], s[120 + j]);
         const float bmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
                            p.scale_log2;
         const float m_new = fmaxf(m, bmax);
