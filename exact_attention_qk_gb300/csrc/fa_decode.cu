@@ -8,11 +8,12 @@
 //     that share a KV head are packed as rows of one CTA (the triton page's
 //     head-swapping trick), so K/V bytes are read once per KV head;
 //   * a producer warp streams 64-key K/V tiles with TMA (128-byte swizzle) into
-//     an NSTAGE-deep mbarrier ring; cache rows at or past seqused_k are never
-//     used in arithmetic;
+//     a 2-deep mbarrier ring (three CTAs per SM keep enough bytes in flight);
+//     cache rows at or past seqused_k are never used in arithmetic;
 //   * four compute warps take 16 keys each per tile: QK^T with 16-byte swizzled
-//     shared loads (conflict-free), online softmax in base 2 with the scale
-//     folded into q, and P.V with per-lane output columns;
+//     shared loads (conflict-free), two keys per lane so each q load feeds both,
+//     packed fp32 FMA (FFMA2), online softmax in base 2 with the scale folded
+//     into q, and P.V with per-lane output columns;
 //   * the four warps' (m, l, O) states merge in shared memory at the end and the
 //     CTA writes either the final bf16 O / fp32 LSE or the fp32 split partials.
 #include <cuda_bf16.h>
@@ -33,7 +34,10 @@ struct DecodeCfg {
   static constexpr int KCH = DK / 64;
   static constexpr int VCH = DV / 64;
   static constexpr int STAGE_BYTES = (KCH + VCH) * kBoxBytes;
-  static constexpr int NSTAGE = (STAGE_BYTES <= 32768) ? 3 : 2;
+  // Two stages keep the CTA under 70 KB of shared memory, so three CTAs (12
+  // compute warps) share an SM: the QK / softmax / PV chains are latency-bound
+  // and need the extra warps more than each CTA needs a deeper ring.
+  static constexpr int NSTAGE = 2;
   static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
   static constexpr int Q_BYTES = NR * DK * 4;
   static constexpr int P_BYTES = kDecWarps * 16 * NR * 4;
@@ -48,7 +52,7 @@ struct DecodeCfg {
 };
 
 template <int DK, int DV, int NR>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                   const FwdParams p) {
   using C = DecodeCfg<DK, DV, NR>;
@@ -314,7 +318,7 @@ __global__ void __launch_bounds__(kDecThreads)
     const int wkey0 = tkey0 + warp * 16;
     const int kbeg = max(0, klo - wkey0);
     const int kend = min(16, key_end - wkey0);
-    for (int k2 = kbeg; k2 < kend; ++k2) {
+    auto pv_key = [&](int k2) {
       const int key = warp * 16 + k2;
       const uint8_t* vp = stage + (C::KCH + vbox) * kBoxBytes + key * 128 + (((vch ^ (key & 7)) << 4) + vbyte);
       float2 vf[E / 2];
@@ -339,6 +343,13 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
         for (int e = 0; e < E / 2; ++e) o[rr][e] = __ffma2_rn(p2, vf[e], o[rr][e]);
       }
+    };
+    if (kbeg == 0 && kend == 16) {
+      // all 16 keys exist (the common case): unrolled so the shared loads overlap
+#pragma unroll 4
+      for (int k2 = 0; k2 < 16; ++k2) pv_key(k2);
+    } else {
+      for (int k2 = kbeg; k2 < kend; ++k2) pv_key(k2);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
