@@ -83,6 +83,35 @@ def is_decode(name):
     return name.startswith("decode")
 
 
+# ------------------------------------------------------------- ncu traffic ----
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources (a changed kernel invalidates old counters)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_qk_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the workload's dominant kernel from the committed
+    ncu summary, or None when that capture predates the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    e = d.get("workloads", {}).get(workload)
+    if not e or d.get("source_sha256") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
 # ------------------------------------------------------------------- peaks ----
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -419,7 +448,7 @@ def main():
                     "unit": "TFLOP/s"}
         roof["frac"] = roof["achieved"] / roof["peak"]
         roof["peak_source"] = peaks["source"] + (" (HBM copy)" if r.decode else " (dense bf16 burst)")
-        roof["traffic"] = None
+        roof["traffic"] = measured_traffic(n)
         res = {"value": value, "unit": unit_of(n), "ms_per_step": ms_step, "kernel_ms": kern_avg,
                "work_per_step": r.work, "roofline": roof, "launches_per_step": r.launches_per_step,
                "median_step_ms": statistics.median(step_ms)}
