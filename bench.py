@@ -377,6 +377,23 @@ def rate(work, ms, name):
     return work / (ms * 1e-3) / (1e9 if is_decode(name) else 1e12)
 
 
+# ------------------------------------------------------- ranks (replicas) ----
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (the slowest replica sets the time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_rank: float, ms_per_step: float, world: int, name: str) -> float:
+    """Whole-job throughput: every rank processes its own replica of the workload."""
+    return rate(work_per_rank * world, ms_per_step, name)
+
+
 # -------------------------------------------------------------------- main ----
 def main():
     ap = argparse.ArgumentParser()
@@ -415,13 +432,6 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode")
                                                       if n != args.workload])
     results = {}
@@ -437,10 +447,10 @@ def main():
         barrier()
         if sampler:
             clocks = sampler.stop()
-        total_ms = max_over_ranks(sum(step_ms))
+        total_ms = max_over_ranks(sum(step_ms), world, dev)
         ms_step = total_ms / args.steps
-        kern_avg = max_over_ranks(sum(kern_ms) / len(kern_ms))
-        value = rate(r.work * world, ms_step, n)
+        kern_avg = max_over_ranks(sum(kern_ms) / len(kern_ms), world, dev)
+        value = job_rate(r.work, ms_step, world, n)
         if r.decode:
             roof = {"bound": "hbm", "achieved": rate(r.work, kern_avg, n), "peak": peaks["hbm"], "unit": "GB/s"}
         else:
@@ -456,8 +466,8 @@ def main():
             res["num_splits"] = r.ns
         if primary:
             e2e_ms, h2d, d2h = time_e2e(r, max(3, args.steps // 4), 2)
-            e2e_ms = max_over_ranks(e2e_ms)
-            res["e2e"] = {"value": rate(r.work * world, e2e_ms, n), "unit": unit_of(n),
+            e2e_ms = max_over_ranks(e2e_ms, world, dev)
+            res["e2e"] = {"value": job_rate(r.work, e2e_ms, world, n), "unit": unit_of(n),
                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
         results[n] = res
         del r
