@@ -3,6 +3,8 @@
 // descriptor or layout mistake shows up in isolation:
 //   fa_selftest_qk:  S[128x128] = Q[128xDK] K[128xDK]^T   (both K-major, SW128)
 //   fa_selftest_pv:  O[128xDV]  = P[128x128] V[128xDV]    (P from TMEM, V MN-major)
+//   fa_selftest_wait_timeout: the bounded mbarrier wait on a barrier nothing
+//                    arrives on gives up, reports and lets the CTA exit cleanly
 // Inputs are bf16 device arrays (row-major, contiguous); outputs fp32.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -176,9 +178,59 @@ __global__ void __launch_bounds__(128) pv_kernel(const __nv_bfloat16* p_in, cons
   }
 }
 
+// A wait that can never complete (nothing arrives on the barrier): the bounded
+// wait must give up after timeout_ns, set the status word, raise the shared
+// abort flag so the other waiting warp gives up too, and let the CTA free its
+// TMEM and exit. report[0] = 1 if warp 0's wait returned false, report[1] = 1 if
+// warp 1 saw the abort (its own wait returned false without timing out first).
+__global__ void __launch_bounds__(64, 1) never_kernel(int* status, int* report, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar_a, bar_b;
+  __shared__ uint32_t slot;
+  __shared__ volatile int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_a, 1);
+    mbar_init(&bar_b, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (lane == 0) {
+    if (warp == 0) {
+      const WaitGuard g{&abort_flag, status, timeout_ns};
+      report[0] = mbar_wait(&bar_a, 0, g) ? 0 : 1;
+    } else {
+      // a much longer limit: only the abort raised by warp 0 can end this wait early
+      int dummy = 0;
+      const WaitGuard g{&abort_flag, &dummy, timeout_ns * 1000ull};
+      const bool r = mbar_wait(&bar_b, 0, g);
+      report[1] = (!r && dummy == 0) ? 1 : 0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(slot, 32);
+  }
+}
+
 }  // namespace
 
 extern "C" {
+
+// Runs never_kernel; status and report are device ints (zeroed by the caller).
+int fa_selftest_wait_timeout(int* status, int* report, unsigned long long timeout_ns, void* stream) {
+  never_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(status, report, timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? 0 : 5;
+}
+
 
 // q, k: bf16 [128, dk] row-major; s: fp32 [128, 128]; status: device int (0 on entry)
 int fa_selftest_qk(const void* q, const void* k, int dk, float* s, int* status, void* stream) {

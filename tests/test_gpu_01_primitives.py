@@ -60,3 +60,21 @@ def test_pv_tile_p_from_tmem(st, dv):
     assert rc == 0 and status.item() == 0
     ref = pf @ vf
     np.testing.assert_allclose(o.cpu().numpy(), ref, rtol=0, atol=2e-2)
+
+
+def test_bounded_wait_gives_up_and_reports(st):
+    """A wait on a barrier nothing arrives on ends after its limit (2 ms here),
+    records the failure in the status word and makes the CTA's other waiters
+    give up as well; the kernel exits normally (no trap, no hang)."""
+    st.fa_selftest_wait_timeout.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    report = torch.zeros(2, dtype=torch.int32, device="cuda")
+    rc = st.fa_selftest_wait_timeout(status.data_ptr(), report.data_ptr(), 2_000_000,
+                                     torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert status.item() == 1                      # the timeout bit
+    assert report.tolist() == [1, 1]
+    # the context is still healthy afterwards
+    x = torch.ones(4, device="cuda")
+    assert (x + x).sum().item() == 8.0
