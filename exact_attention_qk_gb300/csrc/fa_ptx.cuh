@@ -59,6 +59,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, but the thread may be suspended (not spinning, so it takes no issue
+// slots from the warps doing work) until the phase completes or about
+// `hint_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared by every role of a CTA: a wait that runs out raises `abort` so that
 // the other roles stop waiting too, and records the failure in global memory.
 struct WaitGuard {
@@ -75,7 +90,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait_sleep(a, parity, 20000)) return true;
     if (*g.abort) return false;
     if (global_timer_ns() - t0 > g.timeout_ns) {
       *g.abort = 1;
