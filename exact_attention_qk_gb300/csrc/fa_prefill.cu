@@ -55,7 +55,7 @@ struct PrefillCfg {
   static constexpr int OFF_V = OFF_K + KST * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + VST * V_BYTES;
   static constexpr int REL = (KST > VST) ? KST : VST;
-  static constexpr int NBAR = 2 * 2 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2 + REL + 1;
+  static constexpr int NBAR = 2 * 2 + 2 * KST + 3 * VST + 2 + 2 + 2 + 2 + REL + 1;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // at least half the SM's shared memory, so one CTA (the one that owns all
   // 512 TMEM columns) is resident per SM
@@ -158,6 +158,20 @@ __device__ __forceinline__ bool needs_mask(const FwdParams& p, const Tile& T, co
   return !full;
 }
 
+// Block n is the last, partly filled key block of a sequence whose KV cache
+// has unused slots (seqused_k given, TAIL instances only): its V rows past the
+// sequence are cleared in shared memory before P.V, which stops at the next
+// 16-key boundary.
+template <bool TAIL>
+__device__ __forceinline__ bool tail_fix(const Tile& T, int n) {
+  return TAIL && T.sk - n * kBN < kBN;
+}
+
+template <bool TAIL>
+__device__ __forceinline__ int pv_steps(const Tile& T, int n) {
+  return tail_fix<TAIL>(T, n) ? (T.sk - n * kBN + 15) / 16 : kBN / 16;
+}
+
 struct Bars {
   uint64_t* q_full;    // [2]
   uint64_t* q_empty;   // [2]
@@ -165,6 +179,7 @@ struct Bars {
   uint64_t* k_empty;
   uint64_t* v_full;    // [VST]
   uint64_t* v_empty;
+  uint64_t* v_fixed;   // [VST] tail rows of the V tile cleared (seqused_k)
   uint64_t* s_full;    // [2] per S slot
   uint64_t* p_full;    // [2] per S slot
   uint64_t* o_bar;     // [2] per O: one phase per P.V
@@ -183,6 +198,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   B.k_empty = b; b += Cfg::KST;
   B.v_full = b; b += Cfg::VST;
   B.v_empty = b; b += Cfg::VST;
+  B.v_fixed = b; b += Cfg::VST;
   B.s_full = b; b += 2;
   B.p_full = b; b += 2;
   B.o_bar = b; b += 2;
@@ -201,7 +217,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool TAIL>
 __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapV, const FwdParams p) {
@@ -232,6 +248,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
     for (int i = 0; i < Cfg::VST; ++i) {
       mbar_init(&B.v_full[i], 1);
       mbar_init(&B.v_empty[i], 1);
+      mbar_init(&B.v_fixed[i], 1);
     }
     for (int i = 0; i < Cfg::REL; ++i) mbar_init(&B.kv_rel[i], 1);
     mbar_init(B.drain, 1);
@@ -252,12 +269,15 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
   if constexpr (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::REG_OTHER));
   if (warp == Cfg::TMA_QK_WARP || warp == Cfg::TMA_V_WARP) {
     // ================= TMA producers =================
-    if (lane == 0) {
+    // Q/K: lane 0 alone. V: lane 0, or the whole warp when a KV cache with
+    // unused slots (seqused_k) may need rows cleared.
+    constexpr unsigned vmask = TAIL ? 0xffffffffu : 1u;
+    if (lane == 0 || (TAIL && warp == Cfg::TMA_V_WARP)) {
       const bool is_k = warp == Cfg::TMA_QK_WARP;
       if (is_k) {
         tma_prefetch_desc(&mapQ);
         tma_prefetch_desc(&mapK);
-      } else {
+      } else if (lane == 0) {
         tma_prefetch_desc(&mapV);
       }
       uint32_t kc = 0, qc[2] = {0, 0};
@@ -312,12 +332,35 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         } else {
           for (int n = nhi - 1; ok && n >= nlo; --n) {
             const int st = kc % Cfg::VST;
-            if (kc >= Cfg::VST && !wait_release(kc - Cfg::VST, B.v_empty, Cfg::VST)) { ok = false; break; }
             uint8_t* dst = smem + Cfg::OFF_V + st * Cfg::V_BYTES;
-            mbar_arrive_expect_tx(&B.v_full[st], Cfg::V_BYTES);
+            bool w = true;
+            if (lane == 0) {
+              w = kc < Cfg::VST || wait_release(kc - Cfg::VST, B.v_empty, Cfg::VST);
+              if (w) {
+                mbar_arrive_expect_tx(&B.v_full[st], Cfg::V_BYTES);
 #pragma unroll
-            for (int c = 0; c < Cfg::VCH; ++c)
-              tma_load_4d(dst + c * kChunkBytes, &mapV, &B.v_full[st], c * 64, T.k_row0 + n * kBN, T.g, cb);
+                for (int c = 0; c < Cfg::VCH; ++c)
+                  tma_load_4d(dst + c * kChunkBytes, &mapV, &B.v_full[st], c * 64, T.k_row0 + n * kBN, T.g, cb);
+              }
+            }
+            if (!__shfl_sync(vmask, w ? 1 : 0, 0)) { ok = false; break; }
+            if (tail_fix<TAIL>(T, n)) {
+              // Cache slots at or past seqused_k may never have been written
+              // (NaN); P is 0 there, but 0 * NaN is not. Clear the rows up to
+              // the next 16-key step boundary: the P.V of this block stops there.
+              const int valid = T.sk - n * kBN;
+              const bool f = __all_sync(vmask, mbar_wait(&B.v_full[st], (kc / Cfg::VST) & 1, guard));
+              if (!f) { ok = false; break; }
+              const int pieces = (min(kBN, (valid + 15) & ~15) - valid) * Cfg::VCH * 8;
+              for (int idx = lane; idx < pieces; idx += 32) {
+                const int row = valid + idx / (Cfg::VCH * 8), rem = idx % (Cfg::VCH * 8);
+                *reinterpret_cast<uint4*>(dst + (rem >> 3) * kChunkBytes + row * 128 + (rem & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+              __syncwarp(vmask);
+              if (lane == 0) mbar_arrive(&B.v_fixed[st]);
+            }
             ++kc;
           }
         }
@@ -329,7 +372,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           drain_wait(&B.k_full[u % nst], (u / nst) & 1, p.timeout_ns);
         for (int s = 0; s < NQ; ++s)
           if (qc[s] > 0) drain_wait(&B.q_full[s], (qc[s] - 1) & 1, p.timeout_ns);
-      } else {
+      } else if (lane == 0) {
         const int nst = Cfg::VST;
         for (uint32_t u = (kc > (uint32_t)nst ? kc - nst : 0); u < kc; ++u)
           drain_wait(&B.v_full[u % nst], (u / nst) & 1, p.timeout_ns);
@@ -358,13 +401,25 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         }
       };
       // O[o] (+)= P[slot] V[vst]; P from TMEM, V MN-major (64-column chunks 16 KB apart)
-      auto issue_pv = [&](int o, int slot, int vst, bool acc) {
+      auto issue_pv = [&](int o, int slot, int vst, bool acc, int steps) {
         const uint32_t d = tmem + Cfg::O_COL + o * DV;
         const uint64_t vd = sdesc_sw128(v_base + vst * Cfg::V_BYTES, kChunkBytes, 1024);
         const uint32_t pa = tmem + slot * 128;
+        if (steps == kBN / 16) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_bf16_ts(d, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_bf16_ts(d, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
+        } else {
+          for (int kk = 0; kk < steps; ++kk)
+            mma_bf16_ts(d, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
+        }
+      };
+      uint32_t vfix = 0;   // parity bit per V stage of its v_fixed barrier
+      auto wait_fix = [&](int n, int vst, const Tile& T) -> bool {
+        if (!tail_fix<TAIL>(T, n)) return true;
+        const bool r = mbar_wait(&B.v_fixed[vst], (vfix >> vst) & 1u, guard);
+        vfix ^= 1u << vst;
+        return r;
       };
 
       uint32_t kc = 0, vc = 0, qw[2] = {0, 0}, pw[2] = {0, 0}, ou[2] = {0, 0};
@@ -423,6 +478,8 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           for (int n = nhi - 1; n >= nlo; --n) {
             const int vst = vc % Cfg::VST;
             if (!mbar_wait(&B.v_full[vst], (vc / Cfg::VST) & 1, guard)) { ok = false; break; }
+            if (!wait_fix(n, vst, T)) { ok = false; break; }
+            const int steps = pv_steps<TAIL>(T, n);
             const bool has_next = n - 1 >= nlo;
             const int kst = kc % Cfg::KST;
             bool k_ready = false;
@@ -434,7 +491,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
                 tc_fence_after();
                 const bool acc = !first_pv[s];
                 if (!before_pv(s)) return false;
-                issue_pv(s, s, vst, acc);
+                issue_pv(s, s, vst, acc, steps);
                 if (n == R[s].nlo) mma_commit(&B.o_bar[s]);   // O[s] complete for this tile
               }
               if (has_next && part(R[s], n - 1)) {
@@ -480,13 +537,14 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             const int slot = (jc + i) & 1;
             const int vst = vc % Cfg::VST;
             if (!mbar_wait(&B.v_full[vst], (vc / Cfg::VST) & 1, guard)) { ok = false; break; }
+            if (!wait_fix(nhi - 1 - i, vst, T)) { ok = false; break; }
             const uint32_t pwc = slot ? pw[1] : pw[0];
             if (!mbar_wait(&B.p_full[slot], pwc & 1, guard)) { ok = false; break; }
             if (slot) ++pw[1]; else ++pw[0];
             tc_fence_after();
             const bool acc = i > 0;
             if (!before_pv(0)) { ok = false; break; }
-            issue_pv(0, slot, vst, acc);
+            issue_pv(0, slot, vst, acc, pv_steps<TAIL>(T, nhi - 1 - i));
             mma_commit(&B.o_bar[0]);
             mma_commit(&B.v_empty[vst]);
             ++vc;
@@ -698,7 +756,8 @@ template <int DK, int DV>
 cudaError_t launch_prefill_t(const FwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, int num_sms, cudaStream_t stream) {
   using Cfg = PrefillCfg<DK, DV>;
-  auto kern = prefill_kernel<DK, DV>;
+  // the TAIL instance clears cache rows past seqused_k; the other one has no such work
+  auto kern = p.seqused_k != nullptr ? prefill_kernel<DK, DV, true> : prefill_kernel<DK, DV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   long long tiles;

@@ -66,9 +66,8 @@ enum {
  *   q   (total_q, num_heads_q, head_dim_qk)   k, v (total_k, num_heads_kv, ...)
  *   out (total_q, num_heads_q, head_dim_v)    lse (num_heads_q, total_q)
  * seqused_k (int32 [batch], optional): only keys [0, seqused_k[b]) of sequence b
- *   exist; it overrides seqlen_k / the cu_seqlens_k length. The decode path never
- *   reads cache rows past seqused_k[b]. The prefill path reads whole 128-key tiles,
- *   so rows up to the next multiple of 128 past seqused_k[b] must hold finite values.
+ *   exist; it overrides seqlen_k / the cu_seqlens_k length. Cache rows past
+ *   seqused_k[b] may hold anything (NaN included): no arithmetic ever uses them.
  * Masks: causal != 0 forces window_right = 0. window_left / window_right = -1
  *   means unbounded on that side. Key j is visible from query row i of a
  *   sequence with Sq query rows and Sk keys iff

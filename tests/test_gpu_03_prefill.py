@@ -63,10 +63,12 @@ def test_varlen_unequal_q_k(d, dv):
     print(gu.check_workload(w))
 
 
-def test_prefill_seqused_k():
-    # prefill reads whole 128-key tiles: slots past seqused_k hold finite values (zeros)
-    w = inputs.batched("pfsu", 80, 3, 300, 640, 4, 2, 128, 128, causal=True,
-                       seqused_k=np.array([640, 300, 431], np.int32), pad_bits=0)
+@pytest.mark.parametrize("d,dv", [(64, 64), (128, 128), (192, 128), (256, 256)])
+def test_prefill_seqused_k_nan_padding(d, dv):
+    # cache slots past seqused_k hold NaN: prefill loads them with the tile but
+    # must never let them into O (tail V rows cleared, S columns masked)
+    w = inputs.batched("pfsu", 80 + d, 3, 300, 640, 4, 2, d, dv, causal=True,
+                       seqused_k=np.array([640, 300, 431], np.int32))
     print(gu.check_workload(w))
 
 
