@@ -459,55 +459,81 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         };
 
         if constexpr (NQ == 2) {
+          // Q tile s takes part in key block n when lo[s] <= n < hi[s]. The
+          // issuing thread runs straight-line code per block: every branch,
+          // wait and commit between two MMA groups leaves the tensor pipe idle.
+          const int lo0 = has_work(R[0]) ? R[0].nlo : INT32_MAX, hi0 = has_work(R[0]) ? R[0].nhi : INT32_MIN;
+          const int lo1 = has_work(R[1]) ? R[1].nlo : INT32_MAX, hi1 = has_work(R[1]) ? R[1].nhi : INT32_MIN;
+          if (hi0 > lo0) {
+            if (!mbar_wait(&B.q_full[0], qw[0] & 1, guard)) { ok = false; break; }
+            ++qw[0];
+          }
+          if (hi1 > lo1) {
+            if (!mbar_wait(&B.q_full[1], qw[1] & 1, guard)) { ok = false; break; }
+            ++qw[1];
+          }
           // prologue: S for the first block of each participating Q tile
           {
             const int n0 = nhi - 1, st = kc % Cfg::KST;
             if (!mbar_wait(&B.k_full[st], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
-            auto first_s_of = [&](int s) -> bool {
-              if (!part(R[s], n0)) return true;
-              if (!wait_q(s)) return false;
-              issue_s(s, s, st);
-              mma_commit(&B.s_full[s]);
-              if (n0 == R[s].nlo) mma_commit(&B.q_empty[s]);
-              return true;
-            };
-            ok = first_s_of(0) && first_s_of(1);
-            if (!ok) break;
+            if (n0 >= lo0 && n0 < hi0) {
+              issue_s(0, 0, st);
+              mma_commit(&B.s_full[0]);
+              if (n0 == lo0) mma_commit(&B.q_empty[0]);
+            }
+            if (n0 >= lo1 && n0 < hi1) {
+              issue_s(1, 1, st);
+              mma_commit(&B.s_full[1]);
+              if (n0 == lo1) mma_commit(&B.q_empty[1]);
+            }
             ++kc;
           }
+          // the O accumulators are free once the previous tile's epilogue read them
+          if (hi0 > lo0) {
+            if (ou[0] > 0 && !mbar_wait(&B.o_empty[0], (ou[0] - 1) & 1, guard)) { ok = false; break; }
+            ++ou[0];
+          }
+          if (hi1 > lo1) {
+            if (ou[1] > 0 && !mbar_wait(&B.o_empty[1], (ou[1] - 1) & 1, guard)) { ok = false; break; }
+            ++ou[1];
+          }
           for (int n = nhi - 1; n >= nlo; --n) {
-            const int vst = vc % Cfg::VST;
+            const int vst = vc % Cfg::VST, kst = kc % Cfg::KST;
+            const bool has_next = n - 1 >= nlo;
             if (!mbar_wait(&B.v_full[vst], (vc / Cfg::VST) & 1, guard)) { ok = false; break; }
             if (!wait_fix(n, vst, T)) { ok = false; break; }
             const int steps = pv_steps<TAIL>(T, n);
-            const bool has_next = n - 1 >= nlo;
-            const int kst = kc % Cfg::KST;
-            bool k_ready = false;
-            // P.V of this block for Q tile s, then S of the next block for it
-            auto pv_then_s = [&](int s) -> bool {
-              if (part(R[s], n)) {
-                if (!mbar_wait(&B.p_full[s], pw[s] & 1, guard)) return false;
-                ++pw[s];
-                tc_fence_after();
-                const bool acc = !first_pv[s];
-                if (!before_pv(s)) return false;
-                issue_pv(s, s, vst, acc, steps);
-                if (n == R[s].nlo) mma_commit(&B.o_bar[s]);   // O[s] complete for this tile
-              }
-              if (has_next && part(R[s], n - 1)) {
-                if (!k_ready) {
-                  if (!mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) return false;
-                  k_ready = true;
-                }
-                if (!wait_q(s)) return false;
-                issue_s(s, s, kst);
-                mma_commit(&B.s_full[s]);
-                if (n - 1 == R[s].nlo) mma_commit(&B.q_empty[s]);
-              }
-              return true;
-            };
-            ok = pv_then_s(0) && pv_then_s(1);
-            if (!ok) break;
+            bool k_ready = false;   // K(n-1) is waited for just before its first use
+            // Q tile 0: P.V of block n, then S of block n-1 into the same slot
+            if (n >= lo0 && n < hi0) {
+              if (!mbar_wait(&B.p_full[0], pw[0] & 1, guard)) { ok = false; break; }
+              ++pw[0];
+              tc_fence_after();
+              issue_pv(0, 0, vst, n != hi0 - 1, steps);
+              if (n == lo0) mma_commit(&B.o_bar[0]);   // O[0] complete for this tile
+            }
+            if (has_next && n - 1 >= lo0 && n - 1 < hi0) {
+              if (!mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
+              k_ready = true;
+              issue_s(0, 0, kst);
+              mma_commit(&B.s_full[0]);
+              if (n - 1 == lo0) mma_commit(&B.q_empty[0]);
+            }
+            // Q tile 1
+            if (n >= lo1 && n < hi1) {
+              if (!mbar_wait(&B.p_full[1], pw[1] & 1, guard)) { ok = false; break; }
+              ++pw[1];
+              tc_fence_after();
+              issue_pv(1, 1, vst, n != hi1 - 1, steps);
+              if (n == lo1) mma_commit(&B.o_bar[1]);
+            }
+            if (has_next && n - 1 >= lo1 && n - 1 < hi1) {
+              if (!k_ready && !mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
+              k_ready = true;
+              issue_s(1, 1, kst);
+              mma_commit(&B.s_full[1]);
+              if (n - 1 == lo1) mma_commit(&B.q_empty[1]);
+            }
             // every MMA reading K(n) and V(n) is issued: release block n
             mma_commit(&B.kv_rel[rel % Cfg::REL]);
             ++rel;
