@@ -101,3 +101,38 @@ def test_repeat_calls_are_bitwise_stable():
     o1, l1 = gu.run_gpu(w)
     o2, l2 = gu.run_gpu(w)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def _scale_rows(bits, factors, axis_len):
+    """Multiply row j (axis 1 of a [B, S, H, D] tensor) by factors[j], back to bf16."""
+    x = inputs.bf16_bits_to_f32(bits).astype(np.float64)
+    x *= factors.reshape(1, axis_len, 1, 1)
+    return inputs.f32_to_bf16_bits(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("d,dv", [(64, 64), (128, 128), (192, 128), (256, 256)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_grows_every_block(d, dv, causal):
+    """Keys grow in magnitude toward the start of the sequence. Key blocks run
+    from the last one down, so nearly every block raises some row's max by
+    more than the lazy-rescale threshold: O and l are rescaled (and the block
+    exponentiated again) block after block. Such sharp rows make O close to a
+    single V row, so V is scaled down to keep |O| (and its bf16 rounding) small."""
+    sk = 1000
+    w = inputs.batched("grow", 130 + d, 1, 300, sk, 4, 2, d, dv, causal=causal)
+    blocks = np.arange(sk) // 128
+    w.k = _scale_rows(w.k, 1.0 + 1.3 * (blocks.max() - blocks), sk)
+    w.v = _scale_rows(w.v, np.full(sk, 0.25), sk)
+    print(gu.check_workload(w))
+
+
+def test_running_max_grows_for_some_rows_only():
+    """Only odd query rows see growing maxima (their q is large), so a warp
+    mixes rows that rescale with rows that keep their base."""
+    sq, sk = 260, 900
+    w = inputs.batched("growmix", 139, 1, sq, sk, 4, 4, 128, 128, causal=True)
+    blocks = np.arange(sk) // 128
+    w.k = _scale_rows(w.k, 1.0 + 0.9 * (blocks.max() - blocks), sk)
+    w.q = _scale_rows(w.q, np.where(np.arange(sq) % 2 == 1, 2.5, 0.3), sq)
+    w.v = _scale_rows(w.v, np.full(sk, 0.25), sk)
+    print(gu.check_workload(w))
