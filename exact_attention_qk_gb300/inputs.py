@@ -20,6 +20,14 @@ prefill, a large head dim, varlen packing with a sliding window and the
            Dqk=192, Dv=128, causal, window_left=1024
   decode   Sq=1, B=64, Hq=32, Hkv=8, D=128, KV cache capacity 16384,
            seqused_k uniform in [1024, 16384]
+
+KV-cache variants of the decode workload (the fp8 KV-cache decode and paged-KV
+passages of the FlashAttention pages):
+
+  decode_fp8    the decode shape with an e4m3 K/V cache (one byte per element)
+                and per-(sequence, KV head) descales
+  decode_paged  the decode shape with the cache split into 128-key pages held
+                in a shuffled page pool, located through a page table
 """
 from __future__ import annotations
 
@@ -34,6 +42,11 @@ _Q, _K, _V = 0, 1, 2
 # bfloat16 bit pattern of a quiet NaN; written into KV-cache slots past
 # seqused_k so that any read of them that reaches the arithmetic shows up.
 BF16_NAN_BITS = 0x7FC0
+
+# fp8 element formats of a quantized KV cache, and a NaN code of each
+# (e4m3: exponent and mantissa all ones; e5m2: exponent all ones, mantissa != 0)
+FP8_FORMATS = ("e4m3", "e5m2")
+FP8_NAN_CODE = {"e4m3": 0x7F, "e5m2": 0x7F}
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -53,6 +66,32 @@ def normal_bf16(seed: int, tensor_id: int, index: int, shape) -> np.ndarray:
     """N(0,1) draws for one sequence block, rounded to bf16 bits."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tensor_id, index])))
     return f32_to_bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
+
+
+def fp8_codes(seed: int, tensor_id: int, index: int, shape, fmt: str) -> np.ndarray:
+    """Random fp8 element codes (uint8) for one sequence block.
+
+    Each code is assembled from independent draws of its fields: a random sign,
+    a biased exponent from a window that spans magnitudes of about 1/8 to 8,
+    and a uniform mantissa. No floating-point arithmetic is involved.
+    """
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tensor_id, index, 8])))
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8)
+    if fmt == "e4m3":      # 1 sign, 4 exponent (bias 7), 3 mantissa bits
+        e = rng.integers(4, 10, size=shape, dtype=np.uint8)
+        m = rng.integers(0, 8, size=shape, dtype=np.uint8)
+        return (sign << 7) | (e << 3) | m
+    if fmt == "e5m2":      # 1 sign, 5 exponent (bias 15), 2 mantissa bits
+        e = rng.integers(12, 18, size=shape, dtype=np.uint8)
+        m = rng.integers(0, 4, size=shape, dtype=np.uint8)
+        return (sign << 7) | (e << 2) | m
+    raise ValueError(fmt)
+
+
+def uniform_f32(seed: int, tensor_id: int, shape, lo: float, hi: float) -> np.ndarray:
+    """float32 draws uniform in [lo, hi)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tensor_id, 9])))
+    return rng.uniform(lo, hi, size=shape).astype(np.float32)
 
 
 def uniform_lengths(seed: int, n: int, lo: int, hi: int) -> np.ndarray:
@@ -85,6 +124,12 @@ class Workload:
     max_seqlen_q: int = 0
     max_seqlen_k: int = 0
     seed: int = 0
+    # KV-cache forms (defaults: a bf16 cache in the batched or packed layout)
+    kv_format: str = "bf16"                     # "bf16", "e4m3" or "e5m2"
+    k_descale: Optional[np.ndarray] = None      # float32 [B, Hkv]: K element = code value x descale
+    v_descale: Optional[np.ndarray] = None
+    page_table: Optional[np.ndarray] = None     # int32 [B, max_pages]; k/v then hold the page pool
+    page_size: int = 0
 
     @property
     def varlen(self) -> bool:
@@ -118,6 +163,57 @@ def batched(name, seed, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale=None, causal=False,
                     seqlen_q=Sq, seqlen_k=Sk,
                     seqused_k=None if seqused_k is None else np.asarray(seqused_k, np.int32),
                     max_seqlen_q=Sq, max_seqlen_k=Sk, seed=seed)
+
+
+def fp8_batched(name, seed, B, Sq, Sk, Hq, Hkv, D, fmt, seqused_k=None, scale=None, causal=False):
+    """Batched layout with an fp8 K/V cache: q bf16 (B,Sq,Hq,D); k, v uint8
+    codes (B,Sk,Hkv,D); descales float32 (B,Hkv) in [0.25, 1). Cache rows at or
+    past seqused_k hold NaN codes."""
+    q = np.empty((B, Sq, Hq, D), np.uint16)
+    k = np.empty((B, Sk, Hkv, D), np.uint8)
+    v = np.empty((B, Sk, Hkv, D), np.uint8)
+    for b in range(B):
+        q[b] = normal_bf16(seed, _Q, b, (Sq, Hq, D))
+        n = Sk if seqused_k is None else int(seqused_k[b])
+        k[b, :n] = fp8_codes(seed, _K, b, (n, Hkv, D), fmt)
+        v[b, :n] = fp8_codes(seed, _V, b, (n, Hkv, D), fmt)
+        if n < Sk:
+            k[b, n:] = FP8_NAN_CODE[fmt]
+            v[b, n:] = FP8_NAN_CODE[fmt]
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(D))
+    return Workload(name=name, q=q, k=k, v=v, num_heads_q=Hq, num_heads_kv=Hkv,
+                    head_dim_qk=D, head_dim_v=D, softmax_scale=scale, causal=causal, batch=B,
+                    seqlen_q=Sq, seqlen_k=Sk,
+                    seqused_k=None if seqused_k is None else np.asarray(seqused_k, np.int32),
+                    max_seqlen_q=Sq, max_seqlen_k=Sk, seed=seed, kv_format=fmt,
+                    k_descale=uniform_f32(seed, 3, (B, Hkv), 0.25, 1.0),
+                    v_descale=uniform_f32(seed, 4, (B, Hkv), 0.25, 1.0))
+
+
+def to_paged(w: Workload, page_size: int, extra_pages: int = 3) -> Workload:
+    """The same batched cache, moved into a page pool.
+
+    Sequence b's keys [j*page_size, (j+1)*page_size) go to page page_table[b, j];
+    the pages of all sequences are a random permutation of the pool, which also
+    holds `extra_pages` pages no sequence uses. Pool rows that no visible key
+    maps to (past seqused_k, and the extra pages) hold NaN patterns.
+    """
+    assert w.page_table is None and not w.varlen and w.seqlen_k % page_size == 0
+    B, Sk = w.batch, w.seqlen_k
+    per = Sk // page_size
+    n_pages = B * per + extra_pages
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, 7, page_size])))
+    perm = rng.permutation(n_pages).astype(np.int32)
+    table = perm[:B * per].reshape(B, per)
+    nan = FP8_NAN_CODE[w.kv_format] if w.kv_format in FP8_FORMATS else BF16_NAN_BITS
+    pools = []
+    for src in (w.k, w.v):
+        pool = np.full((n_pages, page_size) + src.shape[2:], nan, src.dtype)
+        pool[table.reshape(-1)] = src.reshape((B * per, page_size) + src.shape[2:])
+        pools.append(pool)
+    return dataclasses.replace(w, name=w.name + "_paged", k=pools[0], v=pools[1],
+                               page_table=np.ascontiguousarray(table), page_size=page_size)
 
 
 def packed(name, seed, lens_q, lens_k, Hq, Hkv, Dqk, Dv, scale=None, causal=False,
@@ -172,10 +268,15 @@ def workload(name: str) -> Workload:
                       window_left=1024, window_right=0)
     if name == "decode":
         return batched("decode", 5, 64, 1, 16384, 32, 8, 128, 128, seqused_k=decode_seqused())
+    if name == "decode_fp8":
+        return fp8_batched("decode_fp8", 5, 64, 1, 16384, 32, 8, 128, "e4m3", seqused_k=decode_seqused())
+    if name == "decode_paged":
+        return to_paged(workload("decode"), 128)
     if name == "decode_small":
         # the decode shape with 16 sequences (about 1 GB of cache): a profiling case
         return batched("decode_small", 5, 16, 1, 16384, 32, 8, 128, 128, seqused_k=decode_seqused()[:16])
     raise KeyError(name)
 
 
-WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode", "decode_small")
+WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode", "decode_small",
+             "decode_fp8", "decode_paged")

@@ -15,3 +15,4 @@ from .attention import (  # noqa: F401
     visible_mask,
     widen,
 )
+from .kvcache import dequant_kv, fp8_to_float, gather_pages, plain_kv  # noqa: F401,E402
