@@ -64,25 +64,31 @@ int device_sms() {
   return n;
 }
 
-// 4-D bf16 map (d, rows, heads, batch) with a box of (64, box_rows, 1, 1) and
-// 128-byte swizzle; out-of-range rows read as zero.
+// 4-D map (d, rows, heads, batch-or-page) with a box of (128 bytes of d,
+// box_rows, 1, 1) and 128-byte swizzle: 64 bf16 or 128 one-byte elements per
+// box row. Strides are in elements. Out-of-range coordinates read as zero.
 bool make_map(CUtensorMap* m, const void* base, int64_t d, int64_t rows, int64_t heads, int64_t batch,
-              int64_t row_stride, int64_t head_stride, int64_t batch_stride, int box_rows) {
+              int64_t row_stride, int64_t head_stride, int64_t batch_stride, int box_rows, int esize = 2) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
-  cuuint64_t strides[3] = {(cuuint64_t)(row_stride * 2), (cuuint64_t)(head_stride * 2),
-                           (cuuint64_t)(batch_stride * 2)};
-  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)(row_stride * esize), (cuuint64_t)(head_stride * esize),
+                           (cuuint64_t)(batch_stride * esize)};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0; }
+bool stride_ok_bytes(int64_t s, int esize) { return s >= 0 && (s * esize) % 16 == 0; }
+bool fp8_kv(const fa_fwd_args* a) { return a->kv_format == FA_KV_E4M3 || a->kv_format == FA_KV_E5M2; }
+// fp8 and paged caches run on the decode kernel whatever the query length
+bool kv_special(const fa_fwd_args* a) { return fp8_kv(a) || a->page_table != nullptr; }
 
 struct Resolved {
   bool varlen;
@@ -105,6 +111,20 @@ int check_args(const fa_fwd_args* a, Resolved* out) {
   if (!prefill_supported(a->head_dim_qk, a->head_dim_v)) return FA_ERR_UNSUPPORTED;
   if (a->window_left < -1 || a->window_right < -1) return FA_ERR_INVALID_ARG;
   if (a->num_splits < 0 || a->num_splits > 256) return FA_ERR_INVALID_ARG;
+  if (a->kv_format != FA_KV_BF16 && !fp8_kv(a)) return FA_ERR_INVALID_ARG;
+  if (fp8_kv(a)) {
+    if (varlen) return FA_ERR_UNSUPPORTED;
+    if (!((a->head_dim_qk == 128 && a->head_dim_v == 128) || (a->head_dim_qk == 256 && a->head_dim_v == 256)))
+      return FA_ERR_UNSUPPORTED;
+  }
+  if (a->page_table != nullptr) {
+    // "page_table is not supported with cu_seqlens_k" (interface.py, _flash_attn_fwd)
+    if (varlen) return FA_ERR_INVALID_ARG;
+    const int ps = a->page_size;
+    if (ps <= 0 || !(ps == 8 || ps == 16 || ps == 32 || ps % 64 == 0)) return FA_ERR_UNSUPPORTED;
+    if (a->max_pages_per_seq <= 0 || a->num_pages <= 0) return FA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(a->max_pages_per_seq) * ps > INT32_MAX / 2) return FA_ERR_INVALID_ARG;
+  }
   if (varlen) {
     if (a->total_q < 0 || a->total_k < 0 || a->max_seqlen_q < 0 || a->max_seqlen_k < 0) return FA_ERR_INVALID_ARG;
   } else {
@@ -115,6 +135,7 @@ int check_args(const fa_fwd_args* a, Resolved* out) {
   r.rows_q = varlen ? a->max_seqlen_q : a->seqlen_q;
   r.kmax = varlen ? a->max_seqlen_k : a->seqlen_k;
   r.r = a->num_heads_q / a->num_heads_kv;
+  if (a->page_table != nullptr) r.kmax = a->max_pages_per_seq * a->page_size;
   r.scale = (a->softmax_scale > 0.f && std::isfinite(a->softmax_scale))
                 ? a->softmax_scale
                 : 1.0f / std::sqrt(static_cast<float>(a->head_dim_qk));
@@ -130,12 +151,18 @@ int check_tensors(const fa_fwd_args* a, bool need_out) {
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || (need_out && !aligned16(a->out)))
     return FA_ERR_ALIGNMENT;
   const bool varlen = a->cu_seqlens_q != nullptr;
-  if (!stride_ok(a->q_row_stride) || !stride_ok(a->q_head_stride) || !stride_ok(a->k_row_stride) ||
-      !stride_ok(a->k_head_stride) || !stride_ok(a->v_row_stride) || !stride_ok(a->v_head_stride))
+  const int es = fp8_kv(a) ? 1 : 2;
+  if (!stride_ok(a->q_row_stride) || !stride_ok(a->q_head_stride) || !stride_ok_bytes(a->k_row_stride, es) ||
+      !stride_ok_bytes(a->k_head_stride, es) || !stride_ok_bytes(a->v_row_stride, es) ||
+      !stride_ok_bytes(a->v_head_stride, es))
     return FA_ERR_ALIGNMENT;
   if (need_out && (!stride_ok(a->o_row_stride) || !stride_ok(a->o_head_stride))) return FA_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(a->k_descale) & 3u) || (reinterpret_cast<uintptr_t>(a->v_descale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(a->page_table) & 3u))
+    return FA_ERR_ALIGNMENT;
   if (!varlen) {
-    if (!stride_ok(a->q_batch_stride) || !stride_ok(a->k_batch_stride) || !stride_ok(a->v_batch_stride))
+    if (!stride_ok(a->q_batch_stride) || !stride_ok_bytes(a->k_batch_stride, es) ||
+        !stride_ok_bytes(a->v_batch_stride, es))
       return FA_ERR_ALIGNMENT;
     if (need_out && !stride_ok(a->o_batch_stride)) return FA_ERR_ALIGNMENT;
   }
@@ -179,7 +206,7 @@ struct WsLayout {
 WsLayout ws_layout(const fa_fwd_args* a, const Resolved& r, int ns) {
   WsLayout w{};
   size_t off = 0;
-  const bool prefill = ns <= 1 && !decode_shaped(a, r);
+  const bool prefill = ns <= 1 && !decode_shaped(a, r) && !kv_special(a);
   if (prefill && r.varlen) {
     w.prefix_off = off;
     w.prefix_bytes = align256(sizeof(int) * (static_cast<size_t>(a->batch) + 1));
@@ -229,17 +256,34 @@ void fill_common(FwdParams* p, const fa_fwd_args* a, const Resolved& r) {
   p->write_partial = 0;
   p->status = status_ptr();
   p->timeout_ns = g_timeout_ns.load();
+  p->kv_type = a->kv_format;
+  p->k_descale = a->k_descale;
+  p->v_descale = a->v_descale;
+  p->page_table = a->page_table;
+  p->max_pages = a->max_pages_per_seq;
+  p->page_size = a->page_size;
+  p->num_pages = a->num_pages;
+  if (a->page_table != nullptr) p->seqlen_k = r.kmax;   // key capacity of every sequence
 }
 
 bool kv_maps(const fa_fwd_args* a, const Resolved& r, int box_rows, CUtensorMap* mk, CUtensorMap* mv) {
+  const int es = fp8_kv(a) ? 1 : 2;
+  if (a->page_table != nullptr) {
+    // pools: (d, page_size, heads, pages); a load moves at most one page
+    const int rows = box_rows < a->page_size ? box_rows : a->page_size;
+    return make_map(mk, a->k, a->head_dim_qk, a->page_size, a->num_heads_kv, a->num_pages, a->k_row_stride,
+                    a->k_head_stride, a->k_batch_stride, rows, es) &&
+           make_map(mv, a->v, a->head_dim_v, a->page_size, a->num_heads_kv, a->num_pages, a->v_row_stride,
+                    a->v_head_stride, a->v_batch_stride, rows, es);
+  }
   const int64_t rows = r.varlen ? a->total_k : a->seqlen_k;
   const int64_t nb = r.varlen ? 1 : a->batch;
   const int64_t kbs = r.varlen ? a->k_row_stride * (rows > 0 ? rows : 1) : a->k_batch_stride;
   const int64_t vbs = r.varlen ? a->v_row_stride * (rows > 0 ? rows : 1) : a->v_batch_stride;
   return make_map(mk, a->k, a->head_dim_qk, rows, a->num_heads_kv, nb, a->k_row_stride, a->k_head_stride,
-                  kbs > 0 ? kbs : 8, box_rows) &&
+                  kbs > 0 ? kbs : 16, box_rows, es) &&
          make_map(mv, a->v, a->head_dim_v, rows, a->num_heads_kv, nb, a->v_row_stride, a->v_head_stride,
-                  vbs > 0 ? vbs : 8, box_rows);
+                  vbs > 0 ? vbs : 16, box_rows, es);
 }
 
 int run_decode(const fa_fwd_args* a, const Resolved& r, int ns, float* opart, float* lpart, cudaStream_t st) {
@@ -317,7 +361,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_abi_version(void) { return 100; }
+int fa_abi_version(void) { return 200; }
 
 const char* fa_status_string(int s) {
   switch (s) {
@@ -377,7 +421,7 @@ int fa_fwd(const fa_fwd_args* a, void* workspace, size_t workspace_bytes, void* 
                       a->cu_seqlens_q, r.varlen ? a->total_q : 0, a->out, a->o_batch_stride, a->o_row_stride,
                       a->o_head_stride, a->lse, stream);
   }
-  if (decode_shaped(a, r)) return run_decode(a, r, 1, nullptr, nullptr, st);
+  if (decode_shaped(a, r) || kv_special(a)) return run_decode(a, r, 1, nullptr, nullptr, st);
   return run_prefill(a, r, workspace, w, st);
 }
 

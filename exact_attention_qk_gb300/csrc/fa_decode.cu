@@ -16,7 +16,16 @@
 //     into q, and P.V with per-lane output columns;
 //   * the four warps' (m, l, O) states merge in shared memory at the end and the
 //     CTA writes either the final bf16 O / fp32 LSE or the fp32 split partials.
+// KV-cache forms (the fp8 KV-cache decode and paged-KV passages of the
+// FlashAttention sm_120 pull-request page and of `_flash_attn_fwd`):
+//   * fp8 (E4M3 / E5M2) caches move one byte per element: a 128-byte box row
+//     holds 128 dims; the compute warps widen codes to fp32 in registers, the
+//     K descale is folded into q and the V descale into the written O;
+//   * a paged cache is read page by page: each 64-key tile looks up its page
+//     (or pages, for pages under 64 keys) in the page table and loads from
+//     that page's rows; an index outside the pool reads zeros.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
@@ -29,10 +38,28 @@ constexpr int kDecThreads = (kDecWarps + 1) * 32;
 constexpr int kTileKeys = 64;
 constexpr int kBoxBytes = kTileKeys * 128;   // one 64-element x 64-key box
 
-template <int DK, int DV, int NR>
+// Widen four fp8 codes (one 32-bit word, lowest byte first) to fp32 pairs.
+template <int KVT>
+__device__ __forceinline__ void fp8x4_to_f32(uint32_t w, float2& lo, float2& hi) {
+  uint32_t h0, h1;
+  if constexpr (KVT == 1) {   // E4M3 -> f16 pairs (exact), then f32
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+  } else {                    // E5M2 is the upper byte of an f16
+    h0 = __byte_perm(w, 0u, 0x1404);
+    h1 = __byte_perm(w, 0u, 0x3424);
+  }
+  lo = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+  hi = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+}
+
+template <int DK, int DV, int NR, int KVT>
 struct DecodeCfg {
-  static constexpr int KCH = DK / 64;
-  static constexpr int VCH = DV / 64;
+  static constexpr int ES = KVT ? 1 : 2;          // bytes per K/V element
+  static constexpr int KCH = DK * ES / 128;       // 128-byte boxes per K row
+  static constexpr int VCH = DV * ES / 128;
   static constexpr int STAGE_BYTES = (KCH + VCH) * kBoxBytes;
   // Two stages keep the CTA under 70 KB of shared memory, so three CTAs (12
   // compute warps) share an SM: the QK / softmax / PV chains are latency-bound
@@ -51,11 +78,11 @@ struct DecodeCfg {
   static_assert(NR * E <= 64, "accumulator budget");
 };
 
-template <int DK, int DV, int NR>
+template <int DK, int DV, int NR, int KVT>
 __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                   const FwdParams p) {
-  using C = DecodeCfg<DK, DV, NR>;
+  using C = DecodeCfg<DK, DV, NR, KVT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
@@ -80,6 +107,7 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
     sk = p.cu_seqlens_k[b + 1] - k_row0;
   }
   if (p.seqused_k) sk = p.seqused_k[b];
+  if (!varlen) sk = min(sk, p.seqlen_k);           // never past the cache capacity
   const int rows = sq * p.r;                       // packed rows of this KV head
   const int prow0 = chunk * NR;
   if (prow0 >= rows) return;                       // chunk past this sequence's rows
@@ -159,7 +187,8 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  // q rows -> fp32 with the softmax scale (base 2) folded in
+  // q rows -> fp32 with the softmax scale (base 2) and the K descale folded in
+  const float qscale = p.scale_log2 * (p.k_descale ? p.k_descale[int64_t(b) * p.hkv + g] : 1.f);
   for (int idx = tid; idx < NR * DK; idx += blockDim.x) {
     const int rr = idx / DK, d = idx % DK;
     float v = 0.f;
@@ -169,7 +198,7 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
       const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q);
       v = __bfloat162float(q[(varlen ? 0 : int64_t(b) * p.q_bs) + int64_t(q_row0 + i) * p.q_rs +
                              int64_t(h) * p.q_hs + d]) *
-          p.scale_log2;
+          qscale;
     }
     q_s[idx] = v;
   }
@@ -183,18 +212,46 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
       const int kb = varlen ? 0 : b;
+      constexpr int INNER = 128 / C::ES;   // elements per box row
+      const bool paged = p.page_table != nullptr;
+      const int rpl = paged ? min(kTileKeys, p.page_size) : kTileKeys;   // rows per load
       int t = 0;
       for (; t < ntiles; ++t) {
         const int st = t % C::NSTAGE;
-        if (t >= C::NSTAGE && !mbar_wait(&empty[st], ((t / C::NSTAGE) - 1) & 1, guard)) break;
-        uint8_t* dst = smem + st * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
-        const int row = k_row0 + key_base + t * kTileKeys;
+        const int key = key_base + t * kTileKeys;
+        if (!paged) {
+          if (t >= C::NSTAGE && !mbar_wait(&empty[st], ((t / C::NSTAGE) - 1) & 1, guard)) break;
+          uint8_t* dst = smem + st * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+          const int row = k_row0 + key;
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c) tma_load_4d(dst + c * kBoxBytes, &mapK, &full[st], c * 64, row, g, kb);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(dst + c * kBoxBytes, &mapK, &full[st], c * INNER, row, g, kb);
 #pragma unroll
-        for (int c = 0; c < C::VCH; ++c)
-          tma_load_4d(dst + (C::KCH + c) * kBoxBytes, &mapV, &full[st], c * 64, row, g, kb);
+          for (int c = 0; c < C::VCH; ++c)
+            tma_load_4d(dst + (C::KCH + c) * kBoxBytes, &mapV, &full[st], c * INNER, row, g, kb);
+        } else {
+          // the page of the tile's first key, read before the slot wait so
+          // that its latency overlaps it (pages of 64+ keys: one per tile)
+          const int pi0 = key / p.page_size;
+          const int page0 = pi0 < p.max_pages ? p.page_table[int64_t(b) * p.max_pages + pi0] : p.num_pages;
+          if (t >= C::NSTAGE && !mbar_wait(&empty[st], ((t / C::NSTAGE) - 1) & 1, guard)) break;
+          uint8_t* dst = smem + st * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+          for (int sub = 0; sub < kTileKeys; sub += rpl) {
+            const int kk = key + sub;
+            const int pi = kk / p.page_size;
+            const int page =
+                sub == 0 ? page0 : (pi < p.max_pages ? p.page_table[int64_t(b) * p.max_pages + pi] : p.num_pages);
+            const int r = kk - pi * p.page_size;
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_4d(dst + c * kBoxBytes + sub * 128, &mapK, &full[st], c * INNER, r, g, page);
+#pragma unroll
+            for (int c = 0; c < C::VCH; ++c)
+              tma_load_4d(dst + (C::KCH + c) * kBoxBytes + sub * 128, &mapV, &full[st], c * INNER, r, g, page);
+          }
+        }
       }
       // drain: never leave a copy in flight into shared memory of an exiting CTA
       const WaitGuard drain{abort_flag, p.status, p.timeout_ns};
@@ -227,7 +284,8 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
   }
   float* pw = p_s + warp * 16 * NR;
   const int e0 = lane * E;                       // first output column of this lane
-  const int vbox = e0 / 64, vch = (e0 % 64) / 8, vbyte = (e0 % 8) * 2;
+  // this lane's columns inside a V row: box, 16-byte granule, byte in it
+  const int vbox = e0 * C::ES / 128, vch = (e0 * C::ES % 128) / 16, vbyte = e0 * C::ES % 16;
   const int key_end = min(sk, s_hi);             // keys at or past this are never used
 
   bool ok = true;
@@ -247,6 +305,37 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
       acc0[rr] = make_float2(0.f, 0.f);
       acc1[rr] = make_float2(0.f, 0.f);
     }
+    if constexpr (KVT != 0) {
+      // fp8: 16 dims (one 16-byte granule) per load, DK/64 granules per quarter
+#pragma unroll
+      for (int c = 0; c < DK / 64; ++c) {
+        const int gg = qp * (DK / 64) + c;
+        const uint8_t* kb = stage + (gg >> 3) * kBoxBytes;
+        const uint4 ka = *reinterpret_cast<const uint4*>(kb + kw0 * 128 + (((gg & 7) ^ (kw0 & 7)) << 4));
+        const uint4 kc = *reinterpret_cast<const uint4*>(kb + kw1 * 128 + (((gg & 7) ^ (kw1 & 7)) << 4));
+        float2 a[8], bb[8];
+        fp8x4_to_f32<KVT>(ka.x, a[0], a[1]);
+        fp8x4_to_f32<KVT>(ka.y, a[2], a[3]);
+        fp8x4_to_f32<KVT>(ka.z, a[4], a[5]);
+        fp8x4_to_f32<KVT>(ka.w, a[6], a[7]);
+        fp8x4_to_f32<KVT>(kc.x, bb[0], bb[1]);
+        fp8x4_to_f32<KVT>(kc.y, bb[2], bb[3]);
+        fp8x4_to_f32<KVT>(kc.z, bb[4], bb[5]);
+        fp8x4_to_f32<KVT>(kc.w, bb[6], bb[7]);
+#pragma unroll
+        for (int rr = 0; rr < NR; ++rr) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float4 qv = *reinterpret_cast<const float4*>(q_s + rr * DK + gg * 16 + u * 4);
+            const float2 q0 = make_float2(qv.x, qv.y), q1 = make_float2(qv.z, qv.w);
+            acc0[rr] = __ffma2_rn(q0, a[2 * u], acc0[rr]);
+            acc0[rr] = __ffma2_rn(q1, a[2 * u + 1], acc0[rr]);
+            acc1[rr] = __ffma2_rn(q0, bb[2 * u], acc1[rr]);
+            acc1[rr] = __ffma2_rn(q1, bb[2 * u + 1], acc1[rr]);
+          }
+        }
+      }
+    } else {
 #pragma unroll
     for (int c = 0; c < QCH; ++c) {
       const int gc = qp * QCH + c;
@@ -276,6 +365,7 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
         acc1[rr] = __ffma2_rn(q2, b2, acc1[rr]);
         acc1[rr] = __ffma2_rn(q3, b3, acc1[rr]);
       }
+    }
     }
     const int j0 = tkey0 + kw0, j1 = tkey0 + kw1;
     float s0[NR], s1[NR];
@@ -322,7 +412,13 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
       const int key = warp * 16 + k2;
       const uint8_t* vp = stage + (C::KCH + vbox) * kBoxBytes + key * 128 + (((vch ^ (key & 7)) << 4) + vbyte);
       float2 vf[E / 2];
-      if constexpr (E == 2) {
+      if constexpr (KVT != 0 && E == 4) {
+        fp8x4_to_f32<KVT>(*reinterpret_cast<const uint32_t*>(vp), vf[0], vf[1]);
+      } else if constexpr (KVT != 0 && E == 8) {
+        const uint2 w = *reinterpret_cast<const uint2*>(vp);
+        fp8x4_to_f32<KVT>(w.x, vf[0], vf[1]);
+        fp8x4_to_f32<KVT>(w.y, vf[2], vf[3]);
+      } else if constexpr (E == 2) {
         const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
         vf[0] = make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
       } else if constexpr (E == 4) {
@@ -384,6 +480,7 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
   if (!ok || *abort_flag) return;
+  const float vscale = p.v_descale ? p.v_descale[int64_t(b) * p.hkv + g] : 1.f;
   for (int idx = tid; idx < NR * DV; idx += kDecWarps * 32) {
     const int rr = idx / DV, d = idx % DV;
     if (prow0 + rr >= rows) continue;
@@ -401,7 +498,7 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
       }
     }
     const bool empty_row = !(L > 0.f);
-    const float ov = empty_row ? 0.f : acc / L;
+    const float ov = empty_row ? 0.f : acc / L * vscale;
     const float lse_v = empty_row ? -INFINITY : (M + log2f(L)) * 0.69314718055994530942f;
     write_row(rr, d, ov, lse_v, d == 0);
   }
@@ -480,11 +577,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   if (p.lse && lane == 0) p.lse[lse_base] = lse;
 }
 
-template <int DK, int DV, int NR>
+template <int DK, int DV, int NR, int KVT>
 cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                             cudaStream_t stream) {
-  using C = DecodeCfg<DK, DV, NR>;
-  auto kern = decode_kernel<DK, DV, NR>;
+  using C = DecodeCfg<DK, DV, NR, KVT>;
+  auto kern = decode_kernel<DK, DV, NR, KVT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int rows = p.max_seqlen_q * p.r;
@@ -494,16 +591,16 @@ cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& mk, const CUt
   return cudaGetLastError();
 }
 
-template <int DK, int DV>
+template <int DK, int DV, int KVT = 0>
 cudaError_t launch_decode_nr(const FwdParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                              cudaStream_t stream) {
   // rows per CTA: up to 8 (more would spill the accumulators); larger row
   // counts are split into chunks of 8 over grid.y
   const int rows = p.max_seqlen_q * p.r;
-  if (rows <= 1) return launch_decode_t<DK, DV, 1>(p, mk, mv, stream);
-  if (rows <= 2) return launch_decode_t<DK, DV, 2>(p, mk, mv, stream);
-  if (rows <= 4) return launch_decode_t<DK, DV, 4>(p, mk, mv, stream);
-  return launch_decode_t<DK, DV, 8>(p, mk, mv, stream);
+  if (rows <= 1) return launch_decode_t<DK, DV, 1, KVT>(p, mk, mv, stream);
+  if (rows <= 2) return launch_decode_t<DK, DV, 2, KVT>(p, mk, mv, stream);
+  if (rows <= 4) return launch_decode_t<DK, DV, 4, KVT>(p, mk, mv, stream);
+  return launch_decode_t<DK, DV, 8, KVT>(p, mk, mv, stream);
 }
 
 }  // namespace
@@ -517,6 +614,16 @@ int decode_max_rows() { return 16; }
 
 cudaError_t launch_decode(const FwdParams& p, int dk, int dv, const CUtensorMap& mk, const CUtensorMap& mv,
                           cudaStream_t stream) {
+  if (p.kv_type == 1) {
+    if (dk == 128 && dv == 128) return launch_decode_nr<128, 128, 1>(p, mk, mv, stream);
+    if (dk == 256 && dv == 256) return launch_decode_nr<256, 256, 1>(p, mk, mv, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (p.kv_type == 2) {
+    if (dk == 128 && dv == 128) return launch_decode_nr<128, 128, 2>(p, mk, mv, stream);
+    if (dk == 256 && dv == 256) return launch_decode_nr<256, 256, 2>(p, mk, mv, stream);
+    return cudaErrorInvalidValue;
+  }
   if (dk == 64 && dv == 64) return launch_decode_nr<64, 64>(p, mk, mv, stream);
   if (dk == 128 && dv == 128) return launch_decode_nr<128, 128>(p, mk, mv, stream);
   if (dk == 192 && dv == 128) return launch_decode_nr<192, 128>(p, mk, mv, stream);

@@ -35,6 +35,12 @@ struct FwdParams {
   int num_tiles;                 // batched prefill: total work tiles
   int* status;                   // device status word
   unsigned long long timeout_ns;
+  // KV-cache forms (decode kernel only)
+  int kv_type;                   // 0 bf16, 1 e4m3, 2 e5m2
+  const float* k_descale;        // fp8: [batch * hkv] or NULL
+  const float* v_descale;
+  const int* page_table;         // [batch * max_pages] or NULL
+  int max_pages, page_size, num_pages;
 };
 
 // Launchers (return cudaGetLastError() after the launch).

@@ -57,7 +57,26 @@ class FwdArgs(ctypes.Structure):
         ("softmax_scale", ctypes.c_float),
         ("causal", ctypes.c_int32), ("window_left", ctypes.c_int32), ("window_right", ctypes.c_int32),
         ("num_splits", ctypes.c_int32),
+        ("kv_format", ctypes.c_int32), ("k_descale", ctypes.c_void_p), ("v_descale", ctypes.c_void_p),
+        ("page_table", ctypes.c_void_p), ("max_pages_per_seq", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
     ]
+
+
+# K/V element formats (fa.h FA_KV_*)
+KV_FORMATS = {"bf16": 0, "e4m3": 1, "e5m2": 2}
+
+
+def _kv_format_of(k: torch.Tensor, kv_format) -> int:
+    if kv_format is not None:
+        return KV_FORMATS[kv_format] if isinstance(kv_format, str) else int(kv_format)
+    if hasattr(torch, "float8_e4m3fn") and k.dtype == torch.float8_e4m3fn:
+        return KV_FORMATS["e4m3"]
+    if hasattr(torch, "float8_e5m2") and k.dtype == torch.float8_e5m2:
+        return KV_FORMATS["e5m2"]
+    if k.dtype == torch.uint8:
+        raise ValueError("uint8 K/V need kv_format='e4m3' or 'e5m2'")
+    return KV_FORMATS["bf16"]
 
 
 _P = ctypes.POINTER(FwdArgs)
@@ -115,8 +134,15 @@ def _stream_handle(stream) -> int:
 
 def make_args(q, k, v, out=None, lse=None, *, softmax_scale=None, causal=False, window_left=-1,
               window_right=-1, cu_seqlens_q=None, cu_seqlens_k=None, seqused_k=None, max_seqlen_q=None,
-              max_seqlen_k=None, num_splits=0) -> FwdArgs:
-    """Fill fa_fwd_args from tensors (q/k/v/out bf16, last dim contiguous)."""
+              max_seqlen_k=None, num_splits=0, kv_format=None, k_descale=None, v_descale=None,
+              page_table=None) -> FwdArgs:
+    """Fill fa_fwd_args from tensors (q/out bf16, last dim contiguous).
+
+    k / v: bf16, or one-byte fp8 codes (uint8 with kv_format 'e4m3' / 'e5m2', or
+    torch's float8 dtypes) with fp32 k_descale / v_descale of shape
+    (batch, num_heads_kv). With page_table (int32 (batch, max_pages_per_seq)),
+    k and v are page pools (num_pages, page_size, num_heads_kv, head_dim).
+    """
     a = FwdArgs()
     a.q, a.k, a.v, a.out, a.lse = _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse)
     varlen = cu_seqlens_q is not None
@@ -139,12 +165,20 @@ def make_args(q, k, v, out=None, lse=None, *, softmax_scale=None, causal=False, 
             a.o_batch_stride, a.o_row_stride, a.o_head_stride = out.stride(0), out.stride(1), out.stride(2)
         a.batch, a.seqlen_q, a.seqlen_k = q.shape[0], q.shape[1], k.shape[1]
         a.num_heads_q, a.num_heads_kv = q.shape[2], k.shape[2]
+        if page_table is not None:
+            a.seqlen_k = page_table.shape[1] * k.shape[1]
     a.head_dim_qk, a.head_dim_v = q.shape[-1], v.shape[-1]
     a.cu_seqlens_q, a.cu_seqlens_k, a.seqused_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(seqused_k)
     a.softmax_scale = 0.0 if softmax_scale is None else float(softmax_scale)
     a.causal = 1 if causal else 0
     a.window_left, a.window_right = int(window_left), int(window_right)
     a.num_splits = int(num_splits)
+    if page_table is not None:
+        a.page_table = _ptr(page_table)
+        a.max_pages_per_seq = page_table.shape[1]
+        a.num_pages, a.page_size = k.shape[0], k.shape[1]
+    a.kv_format = _kv_format_of(k, kv_format)
+    a.k_descale, a.v_descale = _ptr(k_descale), _ptr(v_descale)
     return a
 
 

@@ -77,8 +77,35 @@ enum {
  * num_splits: 0 = let the library choose (fa_num_splits), 1 = no split,
  *   > 1 = split-KV with that many splits followed by the combine (<= 256).
  * Supported (head_dim_qk, head_dim_v): (64,64), (128,128), (192,128), (256,256).
- * Element type: bf16 for q, k, v and out.
+ * Element type: bf16 for q and out; k and v are bf16 unless kv_format says otherwise.
+ *
+ * KV-cache forms (every field below zero / NULL: a bf16 cache in the layouts above).
+ *   fp8 cache ("fp8 KV-cache decode (e4m3/e5m2)" on the FlashAttention sm_120
+ *   pull-request page: a bf16 query against a quantized cache with per-(batch,
+ *   kv_head) k_descale / v_descale): kv_format FA_KV_E4M3 or FA_KV_E5M2; k and
+ *   v hold one byte per element in that 8-bit float format, and element
+ *   (b, j, g, d) of K stands for its code value x k_descale[b * num_heads_kv + g]
+ *   (V likewise with v_descale; a NULL descale means 1). K/V strides are still
+ *   in elements (= bytes) and must be multiples of 16. Head dims (128,128) and
+ *   (256,256); batched or paged layout, not varlen.
+ *   Paged cache ("mslk/attention/flash_attn/interface.py", `_flash_attn_fwd`:
+ *   page_table int32 (batch, max_num_pages_per_seq), k/v (num_pages, page_size,
+ *   num_heads_kv, head_dim)): page_table != NULL; k and v are pools of
+ *   num_pages pages, k_batch_stride / v_batch_stride are the page strides, and
+ *   key j of sequence b is row j % page_size of page
+ *   page_table[b * max_pages_per_seq + j / page_size]. The key capacity is
+ *   max_pages_per_seq * page_size (seqlen_k is ignored); seqused_k gives the
+ *   lengths. page_size: 8, 16, 32 or a multiple of 64. Not with cu_seqlens
+ *   (FA_ERR_INVALID_ARG). A page index outside [0, num_pages) reads zeros.
+ *   Both forms run on the split-KV decode kernel, for any number of query rows
+ *   (correct for prefill shapes too, but built for few rows per KV head).
  */
+enum {
+  FA_KV_BF16 = 0,   /* 2-byte bfloat16 elements                                 */
+  FA_KV_E4M3 = 1,   /* 1-byte E4M3 (bias 7, no infinities), times its descale   */
+  FA_KV_E5M2 = 2,   /* 1-byte E5M2 (bias 15, IEEE-style), times its descale     */
+};
+
 typedef struct fa_fwd_args {
   const void* q;
   const void* k;
@@ -108,6 +135,14 @@ typedef struct fa_fwd_args {
   int32_t window_left;
   int32_t window_right;
   int32_t num_splits;
+  /* KV-cache forms (see above); zero / NULL for a plain bf16 cache */
+  int32_t kv_format;           /* FA_KV_BF16, FA_KV_E4M3 or FA_KV_E5M2            */
+  const float* k_descale;      /* fp8: fp32 [batch * num_heads_kv] or NULL (= 1)   */
+  const float* v_descale;
+  const int32_t* page_table;   /* int32 [batch * max_pages_per_seq] or NULL        */
+  int32_t max_pages_per_seq;
+  int32_t page_size;           /* keys per page                                    */
+  int32_t num_pages;           /* pages in the k and v pools                       */
 } fa_fwd_args;
 
 /*
@@ -205,7 +240,7 @@ void fa_set_wait_timeout_ns(uint64_t ns);
 /* Static text for a status code. */
 const char* fa_status_string(int status);
 
-/* ABI version (major*100 + minor). */
+/* ABI version (major*100 + minor): 200 since fa_fwd_args gained the KV-cache fields. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

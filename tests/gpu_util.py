@@ -36,10 +36,37 @@ def oracle_kw(w):
                 seqused_k=w.seqused_k)
 
 
+def kv_to_dev(w, dev="cuda:0"):
+    """K and V of a workload on the device: bf16 bits, or fp8 codes as uint8."""
+    if w.kv_format == "bf16":
+        return to_dev(w.k, dev), to_dev(w.v, dev)
+    return (torch.from_numpy(np.ascontiguousarray(w.k)).to(dev),
+            torch.from_numpy(np.ascontiguousarray(w.v)).to(dev))
+
+
+def kv_kw(w, dev="cuda:0"):
+    """fa_fwd keywords of a workload's KV-cache form (fp8 descales, page table)."""
+    kw = {}
+    if w.kv_format != "bf16":
+        kw.update(kv_format=w.kv_format, k_descale=torch.from_numpy(w.k_descale).to(dev),
+                  v_descale=torch.from_numpy(w.v_descale).to(dev))
+    if w.page_table is not None:
+        kw["page_table"] = i32(w.page_table, dev)
+    return kw
+
+
+def oracle_kv(w):
+    """K and V for the oracle: pages gathered, fp8 codes dequantized."""
+    if w.kv_format == "bf16" and w.page_table is None:
+        return w.k, w.v
+    return oracle.plain_kv(w)
+
+
 def run_gpu(w, num_splits=0, out=None):
     from exact_attention_qk_gb300 import fa
-    q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
-    extra = {}
+    q = to_dev(w.q)
+    k, v = kv_to_dev(w)
+    extra = kv_kw(w)
     if w.varlen:
         extra = dict(cu_seqlens_q=i32(w.cu_seqlens_q), cu_seqlens_k=i32(w.cu_seqlens_k),
                      max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k)
@@ -68,5 +95,6 @@ def compare(o_gpu, l_gpu, o_ref, l_ref, label=""):
 
 def check_workload(w, num_splits=0):
     o, l = run_gpu(w, num_splits=num_splits)
-    o_ref, l_ref = oracle.attention_forward(w.q, w.k, w.v, **oracle_kw(w))
+    k, v = oracle_kv(w)
+    o_ref, l_ref = oracle.attention_forward(w.q, k, v, **oracle_kw(w))
     return compare(o, l, o_ref, l_ref, w.name)

@@ -59,7 +59,7 @@ def test_struct_layout_matches_header(fa, tmp_path):
     assert int(got["sizeof"]) == ctypes.sizeof(fa.FwdArgs)
     for n in fields:
         assert int(got[n]) == getattr(fa.FwdArgs, n).offset, n
-    assert fa.fa_abi_version() == 100
+    assert fa.fa_abi_version() == 200
 
 
 def _args(fa, **over):
