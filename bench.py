@@ -70,13 +70,21 @@ def flops(w) -> float:
 
 
 def decode_bytes(w) -> float:
+    """Q + visible K/V rows + O + LSE, plus the descales of an fp8 cache and
+    the page-table entries of a paged one."""
     rows = sum(sq for sq, _ in seq_lengths(w))
     keys = sum(sk for _, sk in seq_lengths(w))
+    es = 2 if w.kv_format == "bf16" else 1
     q = rows * w.num_heads_q * w.head_dim_qk * 2
-    kv = keys * w.num_heads_kv * (w.head_dim_qk + w.head_dim_v) * 2
+    kv = keys * w.num_heads_kv * (w.head_dim_qk + w.head_dim_v) * es
     o = rows * w.num_heads_q * w.head_dim_v * 2
     lse = rows * w.num_heads_q * 4
-    return float(q + kv + o + lse)
+    extra = 0
+    if w.kv_format != "bf16":
+        extra += 2 * w.batch * w.num_heads_kv * 4
+    if w.page_table is not None:
+        extra += sum(-(-sk // w.page_size) for _, sk in seq_lengths(w)) * 4
+    return float(q + kv + o + lse + extra)
 
 
 def is_decode(name):
@@ -197,12 +205,19 @@ class Runner:
         self.dev = dev
 
         def up(a):
+            if a.dtype == np.uint8:      # fp8 codes
+                return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
         self.q, self.k, self.v = up(w.q), up(w.k), up(w.v)
         self.extra = {}
+        if w.kv_format != "bf16":
+            self.extra.update(kv_format=w.kv_format, k_descale=torch.from_numpy(w.k_descale).to(dev),
+                              v_descale=torch.from_numpy(w.v_descale).to(dev))
+        if w.page_table is not None:
+            self.extra["page_table"] = torch.from_numpy(w.page_table).to(dev)
         if w.varlen:
-            self.extra = dict(cu_seqlens_q=torch.from_numpy(w.cu_seqlens_q).to(dev),
+            self.extra.update(cu_seqlens_q=torch.from_numpy(w.cu_seqlens_q).to(dev),
                               cu_seqlens_k=torch.from_numpy(w.cu_seqlens_k).to(dev),
                               max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k)
         if w.seqused_k is not None:
@@ -299,21 +314,31 @@ def time_e2e(r: Runner, steps: int, warmup: int):
     """Public API end to end: pinned host inputs -> H2D, fa_fwd, O and LSE -> host."""
     torch, fa = r.torch, r.fa
     w = r.w
-    hq = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).pin_memory()
-    hk = torch.from_numpy(np.ascontiguousarray(w.k).view(np.int16)).pin_memory()
-    hv = torch.from_numpy(np.ascontiguousarray(w.v).view(np.int16)).pin_memory()
+    def host(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a if a.dtype == np.uint8 else a.view(np.int16)).pin_memory()
+
+    def bits(t):   # the device tensor as the host copy's element type
+        return t if t.dtype == torch.uint8 else t.view(torch.int16)
+
+    hq, hk, hv = host(w.q), host(w.k), host(w.v)
     ho = torch.empty(r.out.shape, dtype=torch.int16).pin_memory()
     hl = torch.empty(r.lse.shape, dtype=torch.float32).pin_memory()
-    dq = r.q.view(torch.int16)
-    dk = r.k.view(torch.int16)
-    dv = r.v.view(torch.int16)
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    dq, dk, dv = bits(r.q), bits(r.k), bits(r.v)
+    # the small per-call inputs of a KV-cache form travel too
+    small = [(torch.from_numpy(np.ascontiguousarray(x)).pin_memory(), r.extra[name])
+             for name, x in (("k_descale", w.k_descale), ("v_descale", w.v_descale), ("page_table", w.page_table))
+             if name in r.extra]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv)) + \
+        sum(h.numel() * h.element_size() for h, _ in small)
     d2h = ho.numel() * 2 + hl.numel() * 4
 
     def one():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
+        for h, d in small:
+            d.copy_(h, non_blocking=True)
         fa.fa_fwd(r.q, r.k, r.v, out=r.out, lse=r.lse, workspace=r.ws, **r.kw, **r.extra)
         ho.copy_(r.out.view(torch.int16), non_blocking=True)
         hl.copy_(r.lse, non_blocking=True)
@@ -335,9 +360,26 @@ def oracle_sample(w, budget_s: float, max_pairs=None):
     """Time the fp64 oracle on whole (sequence, head) pairs until ~budget_s.
 
     Returns (work units done, seconds, description)."""
+    import dataclasses
     import oracle
-    seqs = oracle.sequences(w.q.shape, w.k.shape, w.cu_seqlens_q, w.cu_seqlens_k, w.seqused_k)
+    kshape = w.k.shape if w.page_table is None else (w.batch, w.page_table.shape[1] * w.page_size) + w.k.shape[2:]
+    seqs = oracle.sequences(w.q.shape, kshape, w.cu_seqlens_q, w.cu_seqlens_k, w.seqused_k)
     r = w.num_heads_q // w.num_heads_kv
+    plain = {}
+
+    def plain_kv(b):
+        # fp8 / paged caches: the oracle's plain K and V of sequence b (timed with it)
+        if b not in plain:
+            sub = dict(q=w.q[b:b + 1], batch=1)
+            if w.page_table is not None:
+                sub["page_table"] = w.page_table[b:b + 1]
+            else:
+                sub.update(k=w.k[b:b + 1], v=w.v[b:b + 1])
+            if w.kv_format != "bf16":
+                sub.update(k_descale=w.k_descale[b:b + 1], v_descale=w.v_descale[b:b + 1])
+            plain.clear()
+            plain[b] = oracle.plain_kv(dataclasses.replace(w, **sub))
+        return plain[b]
     done_work, t_total, pairs = 0.0, 0.0, 0
     order = [(b, h) for b in range(len(seqs)) for h in range(w.num_heads_q)]
     for b, h in order:
@@ -349,16 +391,21 @@ def oracle_sample(w, budget_s: float, max_pairs=None):
             k = w.k[s.k_start:s.k_start + s.sk, h // r][None, :, None, :]
             v = w.v[s.k_start:s.k_start + s.sk, h // r][None, :, None, :]
         else:
+            t0 = time.perf_counter()
+            kk, vv = (w.k, w.v) if (w.kv_format == "bf16" and w.page_table is None) else plain_kv(b)
+            bb = b if kk is w.k else 0
+            t_total += time.perf_counter() - t0
             q = w.q[b:b + 1, :, h:h + 1]
-            k = w.k[b:b + 1, :s.sk, h // r:h // r + 1]
-            v = w.v[b:b + 1, :s.sk, h // r:h // r + 1]
+            k = kk[bb:bb + 1, :s.sk, h // r:h // r + 1]
+            v = vv[bb:bb + 1, :s.sk, h // r:h // r + 1]
         t0 = time.perf_counter()
         oracle.attention_forward(q, k, v, scale=w.softmax_scale, causal=w.causal, window_left=w.window_left,
                                  window_right=w.window_right)
         t_total += time.perf_counter() - t0
         pairs += 1
         if is_decode(w.name):
-            done_work += s.sq * w.head_dim_qk * 2 + s.sk * (w.head_dim_qk + w.head_dim_v) * 2 / r + \
+            es = 2 if w.kv_format == "bf16" else 1
+            done_work += s.sq * w.head_dim_qk * 2 + s.sk * (w.head_dim_qk + w.head_dim_v) * es / r + \
                 s.sq * (w.head_dim_v * 2 + 4)
         else:
             done_work += 2.0 * (w.head_dim_qk + w.head_dim_v) * visible_pairs(
@@ -432,7 +479,8 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode")
+    names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode",
+                                                                 "decode_fp8", "decode_paged")
                                                       if n != args.workload])
     results = {}
     clocks = None
@@ -494,7 +542,7 @@ def main():
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": "bf16" if w0.kv_format == "bf16" else f"bf16 q/o, {w0.kv_format} K/V",
             "data": "synthetic (seeded N(0,1) bf16, numpy PCG64)",
             "config": {"workload": args.workload, "shape": workload_desc(w0), "l2": "flushed between steps",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -520,6 +568,10 @@ def workload_desc(w):
         d.update(batch=w.batch, seqlen_q=w.seqlen_q, seqlen_k=w.seqlen_k)
     if w.seqused_k is not None:
         d["seqused_k"] = "uniform [1024, 16384], seeded"
+    if w.kv_format != "bf16":
+        d["kv_cache"] = f"{w.kv_format}, descale per (sequence, KV head)"
+    if w.page_table is not None:
+        d["paged"] = f"page_size {w.page_size}, {w.k.shape[0]} pages, shuffled"
     return d
 
 

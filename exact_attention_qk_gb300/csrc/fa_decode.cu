@@ -10,17 +10,22 @@
 //   * a producer warp streams 64-key K/V tiles with TMA (128-byte swizzle) into
 //     a 2-deep mbarrier ring (three CTAs per SM keep enough bytes in flight);
 //     cache rows at or past seqused_k are never used in arithmetic;
-//   * four compute warps take 16 keys each per tile: QK^T with 16-byte swizzled
-//     shared loads (conflict-free), two keys per lane so each q load feeds both,
-//     packed fp32 FMA (FFMA2), online softmax in base 2 with the scale folded
-//     into q, and P.V with per-lane output columns;
+//   * four compute warps take 16 keys each per tile and run both products on
+//     the tensor cores as warp-level m16n8k16 MMAs with fp32 accumulation:
+//     S^T = K q^T (M = the warp's 16 keys, N = 8 packed query rows) and
+//     O^T += V^T P^T (M = 16 output columns, N = the same 8 rows). Inside each
+//     16-wide K step the fragment's k indices {2t, 2t+1, 2t+8, 2t+9} stand for
+//     the four CONSECUTIVE dims (or keys) 4t..4t+3, the same on both operands,
+//     so every thread reads its K elements with one 32/64-bit shared load per
+//     key; the online softmax (base 2) runs on the S fragments;
 //   * the four warps' (m, l, O) states merge in shared memory at the end and the
 //     CTA writes either the final bf16 O / fp32 LSE or the fp32 split partials.
 // KV-cache forms (the fp8 KV-cache decode and paged-KV passages of the
 // FlashAttention sm_120 pull-request page and of `_flash_attn_fwd`):
 //   * fp8 (E4M3 / E5M2) caches move one byte per element: a 128-byte box row
-//     holds 128 dims; the compute warps widen codes to fp32 in registers, the
-//     K descale is folded into q and the V descale into the written O;
+//     holds 128 dims; codes convert exactly to f16 pairs straight into the MMA
+//     fragments (q is taken to f16 with a power-of-two prescale that keeps it
+//     in range), the K descale scales S and the V descale the written O;
 //   * a paged cache is read page by page: each 64-key tile looks up its page
 //     (or pages, for pages under 64 keys) in the page table and loads from
 //     that page's rows; an index outside the pool reads zeros.
@@ -36,7 +41,8 @@ namespace {
 constexpr int kDecWarps = 4;            // compute warps
 constexpr int kDecThreads = (kDecWarps + 1) * 32;
 constexpr int kTileKeys = 64;
-constexpr int kBoxBytes = kTileKeys * 128;   // one 64-element x 64-key box
+constexpr int kBoxBytes = kTileKeys * 128;   // one 128-byte x 64-key box
+constexpr int kRows = 8;                     // packed query rows per CTA (the MMAs' N)
 
 // Widen four fp8 codes (one 32-bit word, lowest byte first) to fp32 pairs.
 template <int KVT>
@@ -55,38 +61,66 @@ __device__ __forceinline__ void fp8x4_to_f32(uint32_t w, float2& lo, float2& hi)
   hi = __half22float2(*reinterpret_cast<const __half2*>(&h1));
 }
 
-template <int DK, int DV, int NR, int KVT>
+template <int DK, int DV, int KVT>
 struct DecodeCfg {
   static constexpr int ES = KVT ? 1 : 2;          // bytes per K/V element
   static constexpr int KCH = DK * ES / 128;       // 128-byte boxes per K row
   static constexpr int VCH = DV * ES / 128;
   static constexpr int STAGE_BYTES = (KCH + VCH) * kBoxBytes;
-  // Two stages keep the CTA under 70 KB of shared memory, so three CTAs (12
-  // compute warps) share an SM: the QK / softmax / PV chains are latency-bound
-  // and need the extra warps more than each CTA needs a deeper ring.
-  static constexpr int NSTAGE = 2;
+  // Two bf16 stages keep a D<=192 CTA near 70 KB of shared memory, so three
+  // CTAs share an SM; fp8 tiles are half the bytes: four stages keep the same
+  // bytes in flight in the same space.
+  static constexpr int NSTAGE = KVT ? 4 : 2;
   static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
-  static constexpr int Q_BYTES = NR * DK * 4;
-  static constexpr int P_BYTES = kDecWarps * 16 * NR * 4;
-  static constexpr int MERGE_BYTES = kDecWarps * NR * (DV + 2) * 4;
-  static constexpr int OFF_Q = RING_BYTES;
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;
+  static constexpr int P_BYTES = kDecWarps * kRows * 16 * 2;          // per warp: P[row][16 keys], 16-bit
+  static constexpr int MROW = DV + 4;                                 // merge row: O, m, l, pad
+  static constexpr int MERGE_BYTES = kDecWarps * kRows * MROW * 4;
+  static constexpr int OFF_P = RING_BYTES;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
   static constexpr int SMEM = OFF_BAR + 2 * NSTAGE * 8 + 16 + 1024;   // + alignment slack
-  static constexpr int E = DV / 32;                                   // output columns per lane
   static_assert(MERGE_BYTES <= RING_BYTES, "merge area reuses the ring");
-  static_assert(NR * E <= 64, "accumulator budget");
+  static_assert(DK % 16 == 0 && DV % 32 == 0, "MMA shapes");
 };
 
-template <int DK, int DV, int NR, int KVT>
-__global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
+// m16n8k16 MMAs, fp32 accumulate: bf16 or f16 operands (A row-major, B column-major)
+__device__ __forceinline__ void mma_16816_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_16816_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two fp8 codes (the low 16 bits of w; lower byte first) -> f16 pair (exact).
+template <int KVT>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t w) {
+  uint32_t h;
+  if constexpr (KVT == 1) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t}" : "=r"(h) : "r"(w));
+  } else {   // E5M2 is the upper byte of an f16
+    h = __byte_perm(w, 0u, 0x1404);
+  }
+  return h;
+}
+
+template <int DK, int DV, int KVT>
+__global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                   const FwdParams p) {
-  using C = DecodeCfg<DK, DV, NR, KVT>;
+  using C = DecodeCfg<DK, DV, KVT>;
+  constexpr int NR = kRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* q_s = reinterpret_cast<float*>(smem + C::OFF_Q);
-  float* p_s = reinterpret_cast<float*>(smem + C::OFF_P);
+  uint16_t* p_s = reinterpret_cast<uint16_t*>(smem + C::OFF_P);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::NSTAGE;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + C::NSTAGE);
@@ -116,14 +150,12 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
   const int s_lo = min(sk, split * p.split_len);
   const int s_hi = min(sk, (split + 1) * p.split_len);
 
-  // per-row visible key interval [lo, hi] (inclusive) inside this split
-  int lo[NR], hi[NR];
-  int klo = INT32_MAX, khi = -1;
-#pragma unroll
-  for (int rr = 0; rr < NR; ++rr) {
+  // visible key interval [lo, hi] (inclusive) of packed row rr inside this
+  // split; empty (lo > hi) for padding rows and rows that see nothing here
+  auto interval = [&](int rr, int& lo_, int& hi_) {
     const int pr = prow0 + rr;
-    lo[rr] = 1;
-    hi[rr] = 0;
+    lo_ = 1;
+    hi_ = 0;
     if (pr < rows) {
       const int i = pr / p.r;
       int l = s_lo, h = s_hi - 1;
@@ -131,11 +163,19 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
       if (p.wr >= 0) h = min(h, i + off + p.wr);
       l = max(l, 0);
       if (l <= h) {
-        lo[rr] = l;
-        hi[rr] = h;
-        klo = min(klo, l);
-        khi = max(khi, h + 1);
+        lo_ = l;
+        hi_ = h;
       }
+    }
+  };
+  int klo = INT32_MAX, khi = -1;
+#pragma unroll
+  for (int rr = 0; rr < NR; ++rr) {
+    int l, h;
+    interval(rr, l, h);
+    if (l <= h) {
+      klo = min(klo, l);
+      khi = max(khi, h + 1);
     }
   }
 
@@ -186,21 +226,6 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
     }
     *abort_flag = 0;
     fence_barrier_init();
-  }
-  // q rows -> fp32 with the softmax scale (base 2) and the K descale folded in
-  const float qscale = p.scale_log2 * (p.k_descale ? p.k_descale[int64_t(b) * p.hkv + g] : 1.f);
-  for (int idx = tid; idx < NR * DK; idx += blockDim.x) {
-    const int rr = idx / DK, d = idx % DK;
-    float v = 0.f;
-    if (prow0 + rr < rows) {
-      int i, h;
-      row_out(rr, i, h);
-      const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q);
-      v = __bfloat162float(q[(varlen ? 0 : int64_t(b) * p.q_bs) + int64_t(q_row0 + i) * p.q_rs +
-                             int64_t(h) * p.q_hs + d]) *
-          qscale;
-    }
-    q_s[idx] = v;
   }
   __syncthreads();
 
@@ -265,28 +290,74 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
     return;
   }
 
-  // ---------------- compute warps ----------------
-  // Lane = (key slot kq in 0..7, dim quarter qp in 0..3); each lane takes keys
-  // kq and kq + 8 of its warp's 16, so every q load feeds two keys. Products
-  // run as packed fp32 pairs (FFMA2); a 2-level shuffle sums the quarters.
-  const int kq = lane & 7, qp = lane >> 3;
-  const int kw0 = warp * 16 + kq, kw1 = kw0 + 8;   // keys inside a tile
-  constexpr int E = C::E;
-  constexpr int QCH = DK / 32;                     // 8-dim chunks per quarter
-  float2 o[NR][E / 2];
-  float m_run[NR], l_run[NR];
+  // ---------------- compute warps (tensor cores) ----------------
+  // Fragment coordinates of m16n8k16: g8 = lane / 4 picks the row (A) / column
+  // (B) group, t4 = lane % 4 the k pair. k indices {2t, 2t+1, 2t+8, 2t+9} of a
+  // 16-wide step stand for positions 4t..4t+3 (dims in QK, keys in PV).
+  const int g8 = lane >> 2, t4 = lane & 3;
+  constexpr int KS = DK / 16;     // QK k steps
+  constexpr int MT = DV / 16;     // PV m tiles (16 output columns each)
+  const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q);
+
+  // q^T as the B operand of S^T = K q^T: row g8 (zero for padding rows), dims
+  // 16kk + 4t4 .. +3 (b0 = first two, b1 = last two)
+  uint32_t qf[KS][2];
+  float sscale = p.scale_log2 * (p.k_descale ? p.k_descale[int64_t(b) * p.hkv + g] : 1.f);
+  {
+    const bool real = prow0 + g8 < rows;
+    const __nv_bfloat16* qrow = qg;
+    if (real) {
+      int i, h;
+      row_out(g8, i, h);
+      qrow = qg + (varlen ? 0 : int64_t(b) * p.q_bs) + int64_t(q_row0 + i) * p.q_rs + int64_t(h) * p.q_hs;
+    }
+    if constexpr (KVT == 0) {
 #pragma unroll
-  for (int rr = 0; rr < NR; ++rr) {
-    m_run[rr] = -INFINITY;
-    l_run[rr] = 0.f;
+      for (int kk = 0; kk < KS; ++kk) {
+        uint2 w = make_uint2(0u, 0u);
+        if (real) w = *reinterpret_cast<const uint2*>(qrow + 16 * kk + 4 * t4);
+        qf[kk][0] = w.x;
+        qf[kk][1] = w.y;
+      }
+    } else {
+      // f16 operands: q x 2^-e with e >= 0 chosen (per warp; every warp loads
+      // the same rows) so that the largest |q| stays below 2^15
+      float mx = 0.f;
 #pragma unroll
-    for (int e = 0; e < E / 2; ++e) o[rr][e] = make_float2(0.f, 0.f);
+      for (int kk = 0; kk < KS; ++kk) {
+        uint2 w = make_uint2(0u, 0u);
+        if (real) w = *reinterpret_cast<const uint2*>(qrow + 16 * kk + 4 * t4);
+        qf[kk][0] = w.x;
+        qf[kk][1] = w.y;
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16lo_to_f32(w.x)), fabsf(bf16hi_to_f32(w.x))),
+                             fmaxf(fabsf(bf16lo_to_f32(w.y)), fabsf(bf16hi_to_f32(w.y)))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const int e = (mx >= 32768.f) ? ilogbf(mx) - 14 : 0;
+      sscale = ldexpf(sscale, e);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const __half2 hv = __floats2half2_rn(ldexpf(bf16lo_to_f32(qf[kk][u]), -e),
+                                               ldexpf(bf16hi_to_f32(qf[kk][u]), -e));
+          qf[kk][u] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+      }
+    }
   }
-  float* pw = p_s + warp * 16 * NR;
-  const int e0 = lane * E;                       // first output column of this lane
-  // this lane's columns inside a V row: box, 16-byte granule, byte in it
-  const int vbox = e0 * C::ES / 128, vch = (e0 * C::ES % 128) / 16, vbyte = e0 * C::ES % 16;
-  const int key_end = min(sk, s_hi);             // keys at or past this are never used
+  // this thread's two rows (2 t4, 2 t4 + 1) of every S and O fragment
+  int lo0, hi0, lo1, hi1;
+  interval(2 * t4, lo0, hi0);
+  interval(2 * t4 + 1, lo1, hi1);
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // l: this thread's keys only
+  float o[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  uint16_t* pw = p_s + warp * (NR * 16);          // this warp's P[row][16 keys]
+  const int key_end = min(sk, s_hi);              // keys at or past this are never used
+  const int ka = warp * 16 + g8, kb = ka + 8;     // this thread's two S keys (tile rows)
 
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
@@ -298,184 +369,145 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
     const uint8_t* stage = smem + st * C::STAGE_BYTES;
     const int tkey0 = key_base + t * kTileKeys;
 
-    // ---- S = q K^T for two keys over this lane's quarter of the dims ----
-    float2 acc0[NR], acc1[NR];
+    // ---- S^T = K q^T over this warp's 16 keys ----
+    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {
-      acc0[rr] = make_float2(0.f, 0.f);
-      acc1[rr] = make_float2(0.f, 0.f);
-    }
-    if constexpr (KVT != 0) {
-      // fp8: 16 dims (one 16-byte granule) per load, DK/64 granules per quarter
-#pragma unroll
-      for (int c = 0; c < DK / 64; ++c) {
-        const int gg = qp * (DK / 64) + c;
-        const uint8_t* kb = stage + (gg >> 3) * kBoxBytes;
-        const uint4 ka = *reinterpret_cast<const uint4*>(kb + kw0 * 128 + (((gg & 7) ^ (kw0 & 7)) << 4));
-        const uint4 kc = *reinterpret_cast<const uint4*>(kb + kw1 * 128 + (((gg & 7) ^ (kw1 & 7)) << 4));
-        float2 a[8], bb[8];
-        fp8x4_to_f32<KVT>(ka.x, a[0], a[1]);
-        fp8x4_to_f32<KVT>(ka.y, a[2], a[3]);
-        fp8x4_to_f32<KVT>(ka.z, a[4], a[5]);
-        fp8x4_to_f32<KVT>(ka.w, a[6], a[7]);
-        fp8x4_to_f32<KVT>(kc.x, bb[0], bb[1]);
-        fp8x4_to_f32<KVT>(kc.y, bb[2], bb[3]);
-        fp8x4_to_f32<KVT>(kc.z, bb[4], bb[5]);
-        fp8x4_to_f32<KVT>(kc.w, bb[6], bb[7]);
-#pragma unroll
-        for (int rr = 0; rr < NR; ++rr) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float4 qv = *reinterpret_cast<const float4*>(q_s + rr * DK + gg * 16 + u * 4);
-            const float2 q0 = make_float2(qv.x, qv.y), q1 = make_float2(qv.z, qv.w);
-            acc0[rr] = __ffma2_rn(q0, a[2 * u], acc0[rr]);
-            acc0[rr] = __ffma2_rn(q1, a[2 * u + 1], acc0[rr]);
-            acc1[rr] = __ffma2_rn(q0, bb[2 * u], acc1[rr]);
-            acc1[rr] = __ffma2_rn(q1, bb[2 * u + 1], acc1[rr]);
-          }
-        }
-      }
-    } else {
-#pragma unroll
-    for (int c = 0; c < QCH; ++c) {
-      const int gc = qp * QCH + c;
-      const uint8_t* kb = stage + (gc >> 3) * kBoxBytes;
-      const uint4 ka = *reinterpret_cast<const uint4*>(kb + kw0 * 128 + (((gc & 7) ^ (kw0 & 7)) << 4));
-      const uint4 kc = *reinterpret_cast<const uint4*>(kb + kw1 * 128 + (((gc & 7) ^ (kw1 & 7)) << 4));
-      const float2 a0 = make_float2(bf16lo_to_f32(ka.x), bf16hi_to_f32(ka.x));
-      const float2 a1 = make_float2(bf16lo_to_f32(ka.y), bf16hi_to_f32(ka.y));
-      const float2 a2 = make_float2(bf16lo_to_f32(ka.z), bf16hi_to_f32(ka.z));
-      const float2 a3 = make_float2(bf16lo_to_f32(ka.w), bf16hi_to_f32(ka.w));
-      const float2 b0 = make_float2(bf16lo_to_f32(kc.x), bf16hi_to_f32(kc.x));
-      const float2 b1 = make_float2(bf16lo_to_f32(kc.y), bf16hi_to_f32(kc.y));
-      const float2 b2 = make_float2(bf16lo_to_f32(kc.z), bf16hi_to_f32(kc.z));
-      const float2 b3 = make_float2(bf16lo_to_f32(kc.w), bf16hi_to_f32(kc.w));
-#pragma unroll
-      for (int rr = 0; rr < NR; ++rr) {
-        const float4 qa = *reinterpret_cast<const float4*>(q_s + rr * DK + gc * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(q_s + rr * DK + gc * 8 + 4);
-        const float2 q0 = make_float2(qa.x, qa.y), q1 = make_float2(qa.z, qa.w);
-        const float2 q2 = make_float2(qb.x, qb.y), q3 = make_float2(qb.z, qb.w);
-        acc0[rr] = __ffma2_rn(q0, a0, acc0[rr]);
-        acc0[rr] = __ffma2_rn(q1, a1, acc0[rr]);
-        acc0[rr] = __ffma2_rn(q2, a2, acc0[rr]);
-        acc0[rr] = __ffma2_rn(q3, a3, acc0[rr]);
-        acc1[rr] = __ffma2_rn(q0, b0, acc1[rr]);
-        acc1[rr] = __ffma2_rn(q1, b1, acc1[rr]);
-        acc1[rr] = __ffma2_rn(q2, b2, acc1[rr]);
-        acc1[rr] = __ffma2_rn(q3, b3, acc1[rr]);
-      }
-    }
-    }
-    const int j0 = tkey0 + kw0, j1 = tkey0 + kw1;
-    float s0[NR], s1[NR];
-#pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {
-      float x0 = acc0[rr].x + acc0[rr].y, x1 = acc1[rr].x + acc1[rr].y;
-      x0 += __shfl_xor_sync(0xffffffffu, x0, 8);
-      x1 += __shfl_xor_sync(0xffffffffu, x1, 8);
-      x0 += __shfl_xor_sync(0xffffffffu, x0, 16);
-      x1 += __shfl_xor_sync(0xffffffffu, x1, 16);
-      s0[rr] = (j0 >= lo[rr] && j0 <= hi[rr]) ? x0 : -INFINITY;
-      s1[rr] = (j1 >= lo[rr] && j1 <= hi[rr]) ? x1 : -INFINITY;
-    }
-    // ---- online softmax over this warp's 16 keys (base 2) ----
-#pragma unroll
-    for (int rr = 0; rr < NR; ++rr) {
-      float bm = fmaxf(s0[rr], s1[rr]);
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-      const float m_new = fmaxf(m_run[rr], bm);
-      float factor = 1.f, p0 = 0.f, p1 = 0.f;
-      if (m_new != -INFINITY) {
-        factor = ex2_approx(m_run[rr] - m_new);
-        p0 = ex2_approx(s0[rr] - m_new);
-        p1 = ex2_approx(s1[rr] - m_new);
-      }
-      m_run[rr] = m_new;
-      l_run[rr] = l_run[rr] * factor + (p0 + p1);
-      const float2 f2 = make_float2(factor, factor);
-#pragma unroll
-      for (int e = 0; e < E / 2; ++e) o[rr][e] = __fmul2_rn(o[rr][e], f2);
-      if (qp == 0) {
-        pw[kq * NR + rr] = p0;
-        pw[(kq + 8) * NR + rr] = p1;
-      }
-    }
-    __syncwarp();
-    // ---- O += P V over the keys this warp owns that exist ----
-    const int wkey0 = tkey0 + warp * 16;
-    const int kbeg = max(0, klo - wkey0);
-    const int kend = min(16, key_end - wkey0);
-    auto pv_key = [&](int k2) {
-      const int key = warp * 16 + k2;
-      const uint8_t* vp = stage + (C::KCH + vbox) * kBoxBytes + key * 128 + (((vch ^ (key & 7)) << 4) + vbyte);
-      float2 vf[E / 2];
-      if constexpr (KVT != 0 && E == 4) {
-        fp8x4_to_f32<KVT>(*reinterpret_cast<const uint32_t*>(vp), vf[0], vf[1]);
-      } else if constexpr (KVT != 0 && E == 8) {
-        const uint2 w = *reinterpret_cast<const uint2*>(vp);
-        fp8x4_to_f32<KVT>(w.x, vf[0], vf[1]);
-        fp8x4_to_f32<KVT>(w.y, vf[2], vf[3]);
-      } else if constexpr (E == 2) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
-        vf[0] = make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
-      } else if constexpr (E == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(vp);
-        vf[0] = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
-        vf[1] = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
+    for (int kk = 0; kk < KS; ++kk) {
+      if constexpr (KVT == 0) {
+        // dims 16kk + 4t4 .. +3: 8 bytes in box kk/4, granule 2(kk%4) + t4/2
+        const int gran = 2 * (kk & 3) + (t4 >> 1), byt = 8 * (t4 & 1);
+        const uint8_t* kbox = stage + (kk >> 2) * kBoxBytes;
+        const uint2 x = *reinterpret_cast<const uint2*>(kbox + ka * 128 + ((gran ^ (ka & 7)) << 4) + byt);
+        const uint2 y = *reinterpret_cast<const uint2*>(kbox + kb * 128 + ((gran ^ (kb & 7)) << 4) + byt);
+        mma_16816_bf16(sacc, x.x, y.x, x.y, y.y, qf[kk][0], qf[kk][1]);
       } else {
-        const uint4 w = *reinterpret_cast<const uint4*>(vp);
-        vf[0] = make_float2(bf16lo_to_f32(w.x), bf16hi_to_f32(w.x));
-        vf[1] = make_float2(bf16lo_to_f32(w.y), bf16hi_to_f32(w.y));
-        vf[2] = make_float2(bf16lo_to_f32(w.z), bf16hi_to_f32(w.z));
-        vf[3] = make_float2(bf16lo_to_f32(w.w), bf16hi_to_f32(w.w));
+        // dims 16kk + 4t4 .. +3: 4 bytes in box kk/8, granule kk%8
+        const uint8_t* kbox = stage + (kk >> 3) * kBoxBytes;
+        const uint32_t x = *reinterpret_cast<const uint32_t*>(kbox + ka * 128 + (((kk & 7) ^ (ka & 7)) << 4) + 4 * t4);
+        const uint32_t y = *reinterpret_cast<const uint32_t*>(kbox + kb * 128 + (((kk & 7) ^ (kb & 7)) << 4) + 4 * t4);
+        mma_16816_f16(sacc, fp8x2_to_f16x2<KVT>(x), fp8x2_to_f16x2<KVT>(y), fp8x2_to_f16x2<KVT>(x >> 16),
+                      fp8x2_to_f16x2<KVT>(y >> 16), qf[kk][0], qf[kk][1]);
       }
+    }
+    // sacc: (key ka, row 2t4), (ka, 2t4+1), (kb, 2t4), (kb, 2t4+1); base-2 scores
+    const int ja = tkey0 + ka, jb = tkey0 + kb;
+    const float sa0 = (ja >= lo0 && ja <= hi0) ? sacc[0] * sscale : -INFINITY;
+    const float sa1 = (ja >= lo1 && ja <= hi1) ? sacc[1] * sscale : -INFINITY;
+    const float sb0 = (jb >= lo0 && jb <= hi0) ? sacc[2] * sscale : -INFINITY;
+    const float sb1 = (jb >= lo1 && jb <= hi1) ? sacc[3] * sscale : -INFINITY;
+    // ---- online softmax over the warp's 16 keys (rows 2t4 and 2t4+1) ----
+    float bm0 = fmaxf(sa0, sb0), bm1 = fmaxf(sa1, sb1);
 #pragma unroll
-      for (int rr = 0; rr < NR; ++rr) {
-        const float pr = pw[k2 * NR + rr];
-        const float2 p2 = make_float2(pr, pr);
+    for (int x = 4; x < 32; x <<= 1) {
+      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
+      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
+    }
+    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+    float f0 = 1.f, f1 = 1.f, pa0 = 0.f, pb0 = 0.f, pa1 = 0.f, pb1 = 0.f;
+    if (mn0 != -INFINITY) {
+      f0 = ex2_approx(m0 - mn0);
+      pa0 = ex2_approx(sa0 - mn0);
+      pb0 = ex2_approx(sb0 - mn0);
+    }
+    if (mn1 != -INFINITY) {
+      f1 = ex2_approx(m1 - mn1);
+      pa1 = ex2_approx(sa1 - mn1);
+      pb1 = ex2_approx(sb1 - mn1);
+    }
+    m0 = mn0;
+    m1 = mn1;
+    l0 = l0 * f0 + (pa0 + pb0);
+    l1 = l1 * f1 + (pa1 + pb1);
+    if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
 #pragma unroll
-        for (int e = 0; e < E / 2; ++e) o[rr][e] = __ffma2_rn(p2, vf[e], o[rr][e]);
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= f0;
+        o[mt][1] *= f1;
+        o[mt][2] *= f0;
+        o[mt][3] *= f1;
+      }
+    }
+    // P -> shared memory as P[row][key] (16-bit: bf16 with bf16 V, f16 with fp8 V)
+    auto p16 = [](float v) -> uint16_t {
+      if constexpr (KVT == 0) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      } else {
+        return __half_as_ushort(__float2half_rn(v));
       }
     };
-    if (kbeg == 0 && kend == 16) {
-      // all 16 keys exist (the common case): unrolled so the shared loads overlap
-#pragma unroll 4
-      for (int k2 = 0; k2 < 16; ++k2) pv_key(k2);
-    } else {
-      for (int k2 = kbeg; k2 < kend; ++k2) pv_key(k2);
+    pw[(2 * t4) * 16 + g8] = p16(pa0);
+    pw[(2 * t4 + 1) * 16 + g8] = p16(pa1);
+    pw[(2 * t4) * 16 + g8 + 8] = p16(pb0);
+    pw[(2 * t4 + 1) * 16 + g8 + 8] = p16(pb1);
+    __syncwarp();
+    // P^T as the B operand of O^T += V^T P^T: row g8, keys 4t4 .. +3
+    const uint2 pf = *reinterpret_cast<const uint2*>(pw + g8 * 16 + 4 * t4);
+    // ---- O^T += V^T P^T: this thread's V rows are keys 4t4 .. +3 of the warp ----
+    const int kv0 = warp * 16 + 4 * t4;
+    // keys at or past key_end may hold anything (NaN included): zero them
+    const bool vtail = tkey0 + warp * 16 + 16 > key_end;
+#pragma unroll
+    for (int j = 0; j < DV / 32; ++j) {
+      // columns 32j + 4g8 .. +3: m tile 2j holds (4g8, 4g8+1), m tile 2j+1 (4g8+2, 4g8+3)
+      if constexpr (KVT == 0) {
+        const int gran = 4 * (j & 1) + (g8 >> 1), byt = 8 * (g8 & 1);
+        const uint8_t* vbox = stage + (C::KCH + (j >> 1)) * kBoxBytes;
+        uint2 r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int kr = kv0 + i;
+          r[i] = *reinterpret_cast<const uint2*>(vbox + kr * 128 + ((gran ^ (kr & 7)) << 4) + byt);
+          if (vtail && tkey0 + kr >= key_end) r[i] = make_uint2(0u, 0u);
+        }
+        mma_16816_bf16(o[2 * j], __byte_perm(r[0].x, r[1].x, 0x5410), __byte_perm(r[0].x, r[1].x, 0x7632),
+                       __byte_perm(r[2].x, r[3].x, 0x5410), __byte_perm(r[2].x, r[3].x, 0x7632), pf.x, pf.y);
+        mma_16816_bf16(o[2 * j + 1], __byte_perm(r[0].y, r[1].y, 0x5410), __byte_perm(r[0].y, r[1].y, 0x7632),
+                       __byte_perm(r[2].y, r[3].y, 0x5410), __byte_perm(r[2].y, r[3].y, 0x7632), pf.x, pf.y);
+      } else {
+        const int gran = 2 * (j & 3) + (g8 >> 2), byt = 4 * (g8 & 3);
+        const uint8_t* vbox = stage + (C::KCH + (j >> 2)) * kBoxBytes;
+        uint32_t r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int kr = kv0 + i;
+          r[i] = *reinterpret_cast<const uint32_t*>(vbox + kr * 128 + ((gran ^ (kr & 7)) << 4) + byt);
+          if (vtail && tkey0 + kr >= key_end) r[i] = 0u;
+        }
+        // byte pairs (key 4t4 + 2c, key 4t4 + 2c + 1) of one column
+        const uint32_t c01a = __byte_perm(r[0], r[1], 0x5140), c23a = __byte_perm(r[0], r[1], 0x7362);
+        const uint32_t c01b = __byte_perm(r[2], r[3], 0x5140), c23b = __byte_perm(r[2], r[3], 0x7362);
+        mma_16816_f16(o[2 * j], fp8x2_to_f16x2<KVT>(c01a), fp8x2_to_f16x2<KVT>(c01a >> 16),
+                      fp8x2_to_f16x2<KVT>(c01b), fp8x2_to_f16x2<KVT>(c01b >> 16), pf.x, pf.y);
+        mma_16816_f16(o[2 * j + 1], fp8x2_to_f16x2<KVT>(c23a), fp8x2_to_f16x2<KVT>(c23a >> 16),
+                      fp8x2_to_f16x2<KVT>(c23b), fp8x2_to_f16x2<KVT>(c23b >> 16), pf.x, pf.y);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
   }
 
   // ---- merge the four warps' states ----
-  float lsum[NR];
 #pragma unroll
-  for (int rr = 0; rr < NR; ++rr) {
-    float l = qp == 0 ? l_run[rr] : 0.f;
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    lsum[rr] = l;
+  for (int x = 4; x < 32; x <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, x);
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");   // ring no longer read
-  float* mg = reinterpret_cast<float*>(smem);          // [warp][rr][DV + 2]
+  float* mg = reinterpret_cast<float*>(smem);          // [warp][row][DV + 4]
+  {
+    float* r0 = mg + (warp * NR + 2 * t4) * C::MROW;
+    float* r1 = r0 + C::MROW;
 #pragma unroll
-  for (int rr = 0; rr < NR; ++rr) {
-    float* row = mg + (warp * NR + rr) * (DV + 2);
-#pragma unroll
-    for (int e = 0; e < E / 2; ++e) {
-      row[e0 + 2 * e] = o[rr][e].x;
-      row[e0 + 2 * e + 1] = o[rr][e].y;
+    for (int j = 0; j < DV / 32; ++j) {
+      const int c = 32 * j + 4 * g8;
+      *reinterpret_cast<float4*>(r0 + c) = make_float4(o[2 * j][0], o[2 * j][2], o[2 * j + 1][0], o[2 * j + 1][2]);
+      *reinterpret_cast<float4*>(r1 + c) = make_float4(o[2 * j][1], o[2 * j][3], o[2 * j + 1][1], o[2 * j + 1][3]);
     }
-    if (lane == 0) {
-      row[DV] = m_run[rr];
-      row[DV + 1] = lsum[rr];
+    if (g8 == 0) {
+      r0[DV] = m0;
+      r0[DV + 1] = l0;
+      r1[DV] = m1;
+      r1[DV + 1] = l1;
     }
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
@@ -486,12 +518,12 @@ __global__ void __launch_bounds__(kDecThreads, (NR <= 4) ? 3 : 2)
     if (prow0 + rr >= rows) continue;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mg[(w * NR + rr) * (DV + 2) + DV]);
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mg[(w * NR + rr) * C::MROW + DV]);
     float L = 0.f, acc = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) {
-        const float* row = mg + (w * NR + rr) * (DV + 2);
+        const float* row = mg + (w * NR + rr) * C::MROW;
         const float sc = ex2_approx(row[DV] - M);
         L += row[DV + 1] * sc;
         acc += row[d] * sc;
@@ -577,30 +609,19 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   if (p.lse && lane == 0) p.lse[lse_base] = lse;
 }
 
-template <int DK, int DV, int NR, int KVT>
+template <int DK, int DV, int KVT = 0>
 cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
                             cudaStream_t stream) {
-  using C = DecodeCfg<DK, DV, NR, KVT>;
-  auto kern = decode_kernel<DK, DV, NR, KVT>;
+  using C = DecodeCfg<DK, DV, KVT>;
+  auto kern = decode_kernel<DK, DV, KVT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
+  // packed rows (query rows x heads per KV head) in chunks of kRows over grid.y
   const int rows = p.max_seqlen_q * p.r;
-  const int chunks = (rows + NR - 1) / NR;
+  const int chunks = (rows + kRows - 1) / kRows;
   dim3 grid(p.num_splits, p.hkv * chunks, p.batch);
   kern<<<grid, kDecThreads, C::SMEM, stream>>>(mk, mv, p);
   return cudaGetLastError();
-}
-
-template <int DK, int DV, int KVT = 0>
-cudaError_t launch_decode_nr(const FwdParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
-                             cudaStream_t stream) {
-  // rows per CTA: up to 8 (more would spill the accumulators); larger row
-  // counts are split into chunks of 8 over grid.y
-  const int rows = p.max_seqlen_q * p.r;
-  if (rows <= 1) return launch_decode_t<DK, DV, 1, KVT>(p, mk, mv, stream);
-  if (rows <= 2) return launch_decode_t<DK, DV, 2, KVT>(p, mk, mv, stream);
-  if (rows <= 4) return launch_decode_t<DK, DV, 4, KVT>(p, mk, mv, stream);
-  return launch_decode_t<DK, DV, 8, KVT>(p, mk, mv, stream);
 }
 
 }  // namespace
@@ -615,19 +636,19 @@ int decode_max_rows() { return 16; }
 cudaError_t launch_decode(const FwdParams& p, int dk, int dv, const CUtensorMap& mk, const CUtensorMap& mv,
                           cudaStream_t stream) {
   if (p.kv_type == 1) {
-    if (dk == 128 && dv == 128) return launch_decode_nr<128, 128, 1>(p, mk, mv, stream);
-    if (dk == 256 && dv == 256) return launch_decode_nr<256, 256, 1>(p, mk, mv, stream);
+    if (dk == 128 && dv == 128) return launch_decode_t<128, 128, 1>(p, mk, mv, stream);
+    if (dk == 256 && dv == 256) return launch_decode_t<256, 256, 1>(p, mk, mv, stream);
     return cudaErrorInvalidValue;
   }
   if (p.kv_type == 2) {
-    if (dk == 128 && dv == 128) return launch_decode_nr<128, 128, 2>(p, mk, mv, stream);
-    if (dk == 256 && dv == 256) return launch_decode_nr<256, 256, 2>(p, mk, mv, stream);
+    if (dk == 128 && dv == 128) return launch_decode_t<128, 128, 2>(p, mk, mv, stream);
+    if (dk == 256 && dv == 256) return launch_decode_t<256, 256, 2>(p, mk, mv, stream);
     return cudaErrorInvalidValue;
   }
-  if (dk == 64 && dv == 64) return launch_decode_nr<64, 64>(p, mk, mv, stream);
-  if (dk == 128 && dv == 128) return launch_decode_nr<128, 128>(p, mk, mv, stream);
-  if (dk == 192 && dv == 128) return launch_decode_nr<192, 128>(p, mk, mv, stream);
-  if (dk == 256 && dv == 256) return launch_decode_nr<256, 256>(p, mk, mv, stream);
+  if (dk == 64 && dv == 64) return launch_decode_t<64, 64>(p, mk, mv, stream);
+  if (dk == 128 && dv == 128) return launch_decode_t<128, 128>(p, mk, mv, stream);
+  if (dk == 192 && dv == 128) return launch_decode_t<192, 128>(p, mk, mv, stream);
+  if (dk == 256 && dv == 256) return launch_decode_t<256, 256>(p, mk, mv, stream);
   return cudaErrorInvalidValue;
 }
 

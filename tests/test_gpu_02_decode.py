@@ -65,8 +65,11 @@ def test_splitkv_partials_and_combine():
     fin = np.isfinite(l_s)
     assert (np.isneginf(lpg[~fin])).all()          # empty splits
     assert np.abs(lpg[fin] - l_s[fin]).max() <= gu.TOL_MAX_LSE
-    # partial O rows of empty splits are 0; others within fp32 tolerance
-    assert np.abs(opg - o_s).max() <= 2e-3
+    # partial O rows of empty splits are 0; the others carry the rounding of P
+    # to bf16 ahead of the P.V product (as every P.V here does), so they meet
+    # the output tolerances
+    d = np.abs(opg - o_s)
+    assert d.max() <= gu.TOL_MAX_O and d.mean() <= gu.TOL_MEAN_O
     out, lse = fa.fa_combine(op, lp)
     o_ref, l_ref = oracle.attention_forward(w.q, w.k, w.v, scale=w.softmax_scale, seqused_k=w.seqused_k)
     print(gu.compare(out, lse, o_ref, l_ref, "combine"))
