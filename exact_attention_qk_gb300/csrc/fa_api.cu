@@ -87,8 +87,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0; }
 bool stride_ok_bytes(int64_t s, int esize) { return s >= 0 && (s * esize) % 16 == 0; }
 bool fp8_kv(const fa_fwd_args* a) { return a->kv_format == FA_KV_E4M3 || a->kv_format == FA_KV_E5M2; }
-// fp8 and paged caches run on the decode kernel whatever the query length
-bool kv_special(const fa_fwd_args* a) { return fp8_kv(a) || a->page_table != nullptr; }
+// fp8 caches run on the decode kernel whatever the query length
+bool kv_special(const fa_fwd_args* a) { return fp8_kv(a); }
 
 struct Resolved {
   bool varlen;
@@ -269,8 +269,10 @@ void fill_common(FwdParams* p, const fa_fwd_args* a, const Resolved& r) {
 bool kv_maps(const fa_fwd_args* a, const Resolved& r, int box_rows, CUtensorMap* mk, CUtensorMap* mv) {
   const int es = fp8_kv(a) ? 1 : 2;
   if (a->page_table != nullptr) {
-    // pools: (d, page_size, heads, pages); a load moves at most one page
-    const int rows = box_rows < a->page_size ? box_rows : a->page_size;
+    // pools: (d, page_size, heads, pages); a load moves a piece of one page:
+    // box_rows when the page size is a multiple of it, else 64, else a page
+    const int ps = a->page_size;
+    const int rows = (ps % box_rows == 0) ? box_rows : (ps % 64 == 0 ? 64 : ps);
     return make_map(mk, a->k, a->head_dim_qk, a->page_size, a->num_heads_kv, a->num_pages, a->k_row_stride,
                     a->k_head_stride, a->k_batch_stride, rows, es) &&
            make_map(mv, a->v, a->head_dim_v, a->page_size, a->num_heads_kv, a->num_pages, a->v_row_stride,

@@ -208,6 +208,27 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   return B;
 }
 
+// Key block n of sequence b from a paged cache ("interface.py",
+// `_flash_attn_fwd`: k/v (num_pages, page_size, Hkv, D), page_table
+// (batch, max_pages)): key j is row j % page_size of page
+// page_table[b, j / page_size]. The block is moved in pieces that each lie
+// inside one page (128 rows when page_size is a multiple of 128, else 64, else
+// page_size rows); a page index outside the pool reads zeros.
+template <int NCH>
+__device__ __forceinline__ void load_paged(const FwdParams& p, int b, int n, uint8_t* dst, const CUtensorMap* map,
+                                           uint64_t* bar, int g) {
+  const int ps = p.page_size;
+  const int rpl = (ps % kBN == 0) ? kBN : (ps % 64 == 0 ? 64 : ps);
+  for (int sub = 0; sub < kBN; sub += rpl) {
+    const int key = n * kBN + sub;
+    const int pi = key / ps;
+    const int page = pi < p.max_pages ? p.page_table[int64_t(b) * p.max_pages + pi] : p.num_pages;
+    const int row = key - pi * ps;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) tma_load_4d(dst + c * kChunkBytes + sub * 128, map, bar, c * 64, row, g, page);
+  }
+}
+
 // Spin (bounded, ignoring the abort flag) until the given phase completed:
 // used to drain copies / MMAs in flight before the CTA exits.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -324,9 +345,13 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             if (kc >= Cfg::KST && !wait_release(kc - Cfg::KST, B.k_empty, Cfg::KST)) { ok = false; break; }
             uint8_t* dst = smem + Cfg::OFF_K + st * Cfg::K_BYTES;
             mbar_arrive_expect_tx(&B.k_full[st], Cfg::K_BYTES);
+            if (p.page_table == nullptr) {
 #pragma unroll
-            for (int c = 0; c < Cfg::KCH; ++c)
-              tma_load_4d(dst + c * kChunkBytes, &mapK, &B.k_full[st], c * 64, T.k_row0 + n * kBN, T.g, cb);
+              for (int c = 0; c < Cfg::KCH; ++c)
+                tma_load_4d(dst + c * kChunkBytes, &mapK, &B.k_full[st], c * 64, T.k_row0 + n * kBN, T.g, cb);
+            } else {
+              load_paged<Cfg::KCH>(p, T.b, n, dst, &mapK, &B.k_full[st], T.g);
+            }
             ++kc;
           }
         } else {
@@ -338,9 +363,13 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
               w = kc < Cfg::VST || wait_release(kc - Cfg::VST, B.v_empty, Cfg::VST);
               if (w) {
                 mbar_arrive_expect_tx(&B.v_full[st], Cfg::V_BYTES);
+                if (p.page_table == nullptr) {
 #pragma unroll
-                for (int c = 0; c < Cfg::VCH; ++c)
-                  tma_load_4d(dst + c * kChunkBytes, &mapV, &B.v_full[st], c * 64, T.k_row0 + n * kBN, T.g, cb);
+                  for (int c = 0; c < Cfg::VCH; ++c)
+                    tma_load_4d(dst + c * kChunkBytes, &mapV, &B.v_full[st], c * 64, T.k_row0 + n * kBN, T.g, cb);
+                } else {
+                  load_paged<Cfg::VCH>(p, T.b, n, dst, &mapV, &B.v_full[st], T.g);
+                }
               }
             }
             if (!__shfl_sync(vmask, w ? 1 : 0, 0)) { ok = false; break; }

@@ -97,8 +97,10 @@ enum {
  *   max_pages_per_seq * page_size (seqlen_k is ignored); seqused_k gives the
  *   lengths. page_size: 8, 16, 32 or a multiple of 64. Not with cu_seqlens
  *   (FA_ERR_INVALID_ARG). A page index outside [0, num_pages) reads zeros.
- *   Both forms run on the split-KV decode kernel, for any number of query rows
- *   (correct for prefill shapes too, but built for few rows per KV head).
+ *   An fp8 cache runs on the split-KV decode kernel for any number of query
+ *   rows (correct for prefill shapes too, but built for few rows per KV head);
+ *   a paged bf16 cache runs on the same kernels as the plain layout (decode
+ *   for few rows per KV head, the tensor-memory prefill kernel otherwise).
  */
 enum {
   FA_KV_BF16 = 0,   /* 2-byte bfloat16 elements                                 */

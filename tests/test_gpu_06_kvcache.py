@@ -68,6 +68,23 @@ def test_paged_page_size_8_and_32():
         print(gu.check_workload(inputs.to_paged(w, ps)))
 
 
+@pytest.mark.parametrize("page_size", [16, 64, 128, 192, 256])
+@pytest.mark.parametrize("d,dv", [(64, 64), (128, 128), (192, 128), (256, 256)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_prefill(page_size, d, dv, causal):
+    # prefill shapes with a page table run on the tensor-memory prefill kernel;
+    # 192-key pages are moved in 64-row pieces, smaller pages one page a piece
+    w = inputs.batched("pgpf", 240 + d, 2, 300, 768, 4, 2, d, dv, causal=causal,
+                       seqused_k=np.array([768, 517], np.int32))
+    print(gu.check_workload(inputs.to_paged(w, page_size)))
+
+
+def test_paged_prefill_window_and_gqa():
+    w = inputs.batched("pgpfw", 245, 2, 400, 1024, 16, 2, 128, 128, causal=True, window_left=200,
+                       seqused_k=np.array([1024, 700], np.int32))
+    print(gu.check_workload(inputs.to_paged(w, 64)))
+
+
 def test_paged_fp8():
     w = inputs.fp8_batched("pgfp8", 232, 3, 1, 1024, 8, 2, 128, "e4m3", seqused_k=np.array([1024, 200, 700], np.int32))
     print(gu.check_workload(inputs.to_paged(w, 128)))
