@@ -92,13 +92,15 @@ def is_decode(name):
 
 
 # ------------------------------------------------------------- ncu traffic ----
-def kernel_source_hash() -> str:
-    """sha256 over the CUDA sources (a changed kernel invalidates old counters)."""
+def kernel_source_hash(files=None) -> str:
+    """sha256 over CUDA sources (a changed kernel invalidates old counters):
+    the named files of the library's csrc folder, or all of them."""
     import glob
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_qk_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*"))):
+    paths = sorted(glob.glob(os.path.join(csrc, "*"))) if files is None else [os.path.join(csrc, f) for f in files]
+    for f in paths:
         h.update(os.path.basename(f).encode())
         h.update(open(f, "rb").read())
     return h.hexdigest()
@@ -106,7 +108,8 @@ def kernel_source_hash() -> str:
 
 def measured_traffic(workload: str):
     """DRAM bytes per launch of the workload's dominant kernel from the committed
-    ncu summary, or None when that capture predates the current kernel sources."""
+    ncu summary, or None when that capture predates the kernel's current sources
+    (each entry names the source files of its kernel and their hash)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -115,7 +118,7 @@ def measured_traffic(workload: str):
     except Exception:
         return None
     e = d.get("workloads", {}).get(workload)
-    if not e or d.get("source_sha256") != kernel_source_hash():
+    if not e or not e.get("sources") or e.get("source_sha256") != kernel_source_hash(e["sources"]):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -480,7 +483,7 @@ def main():
         torch.cuda.synchronize()
 
     names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode",
-                                                                 "decode_fp8", "decode_paged")
+                                                                 "decode_fp8", "decode_paged", "causal_paged")
                                                       if n != args.workload])
     results = {}
     clocks = None

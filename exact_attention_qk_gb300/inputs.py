@@ -28,6 +28,8 @@ passages of the FlashAttention pages):
                 and per-(sequence, KV head) descales
   decode_paged  the decode shape with the cache split into 128-key pages held
                 in a shuffled page pool, located through a page table
+  causal_paged  the causal prefill workload with its K/V cache paged the same way
+  decode_*_small  the first 16 sequences of a decode workload (profiling cases)
 """
 from __future__ import annotations
 
@@ -273,6 +275,13 @@ def workload(name: str) -> Workload:
         return fp8_batched("decode_fp8", 5, 64, 1, 16384, 32, 8, 128, "e4m3", seqused_k=decode_seqused())
     if name == "decode_paged":
         return to_paged(workload("decode"), 128)
+    if name == "causal_paged":
+        # the causal prefill workload with its K/V cache in shuffled 128-key pages
+        return to_paged(workload("causal"), 128)
+    if name == "decode_fp8_small":
+        return fp8_batched("decode_fp8_small", 5, 16, 1, 16384, 32, 8, 128, "e4m3", seqused_k=decode_seqused()[:16])
+    if name == "decode_paged_small":
+        return to_paged(workload("decode_small"), 128)
     if name == "decode_small":
         # the decode shape with 16 sequences (about 1 GB of cache): a profiling case
         return batched("decode_small", 5, 16, 1, 16384, 32, 8, 128, 128, seqused_k=decode_seqused()[:16])
@@ -280,4 +289,5 @@ def workload(name: str) -> Workload:
 
 
 WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode", "decode_small",
-             "decode_fp8", "decode_paged")
+             "decode_fp8", "decode_paged", "causal_paged",
+             "decode_fp8_small", "decode_paged_small")
