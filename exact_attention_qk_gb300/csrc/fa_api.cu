@@ -83,6 +83,24 @@ bool make_map(CUtensorMap* m, const void* base, int64_t d, int64_t rows, int64_t
   return r == CUDA_SUCCESS;
 }
 
+// 5-D bf16 map of q for pack-GQA: (d, head within the KV group, row, KV head,
+// batch) with a box of (64, r, 128 / r, 1, 1), so one box is 128 tile rows
+// ordered (query row, head) with the r heads of a row adjacent.
+bool make_map_packed_q(CUtensorMap* m, const void* base, int64_t d, int64_t r, int64_t rows, int64_t hkv,
+                       int64_t batch, int64_t row_stride, int64_t head_stride, int64_t batch_stride) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)r, (cuuint64_t)rows, (cuuint64_t)hkv, (cuuint64_t)batch};
+  cuuint64_t strides[4] = {(cuuint64_t)(head_stride * 2), (cuuint64_t)(row_stride * 2),
+                           (cuuint64_t)(head_stride * r * 2), (cuuint64_t)(batch_stride * 2)};
+  cuuint32_t box[5] = {64, (cuuint32_t)r, (cuuint32_t)(128 / r), 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult res = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0; }
 bool stride_ok_bytes(int64_t s, int esize) { return s >= 0 && (s * esize) % 16 == 0; }
@@ -172,6 +190,10 @@ int check_tensors(const fa_fwd_args* a, bool need_out) {
 bool decode_shaped(const fa_fwd_args* a, const Resolved& r) {
   return static_cast<long long>(r.rows_q) * r.r <= decode_max_rows();
 }
+
+// Prefill packs the r q heads of a KV head into the tile rows when r > 1
+// divides 128 and no sequence has more than 128 query rows.
+bool pack_gqa(const Resolved& r) { return r.r > 1 && 128 % r.r == 0 && r.rows_q <= 128; }
 
 int resolve_splits(const fa_fwd_args* a, const Resolved& r, int num_sms) {
   if (a->num_splits > 0) return a->num_splits;
@@ -308,21 +330,30 @@ int run_prefill(const fa_fwd_args* a, const Resolved& r, void* ws, const WsLayou
   fill_common(&p, a, r);
   if (!p.status) return FA_ERR_CUDA;
   const int rpt = prefill_rows_per_tile(a->head_dim_qk, a->head_dim_v);
+  // Pack-GQA for short query sequences: with at most 128 query rows a head's
+  // tile would be mostly empty and each K/V block would be read once per head
+  p.pack = pack_gqa(r) ? 1 : 0;
+  const int mult = p.pack ? r.r : 1;
   if (r.varlen) {
     p.tile_prefix = reinterpret_cast<int*>(static_cast<char*>(ws) + w.prefix_off);
     cudaError_t e = launch_varlen_prepare(p, rpt, st);
     if (e != cudaSuccess) return FA_ERR_LAUNCH;
   } else {
-    p.m_blocks = (a->seqlen_q + rpt - 1) / rpt;
-    p.num_tiles = p.m_blocks * a->num_heads_q * a->batch;
+    p.m_blocks = (a->seqlen_q * mult + rpt - 1) / rpt;
+    p.num_tiles = p.m_blocks * (p.pack ? a->num_heads_kv : a->num_heads_q) * a->batch;
   }
   CUtensorMap mq, mk, mv;
   const int64_t qrows = r.varlen ? a->total_q : a->seqlen_q;
   const int64_t qb = r.varlen ? 1 : a->batch;
   const int64_t qbs = r.varlen ? a->q_row_stride * (qrows > 0 ? qrows : 1) : a->q_batch_stride;
-  if (!make_map(&mq, a->q, a->head_dim_qk, qrows, a->num_heads_q, qb, a->q_row_stride, a->q_head_stride,
-                qbs > 0 ? qbs : 8, 128))
+  if (p.pack) {
+    if (!make_map_packed_q(&mq, a->q, a->head_dim_qk, r.r, qrows, a->num_heads_kv, qb, a->q_row_stride,
+                           a->q_head_stride, qbs > 0 ? qbs : 8))
+      return FA_ERR_CUDA;
+  } else if (!make_map(&mq, a->q, a->head_dim_qk, qrows, a->num_heads_q, qb, a->q_row_stride, a->q_head_stride,
+                       qbs > 0 ? qbs : 8, 128)) {
     return FA_ERR_CUDA;
+  }
   if (!kv_maps(a, r, 128, &mk, &mv)) return FA_ERR_CUDA;
   const int sms = device_sms();
   if (sms <= 0) return FA_ERR_CUDA;

@@ -31,7 +31,8 @@ struct FwdParams {
   int num_splits;                // decode grid extent over key splits (>= 1)
   int split_len;                 // keys per split (covers every key when num_splits == 1)
   int write_partial;             // decode: 1 = fp32 partials at [split], 0 = final bf16 O / LSE
-  int m_blocks;                  // batched prefill: ceil(seqlen_q / tile rows)
+  int pack;                      // prefill: 1 = tile rows are (query row, head) pairs of one KV head
+  int m_blocks;                  // batched prefill: ceil(tile rows of a sequence / rows per tile)
   int num_tiles;                 // batched prefill: total work tiles
   int* status;                   // device status word
   unsigned long long timeout_ns;

@@ -75,14 +75,20 @@ struct PrefillCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
+// Pack-GQA ("interface.py", pack_gqa; the sm_120 PR page, Pack-GQA: the q heads
+// sharing a KV head fold into the row axis): with p.pack, tile row t of a
+// sequence is query row t / r of q head g*r + t % r, so one tile reads each
+// K/V block once for r heads. Otherwise tile rows are query rows of head h.
 struct Tile {
-  int b, h, g, mb;
+  int b, h, g, mb;      // h: q head (unpacked) or the KV head (packed)
   int q_row0, k_row0;   // first row of the sequence in q's / k's row axis
   int sq, sk;
+  int rows;             // tile rows of the sequence: sq, or sq * r packed
 };
 
 struct Range {
-  int r0;       // first query row of this Q tile inside the sequence
+  int r0;       // first tile row of this Q tile inside the sequence
+  int i0, i1;   // first and last query row it covers
   bool active;  // the Q tile has rows
   int nlo, nhi; // key blocks [nlo, nhi) hold visible keys; empty when nhi <= nlo
 };
@@ -99,11 +105,12 @@ template <int ROWS_PER_TILE>
 __device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
   if (p.cu_seqlens_q == nullptr) {
     if (t >= p.num_tiles) return false;
-    const int per = p.hq * p.batch;
+    const int nh = p.pack ? p.hkv : p.hq;
+    const int per = nh * p.batch;
     const int mbi = t / per, rem = t - mbi * per;
     T.mb = p.m_blocks - 1 - mbi;   // longest-first for causal; a fixed order otherwise
-    T.h = rem % p.hq;
-    T.b = rem / p.hq;
+    T.h = rem % nh;
+    T.b = rem / nh;
     T.q_row0 = 0;
     T.k_row0 = 0;
     T.sq = p.seqlen_q;
@@ -118,28 +125,33 @@ __device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
     }
     T.b = lo;
     const int local = t - p.tile_prefix[lo];
-    const int nmb = (p.tile_prefix[lo + 1] - p.tile_prefix[lo]) / p.hq;
-    T.mb = nmb - 1 - local / p.hq;
-    T.h = local % p.hq;
+    const int nh = p.pack ? p.hkv : p.hq;
+    const int nmb = (p.tile_prefix[lo + 1] - p.tile_prefix[lo]) / nh;
+    T.mb = nmb - 1 - local / nh;
+    T.h = local % nh;
     T.q_row0 = p.cu_seqlens_q[lo];
     T.sq = p.cu_seqlens_q[lo + 1] - T.q_row0;
     T.k_row0 = p.cu_seqlens_k[lo];
     T.sk = p.seqused_k ? p.seqused_k[lo] : p.cu_seqlens_k[lo + 1] - T.k_row0;
   }
-  T.g = T.h / p.r;
+  T.g = p.pack ? T.h : T.h / p.r;
+  T.rows = p.pack ? T.sq * p.r : T.sq;
   return true;
 }
 
 __device__ __forceinline__ Range stage_range(const FwdParams& p, const Tile& T, int r0) {
   Range R;
   R.r0 = r0;
-  R.active = r0 < T.sq;
+  R.active = r0 < T.rows;
   R.nlo = R.nhi = 0;
+  const int rr = p.pack ? p.r : 1;
+  R.i0 = r0 / rr;
+  R.i1 = min(r0 + kBM - 1, T.rows - 1) / rr;
   if (!R.active) return R;
-  const int ilast = min(r0 + kBM - 1, T.sq - 1), off = T.sk - T.sq;
+  const int off = T.sk - T.sq;
   int klo = 0, khi = T.sk;
-  if (p.wl >= 0) klo = max(klo, r0 + off - p.wl);
-  if (p.wr >= 0) khi = min(khi, ilast + off + p.wr + 1);
+  if (p.wl >= 0) klo = max(klo, R.i0 + off - p.wl);
+  if (p.wr >= 0) khi = min(khi, R.i1 + off + p.wr + 1);
   if (khi > klo) {
     R.nlo = klo / kBN;
     R.nhi = (khi + kBN - 1) / kBN;
@@ -153,8 +165,8 @@ __device__ __forceinline__ bool part(const Range& R, int n) { return R.nhi > R.n
 // true when some (row, key) of Q tile R x key block n is not visible
 __device__ __forceinline__ bool needs_mask(const FwdParams& p, const Tile& T, const Range& R, int n) {
   const int off = T.sk - T.sq;
-  const bool full = ((n + 1) * kBN <= T.sk) && (p.wr < 0 || (n + 1) * kBN - 1 <= R.r0 + off + p.wr) &&
-                    (p.wl < 0 || n * kBN >= R.r0 + kBM - 1 + off - p.wl);
+  const bool full = ((n + 1) * kBN <= T.sk) && (p.wr < 0 || (n + 1) * kBN - 1 <= R.i0 + off + p.wr) &&
+                    (p.wl < 0 || n * kBN >= R.i1 + off - p.wl);
   return !full;
 }
 
@@ -336,8 +348,13 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             uint8_t* dst = smem + Cfg::OFF_Q + s * Cfg::Q_BYTES;
             mbar_arrive_expect_tx(&B.q_full[s], Cfg::Q_BYTES);
 #pragma unroll
-            for (int c = 0; c < Cfg::KCH; ++c)
-              tma_load_4d(dst + c * kChunkBytes, &mapQ, &B.q_full[s], c * 64, T.q_row0 + R[s].r0, T.h, cb);
+            for (int c = 0; c < Cfg::KCH; ++c) {
+              if (p.pack)   // (d, head in group, query row, KV head, batch): r heads x 128/r rows
+                tma_load_5d(dst + c * kChunkBytes, &mapQ, &B.q_full[s], c * 64, 0, T.q_row0 + R[s].r0 / p.r, T.g,
+                            cb);
+              else
+                tma_load_4d(dst + c * kChunkBytes, &mapQ, &B.q_full[s], c * 64, T.q_row0 + R[s].r0, T.h, cb);
+            }
             ++qc[s];
           }
           for (int n = nhi - 1; ok && n >= nlo; --n) {
@@ -633,12 +650,14 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, tile_of(k), T)) break;
       const Range R = stage_range(p, T, T.mb * Cfg::ROWS_PER_TILE + wg * kBM);
       if (!R.active) continue;
-      const int i = R.r0 + row_local;
-      const bool valid = i < T.sq;
+      const int trow = R.r0 + row_local;                  // tile row
+      const bool valid = trow < T.rows;
+      const int i = p.pack ? trow / p.r : trow;            // query row
+      const int hh = p.pack ? T.g * p.r + trow % p.r : T.h;   // q head
       const int64_t orow = (varlen ? 0 : int64_t(T.b) * p.o_bs) + int64_t(T.q_row0 + i) * p.o_rs +
-                           int64_t(T.h) * p.o_hs;
-      const int64_t lrow = varlen ? int64_t(T.h) * p.total_q + T.q_row0 + i
-                                  : (int64_t(T.b) * p.hq + T.h) * p.seqlen_q + i;
+                           int64_t(hh) * p.o_hs;
+      const int64_t lrow = varlen ? int64_t(hh) * p.total_q + T.q_row0 + i
+                                  : (int64_t(T.b) * p.hq + hh) * p.seqlen_q + i;
       if (!has_work(R)) {
         if (valid) {
           uint4 z = make_uint4(0, 0, 0, 0);
@@ -780,7 +799,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
 }
 
 __global__ void varlen_prepare_kernel(const int* cu_seqlens_q, int batch, int rows_per_tile, int hq,
-                                      int* prefix) {
+                                      int mult, int* prefix) {
   __shared__ int part[1024];
   const int tid = threadIdx.x, nt = blockDim.x;
   const int per = (batch + nt - 1) / nt;
@@ -788,7 +807,7 @@ __global__ void varlen_prepare_kernel(const int* cu_seqlens_q, int batch, int ro
   int sum = 0;
   for (int b = b0; b < b1; ++b) {
     const int sq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
-    sum += ((sq + rows_per_tile - 1) / rows_per_tile) * hq;
+    sum += ((sq * mult + rows_per_tile - 1) / rows_per_tile) * hq;
   }
   part[tid] = sum;
   __syncthreads();
@@ -802,7 +821,7 @@ __global__ void varlen_prepare_kernel(const int* cu_seqlens_q, int batch, int ro
   for (int b = b0; b < b1; ++b) {
     prefix[b] = run;
     const int sq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
-    run += ((sq + rows_per_tile - 1) / rows_per_tile) * hq;
+    run += ((sq * mult + rows_per_tile - 1) / rows_per_tile) * hq;
   }
   if (tid == nt - 1) prefix[batch] = part[tid];
 }
@@ -819,7 +838,8 @@ cudaError_t launch_prefill_t(const FwdParams& p, const CUtensorMap& mq, const CU
   if (p.cu_seqlens_q == nullptr) {
     tiles = p.num_tiles;
   } else {
-    tiles = (long long)p.batch * p.hq * ((p.max_seqlen_q + Cfg::ROWS_PER_TILE - 1) / Cfg::ROWS_PER_TILE);
+    const long long rows = (long long)p.max_seqlen_q * (p.pack ? p.r : 1);
+    tiles = (long long)p.batch * (p.pack ? p.hkv : p.hq) * ((rows + Cfg::ROWS_PER_TILE - 1) / Cfg::ROWS_PER_TILE);
   }
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
   if (grid <= 0) return cudaSuccess;
@@ -852,7 +872,8 @@ cudaError_t launch_prefill(const FwdParams& p, int dk, int dv, const CUtensorMap
 }
 
 cudaError_t launch_varlen_prepare(const FwdParams& p, int rows_per_tile, cudaStream_t stream) {
-  varlen_prepare_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens_q, p.batch, rows_per_tile, p.hq, p.tile_prefix);
+  varlen_prepare_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens_q, p.batch, rows_per_tile, p.pack ? p.hkv : p.hq,
+                                                p.pack ? p.r : 1, p.tile_prefix);
   return cudaGetLastError();
 }
 
