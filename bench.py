@@ -483,7 +483,7 @@ def main():
         torch.cuda.synchronize()
 
     names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode",
-                                                                 "decode_fp8", "decode_paged", "causal_paged")
+                                                                 "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa")
                                                       if n != args.workload])
     results = {}
     clocks = None

@@ -76,7 +76,7 @@ struct PrefillCfg {
 };
 
 // Pack-GQA ("interface.py", pack_gqa; the sm_120 PR page, Pack-GQA: the q heads
-// sharing a KV head fold into the row axis): with p.pack, tile row t of a
+// sharing a KV head fold into the row axis): in the PACK instances tile row t of a
 // sequence is query row t / r of q head g*r + t % r, so one tile reads each
 // K/V block once for r heads. Otherwise tile rows are query rows of head h.
 struct Tile {
@@ -101,11 +101,11 @@ __device__ __forceinline__ int tile_of(int k) {
   return k * g + ((k & 1) ? g - 1 - c : c);
 }
 
-template <int ROWS_PER_TILE>
+template <int ROWS_PER_TILE, bool PACK>
 __device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
   if (p.cu_seqlens_q == nullptr) {
     if (t >= p.num_tiles) return false;
-    const int nh = p.pack ? p.hkv : p.hq;
+    const int nh = PACK ? p.hkv : p.hq;
     const int per = nh * p.batch;
     const int mbi = t / per, rem = t - mbi * per;
     T.mb = p.m_blocks - 1 - mbi;   // longest-first for causal; a fixed order otherwise
@@ -125,7 +125,7 @@ __device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
     }
     T.b = lo;
     const int local = t - p.tile_prefix[lo];
-    const int nh = p.pack ? p.hkv : p.hq;
+    const int nh = PACK ? p.hkv : p.hq;
     const int nmb = (p.tile_prefix[lo + 1] - p.tile_prefix[lo]) / nh;
     T.mb = nmb - 1 - local / nh;
     T.h = local % nh;
@@ -134,24 +134,33 @@ __device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
     T.k_row0 = p.cu_seqlens_k[lo];
     T.sk = p.seqused_k ? p.seqused_k[lo] : p.cu_seqlens_k[lo + 1] - T.k_row0;
   }
-  T.g = p.pack ? T.h : T.h / p.r;
-  T.rows = p.pack ? T.sq * p.r : T.sq;
+  T.g = PACK ? T.h : T.h / p.r;
+  T.rows = PACK ? T.sq * p.r : T.sq;
   return true;
 }
 
+template <bool PACK>
 __device__ __forceinline__ Range stage_range(const FwdParams& p, const Tile& T, int r0) {
   Range R;
   R.r0 = r0;
-  R.active = r0 < T.rows;
   R.nlo = R.nhi = 0;
-  const int rr = p.pack ? p.r : 1;
-  R.i0 = r0 / rr;
-  R.i1 = min(r0 + kBM - 1, T.rows - 1) / rr;
+  int ilast;
+  if constexpr (PACK) {
+    R.active = r0 < T.rows;
+    R.i0 = r0 / p.r;
+    R.i1 = min(r0 + kBM - 1, T.rows - 1) / p.r;
+    ilast = R.i1;
+  } else {
+    R.active = r0 < T.sq;
+    R.i0 = r0;
+    R.i1 = r0 + kBM - 1;
+    ilast = min(r0 + kBM - 1, T.sq - 1);
+  }
   if (!R.active) return R;
   const int off = T.sk - T.sq;
   int klo = 0, khi = T.sk;
   if (p.wl >= 0) klo = max(klo, R.i0 + off - p.wl);
-  if (p.wr >= 0) khi = min(khi, R.i1 + off + p.wr + 1);
+  if (p.wr >= 0) khi = min(khi, ilast + off + p.wr + 1);
   if (khi > klo) {
     R.nlo = klo / kBN;
     R.nhi = (khi + kBN - 1) / kBN;
@@ -250,7 +259,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-template <int DK, int DV, bool TAIL>
+template <int DK, int DV, bool TAIL, bool PACK>
 __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapV, const FwdParams p) {
@@ -327,12 +336,12 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       };
       for (int k = 0; ok; ++k) {
         Tile T;
-        if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, tile_of(k), T)) break;
+        if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK>(p, tile_of(k), T)) break;
         Range R[NQ];
         int nlo = INT32_MAX, nhi = INT32_MIN;
 #pragma unroll
         for (int s = 0; s < NQ; ++s) {
-          R[s] = stage_range(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
+          R[s] = stage_range<PACK>(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
           if (has_work(R[s])) {
             nlo = min(nlo, R[s].nlo);
             nhi = max(nhi, R[s].nhi);
@@ -349,7 +358,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             mbar_arrive_expect_tx(&B.q_full[s], Cfg::Q_BYTES);
 #pragma unroll
             for (int c = 0; c < Cfg::KCH; ++c) {
-              if (p.pack)   // (d, head in group, query row, KV head, batch): r heads x 128/r rows
+              if constexpr (PACK)   // (d, head in group, query row, KV head, batch): r heads x 128/r rows
                 tma_load_5d(dst + c * kChunkBytes, &mapQ, &B.q_full[s], c * 64, 0, T.q_row0 + R[s].r0 / p.r, T.g,
                             cb);
               else
@@ -474,12 +483,12 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       bool ok = true;
       for (int k = 0; ok; ++k) {
         Tile T;
-        if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, tile_of(k), T)) break;
+        if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK>(p, tile_of(k), T)) break;
         Range R[NQ];
         int nlo = INT32_MAX, nhi = INT32_MIN;
 #pragma unroll
         for (int s = 0; s < NQ; ++s) {
-          R[s] = stage_range(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
+          R[s] = stage_range<PACK>(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
           if (has_work(R[s])) {
             nlo = min(nlo, R[s].nlo);
             nhi = max(nhi, R[s].nhi);
@@ -647,13 +656,13 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       Tile T;
-      if (!fetch_tile<Cfg::ROWS_PER_TILE>(p, tile_of(k), T)) break;
-      const Range R = stage_range(p, T, T.mb * Cfg::ROWS_PER_TILE + wg * kBM);
+      if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK>(p, tile_of(k), T)) break;
+      const Range R = stage_range<PACK>(p, T, T.mb * Cfg::ROWS_PER_TILE + wg * kBM);
       if (!R.active) continue;
-      const int trow = R.r0 + row_local;                  // tile row
-      const bool valid = trow < T.rows;
-      const int i = p.pack ? trow / p.r : trow;            // query row
-      const int hh = p.pack ? T.g * p.r + trow % p.r : T.h;   // q head
+      const int trow = R.r0 + row_local;                       // tile row
+      const bool valid = PACK ? trow < T.rows : trow < T.sq;
+      const int i = PACK ? trow / p.r : trow;                  // query row
+      const int hh = PACK ? T.g * p.r + trow % p.r : T.h;      // q head
       const int64_t orow = (varlen ? 0 : int64_t(T.b) * p.o_bs) + int64_t(T.q_row0 + i) * p.o_rs +
                            int64_t(hh) * p.o_hs;
       const int64_t lrow = varlen ? int64_t(hh) * p.total_q + T.q_row0 + i
@@ -830,8 +839,10 @@ template <int DK, int DV>
 cudaError_t launch_prefill_t(const FwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& mv, int num_sms, cudaStream_t stream) {
   using Cfg = PrefillCfg<DK, DV>;
-  // the TAIL instance clears cache rows past seqused_k; the other one has no such work
-  auto kern = p.seqused_k != nullptr ? prefill_kernel<DK, DV, true> : prefill_kernel<DK, DV, false>;
+  // the TAIL instances clear cache rows past seqused_k, the PACK ones fold q
+  // heads into tile rows; the plain instance has neither
+  auto kern = p.seqused_k != nullptr ? (p.pack ? prefill_kernel<DK, DV, true, true> : prefill_kernel<DK, DV, true, false>)
+                                     : (p.pack ? prefill_kernel<DK, DV, false, true> : prefill_kernel<DK, DV, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   long long tiles;

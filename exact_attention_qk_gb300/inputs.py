@@ -29,6 +29,8 @@ passages of the FlashAttention pages):
   decode_paged  the decode shape with the cache split into 128-key pages held
                 in a shuffled page pool, located through a page table
   causal_paged  the causal prefill workload with its K/V cache paged the same way
+  chunk_gqa     chunked prefill: 8 sequences of 128 new rows against 8192 keys,
+                Hq=32 Hkv=4 D=128, causal (the pack-GQA prefill case)
   decode_*_small  the first 16 sequences of a decode workload (profiling cases)
 """
 from __future__ import annotations
@@ -275,6 +277,10 @@ def workload(name: str) -> Workload:
         return fp8_batched("decode_fp8", 5, 64, 1, 16384, 32, 8, 128, "e4m3", seqused_k=decode_seqused())
     if name == "decode_paged":
         return to_paged(workload("decode"), 128)
+    if name == "chunk_gqa":
+        # chunked prefill: 128 new query rows of each of 8 sequences against an
+        # 8192-key cache (bottom-right causal), GQA 32/4
+        return batched("chunk_gqa", 6, 8, 128, 8192, 32, 4, 128, 128, causal=True)
     if name == "causal_paged":
         # the causal prefill workload with its K/V cache in shuffled 128-key pages
         return to_paged(workload("causal"), 128)
@@ -289,5 +295,5 @@ def workload(name: str) -> Workload:
 
 
 WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode", "decode_small",
-             "decode_fp8", "decode_paged", "causal_paged",
+             "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
              "decode_fp8_small", "decode_paged_small")
