@@ -83,17 +83,18 @@ bool make_map(CUtensorMap* m, const void* base, int64_t d, int64_t rows, int64_t
   return r == CUDA_SUCCESS;
 }
 
-// 5-D bf16 map of q for pack-GQA: (d, head within the KV group, row, KV head,
-// batch) with a box of (64, r, 128 / r, 1, 1), so one box is 128 tile rows
-// ordered (query row, head) with the r heads of a row adjacent.
+// 5-D bf16 map of q (or O) for pack-GQA: (d, head within the KV group, row,
+// KV head, batch) with a box of (64, r, box_rows / r, 1, 1), so one box is
+// box_rows tile rows ordered (query row, head) with the r heads of a row adjacent.
 bool make_map_packed_q(CUtensorMap* m, const void* base, int64_t d, int64_t r, int64_t rows, int64_t hkv,
-                       int64_t batch, int64_t row_stride, int64_t head_stride, int64_t batch_stride) {
+                       int64_t batch, int64_t row_stride, int64_t head_stride, int64_t batch_stride,
+                       int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)r, (cuuint64_t)rows, (cuuint64_t)hkv, (cuuint64_t)batch};
   cuuint64_t strides[4] = {(cuuint64_t)(head_stride * 2), (cuuint64_t)(row_stride * 2),
                            (cuuint64_t)(head_stride * r * 2), (cuuint64_t)(batch_stride * 2)};
-  cuuint32_t box[5] = {64, (cuuint32_t)r, (cuuint32_t)(128 / r), 1, 1};
+  cuuint32_t box[5] = {64, (cuuint32_t)r, (cuuint32_t)(box_rows / r), 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult res = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -346,18 +347,27 @@ int run_prefill(const fa_fwd_args* a, const Resolved& r, void* ws, const WsLayou
   const int64_t qrows = r.varlen ? a->total_q : a->seqlen_q;
   const int64_t qb = r.varlen ? 1 : a->batch;
   const int64_t qbs = r.varlen ? a->q_row_stride * (qrows > 0 ? qrows : 1) : a->q_batch_stride;
+  // O has q's layout with head_dim_v; the kernel stores 32-row boxes (one per
+  // softmax warp); packed groups of more than 32 heads are stored row by row
+  CUtensorMap mo;
+  std::memset(&mo, 0, sizeof(mo));
+  const int64_t obs = r.varlen ? a->o_row_stride * (qrows > 0 ? qrows : 1) : a->o_batch_stride;
   if (p.pack) {
     if (!make_map_packed_q(&mq, a->q, a->head_dim_qk, r.r, qrows, a->num_heads_kv, qb, a->q_row_stride,
-                           a->q_head_stride, qbs > 0 ? qbs : 8))
+                           a->q_head_stride, qbs > 0 ? qbs : 8) ||
+        (r.r <= 32 && !make_map_packed_q(&mo, a->out, a->head_dim_v, r.r, qrows, a->num_heads_kv, qb,
+                                         a->o_row_stride, a->o_head_stride, obs > 0 ? obs : 8, 32)))
       return FA_ERR_CUDA;
   } else if (!make_map(&mq, a->q, a->head_dim_qk, qrows, a->num_heads_q, qb, a->q_row_stride, a->q_head_stride,
-                       qbs > 0 ? qbs : 8, 128)) {
+                       qbs > 0 ? qbs : 8, 128) ||
+             !make_map(&mo, a->out, a->head_dim_v, qrows, a->num_heads_q, qb, a->o_row_stride, a->o_head_stride,
+                       obs > 0 ? obs : 8, 32)) {
     return FA_ERR_CUDA;
   }
   if (!kv_maps(a, r, 128, &mk, &mv)) return FA_ERR_CUDA;
   const int sms = device_sms();
   if (sms <= 0) return FA_ERR_CUDA;
-  cudaError_t e = launch_prefill(p, a->head_dim_qk, a->head_dim_v, mq, mk, mv, sms, st);
+  cudaError_t e = launch_prefill(p, a->head_dim_qk, a->head_dim_v, mq, mk, mv, mo, sms, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -46,7 +46,7 @@ struct FwdParams {
 
 // Launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_prefill(const FwdParams& p, int dk, int dv, const CUtensorMap& mq, const CUtensorMap& mk,
-                           const CUtensorMap& mv, int num_sms, cudaStream_t stream);
+                           const CUtensorMap& mv, const CUtensorMap& mo, int num_sms, cudaStream_t stream);
 cudaError_t launch_varlen_prepare(const FwdParams& p, int rows_per_tile, cudaStream_t stream);
 int prefill_rows_per_tile(int dk, int dv);
 bool prefill_supported(int dk, int dv);

@@ -53,7 +53,12 @@ struct PrefillCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KST * K_BYTES;
-  static constexpr int OFF_BAR = OFF_V + VST * V_BYTES;
+  // O staging for coalesced TMA stores: 64 columns x 32 rows per softmax warp
+  // (two-tile kernels with D <= 128, where shared memory has room)
+  static constexpr bool OSTAGE = (NQ == 2) && (DK <= 128);
+  static constexpr int OFF_OST = OFF_V + VST * V_BYTES;
+  static constexpr int OST_BYTES = OSTAGE ? 2 * kChunkBytes : 0;
+  static constexpr int OFF_BAR = OFF_OST + OST_BYTES;
   static constexpr int REL = (KST > VST) ? KST : VST;
   static constexpr int NBAR = 2 * 2 + 2 * KST + 3 * VST + 2 + 2 + 2 + 2 + REL + 1;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
@@ -262,7 +267,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 template <int DK, int DV, bool TAIL, bool PACK>
 __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                   const __grid_constant__ CUtensorMap mapV, const FwdParams p) {
+                   const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
+                   const FwdParams p) {
   using Cfg = PrefillCfg<DK, DV>;
   constexpr int NQ = Cfg::NQ;
   extern __shared__ uint8_t smem_raw[];
@@ -776,26 +782,73 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       tc_fence_after();
       const bool empty_row = !(l > 0.f);
       const float inv_l = empty_row ? 0.f : 1.f / l;
+      // Each warp's 32 rows go out by TMA from its own staging buffer (64
+      // columns at a time, rows 128-byte swizzled so the warp's 16-byte writes
+      // take the minimum four wavefronts); rows past the tensor end are clipped
+      // by the store, and no wait spans more than the warp. Rows of a varlen
+      // tile that would run into the next sequence, and packed groups of more
+      // than 32 heads, are written row by row.
+      const int wrow0 = R.r0 + (warp & 3) * 32;   // first tile row of this warp
+      bool staged = false;
+      if constexpr (Cfg::OSTAGE) staged = (!varlen || wrow0 + 32 <= T.rows) && (!PACK || p.r <= 32);
+      if (staged) {
+        uint8_t* stg = smem + Cfg::OFF_OST + wg * kChunkBytes + (warp & 3) * (kChunkBytes / 4);
+        const int cb = varlen ? 0 : T.b;
 #pragma unroll 1
-      for (int c = 0; c < DV / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(o_addr + c * 32, o);
-        if (valid) {
-          uint32_t w[16];
+        for (int half = 0; half < DV / 64; ++half) {
+          if (lane == 0) bulk_wait_read_all();   // this warp's previous store has read the buffer
+          __syncwarp();
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(out + orow + c * 32);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + half * 64 + c2 * 32, o);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint4 v4 = make_uint4(
+                  pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l),
+                  pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l));
+              const int gi = c2 * 4 + k;
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((gi ^ (lane & 7)) << 4)) = v4;
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (PACK)
+              tma_store_5d(&mapO, stg, half * 64, 0, T.q_row0 + wrow0 / p.r, T.g, cb);
+            else
+              tma_store_4d(&mapO, stg, half * 64, T.q_row0 + wrow0, T.h, cb);
+            bulk_commit_group();
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          if (valid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+            uint4* dst = reinterpret_cast<uint4*>(out + orow + c * 32);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          }
         }
       }
       if (valid && p.lse) p.lse[lrow] = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.o_empty[o_idx]);
+    }
+    // the staging buffers stay in use until every store has completed
+    if constexpr (Cfg::OSTAGE) {
+      if (lane == 0) bulk_wait_all();
     }
   }
 
@@ -837,7 +890,7 @@ __global__ void varlen_prepare_kernel(const int* cu_seqlens_q, int batch, int ro
 
 template <int DK, int DV>
 cudaError_t launch_prefill_t(const FwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                             const CUtensorMap& mv, int num_sms, cudaStream_t stream) {
+                             const CUtensorMap& mv, const CUtensorMap& mo, int num_sms, cudaStream_t stream) {
   using Cfg = PrefillCfg<DK, DV>;
   // the TAIL instances clear cache rows past seqused_k, the PACK ones fold q
   // heads into tile rows; the plain instance has neither
@@ -854,7 +907,7 @@ cudaError_t launch_prefill_t(const FwdParams& p, const CUtensorMap& mq, const CU
   }
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, p);
+  kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mo, p);
   return cudaGetLastError();
 }
 
@@ -874,11 +927,11 @@ int prefill_rows_per_tile(int dk, int dv) {
 }
 
 cudaError_t launch_prefill(const FwdParams& p, int dk, int dv, const CUtensorMap& mq, const CUtensorMap& mk,
-                           const CUtensorMap& mv, int num_sms, cudaStream_t stream) {
-  if (dk == 64 && dv == 64) return launch_prefill_t<64, 64>(p, mq, mk, mv, num_sms, stream);
-  if (dk == 128 && dv == 128) return launch_prefill_t<128, 128>(p, mq, mk, mv, num_sms, stream);
-  if (dk == 192 && dv == 128) return launch_prefill_t<192, 128>(p, mq, mk, mv, num_sms, stream);
-  if (dk == 256 && dv == 256) return launch_prefill_t<256, 256>(p, mq, mk, mv, num_sms, stream);
+                           const CUtensorMap& mv, const CUtensorMap& mo, int num_sms, cudaStream_t stream) {
+  if (dk == 64 && dv == 64) return launch_prefill_t<64, 64>(p, mq, mk, mv, mo, num_sms, stream);
+  if (dk == 128 && dv == 128) return launch_prefill_t<128, 128>(p, mq, mk, mv, mo, num_sms, stream);
+  if (dk == 192 && dv == 128) return launch_prefill_t<192, 128>(p, mq, mk, mv, mo, num_sms, stream);
+  if (dk == 256 && dv == 256) return launch_prefill_t<256, 256>(p, mq, mk, mv, mo, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 
