@@ -64,21 +64,24 @@ int device_sms() {
   return n;
 }
 
-// 4-D map (d, rows, heads, batch-or-page) with a box of (128 bytes of d,
-// box_rows, 1, 1) and 128-byte swizzle: 64 bf16 or 128 one-byte elements per
-// box row. Strides are in elements. Out-of-range coordinates read as zero.
+// 4-D map (d, rows, heads, batch-or-page) with a box of (box_bytes of d,
+// box_rows, 1, 1), swizzled over box_bytes (128: 64 bf16 or 128 one-byte
+// elements per box row; 64: 32 bf16). Strides are in elements. Out-of-range
+// coordinates read as zero (loads) or are not written (stores).
 bool make_map(CUtensorMap* m, const void* base, int64_t d, int64_t rows, int64_t heads, int64_t batch,
-              int64_t row_stride, int64_t head_stride, int64_t batch_stride, int box_rows, int esize = 2) {
+              int64_t row_stride, int64_t head_stride, int64_t batch_stride, int box_rows, int esize = 2,
+              int box_bytes = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
   cuuint64_t strides[3] = {(cuuint64_t)(row_stride * esize), (cuuint64_t)(head_stride * esize),
                            (cuuint64_t)(batch_stride * esize)};
-  cuuint32_t box[4] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t box[4] = {(cuuint32_t)(box_bytes / esize), (cuuint32_t)box_rows, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt = esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUtensorMapSwizzle sw = box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -88,16 +91,17 @@ bool make_map(CUtensorMap* m, const void* base, int64_t d, int64_t rows, int64_t
 // box_rows tile rows ordered (query row, head) with the r heads of a row adjacent.
 bool make_map_packed_q(CUtensorMap* m, const void* base, int64_t d, int64_t r, int64_t rows, int64_t hkv,
                        int64_t batch, int64_t row_stride, int64_t head_stride, int64_t batch_stride,
-                       int box_rows = 128) {
+                       int box_rows = 128, int box_cols = 64) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)r, (cuuint64_t)rows, (cuuint64_t)hkv, (cuuint64_t)batch};
   cuuint64_t strides[4] = {(cuuint64_t)(head_stride * 2), (cuuint64_t)(row_stride * 2),
                            (cuuint64_t)(head_stride * r * 2), (cuuint64_t)(batch_stride * 2)};
-  cuuint32_t box[5] = {64, (cuuint32_t)r, (cuuint32_t)(box_rows / r), 1, 1};
+  cuuint32_t box[5] = {(cuuint32_t)box_cols, (cuuint32_t)r, (cuuint32_t)(box_rows / r), 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult res = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return res == CUDA_SUCCESS;
 }
@@ -347,8 +351,9 @@ int run_prefill(const fa_fwd_args* a, const Resolved& r, void* ws, const WsLayou
   const int64_t qrows = r.varlen ? a->total_q : a->seqlen_q;
   const int64_t qb = r.varlen ? 1 : a->batch;
   const int64_t qbs = r.varlen ? a->q_row_stride * (qrows > 0 ? qrows : 1) : a->q_batch_stride;
-  // O has q's layout with head_dim_v; the kernel stores 32-row boxes (one per
-  // softmax warp); packed groups of more than 32 heads are stored row by row
+  // O has q's layout with head_dim_v; the kernel stores boxes of 32 rows x 32
+  // columns (64-byte swizzle); packed groups of more than 32 heads are stored
+  // row by row
   CUtensorMap mo;
   std::memset(&mo, 0, sizeof(mo));
   const int64_t obs = r.varlen ? a->o_row_stride * (qrows > 0 ? qrows : 1) : a->o_batch_stride;
@@ -356,12 +361,12 @@ int run_prefill(const fa_fwd_args* a, const Resolved& r, void* ws, const WsLayou
     if (!make_map_packed_q(&mq, a->q, a->head_dim_qk, r.r, qrows, a->num_heads_kv, qb, a->q_row_stride,
                            a->q_head_stride, qbs > 0 ? qbs : 8) ||
         (r.r <= 32 && !make_map_packed_q(&mo, a->out, a->head_dim_v, r.r, qrows, a->num_heads_kv, qb,
-                                         a->o_row_stride, a->o_head_stride, obs > 0 ? obs : 8, 32)))
+                                         a->o_row_stride, a->o_head_stride, obs > 0 ? obs : 8, 32, 32)))
       return FA_ERR_CUDA;
   } else if (!make_map(&mq, a->q, a->head_dim_qk, qrows, a->num_heads_q, qb, a->q_row_stride, a->q_head_stride,
                        qbs > 0 ? qbs : 8, 128) ||
              !make_map(&mo, a->out, a->head_dim_v, qrows, a->num_heads_q, qb, a->o_row_stride, a->o_head_stride,
-                       obs > 0 ? obs : 8, 32)) {
+                       obs > 0 ? obs : 8, 32, 2, 64)) {
     return FA_ERR_CUDA;
   }
   if (!kv_maps(a, r, 128, &mk, &mv)) return FA_ERR_CUDA;

@@ -53,8 +53,8 @@ struct PrefillCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KST * K_BYTES;
-  // O staging for coalesced TMA stores: 64 columns x 32 rows per softmax warp
-  // (two-tile kernels with D <= 128, where shared memory has room)
+  // O staging for coalesced TMA stores: two 32-column x 32-row buffers per
+  // softmax warp (two-tile kernels with D <= 128, where shared memory has room)
   static constexpr bool OSTAGE = (NQ == 2) && (DK <= 128);
   static constexpr int OFF_OST = OFF_V + VST * V_BYTES;
   static constexpr int OST_BYTES = OSTAGE ? 2 * kChunkBytes : 0;
@@ -782,12 +782,13 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       tc_fence_after();
       const bool empty_row = !(l > 0.f);
       const float inv_l = empty_row ? 0.f : 1.f / l;
-      // Each warp's 32 rows go out by TMA from its own staging buffer (64
-      // columns at a time, rows 128-byte swizzled so the warp's 16-byte writes
-      // take the minimum four wavefronts); rows past the tensor end are clipped
-      // by the store, and no wait spans more than the warp. Rows of a varlen
-      // tile that would run into the next sequence, and packed groups of more
-      // than 32 heads, are written row by row.
+      // Each warp's 32 rows go out by TMA, 32 columns at a time, through two
+      // 2 KB staging buffers used in turn (rows 64-byte swizzled, so the
+      // warp's 16-byte writes take the minimum four wavefronts): a chunk only
+      // waits for the store two chunks back to have read its buffer. Rows past
+      // the tensor end are clipped by the store, and no wait spans more than
+      // the warp. Rows of a varlen tile that would run into the next sequence,
+      // and packed groups of more than 32 heads, are written row by row.
       const int wrow0 = R.r0 + (warp & 3) * 32;   // first tile row of this warp
       bool staged = false;
       if constexpr (Cfg::OSTAGE) staged = (!varlen || wrow0 + 32 <= T.rows) && (!PACK || p.r <= 32);
@@ -795,31 +796,28 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         uint8_t* stg = smem + Cfg::OFF_OST + wg * kChunkBytes + (warp & 3) * (kChunkBytes / 4);
         const int cb = varlen ? 0 : T.b;
 #pragma unroll 1
-        for (int half = 0; half < DV / 64; ++half) {
-          if (lane == 0) bulk_wait_read_all();   // this warp's previous store has read the buffer
+        for (int c = 0; c < DV / 32; ++c) {
+          uint8_t* buf = stg + (c & 1) * 2048;
+          if (lane == 0) bulk_wait_read_but_one();   // the store two chunks back has read buf
           __syncwarp();
+          uint32_t o[32];
+          tmem_ld32(o_addr + c * 32, o);
 #pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t o[32];
-            tmem_ld32(o_addr + half * 64 + c2 * 32, o);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint4 v4 = make_uint4(
-                  pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l),
-                  pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l));
-              const int gi = c2 * 4 + k;
-              *reinterpret_cast<uint4*>(stg + lane * 128 + ((gi ^ (lane & 7)) << 4)) = v4;
-            }
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v4 = make_uint4(
+                pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l),
+                pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l));
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4)) = v4;
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             if constexpr (PACK)
-              tma_store_5d(&mapO, stg, half * 64, 0, T.q_row0 + wrow0 / p.r, T.g, cb);
+              tma_store_5d(&mapO, buf, c * 32, 0, T.q_row0 + wrow0 / p.r, T.g, cb);
             else
-              tma_store_4d(&mapO, stg, half * 64, T.q_row0 + wrow0, T.h, cb);
+              tma_store_4d(&mapO, buf, c * 32, T.q_row0 + wrow0, T.h, cb);
             bulk_commit_group();
           }
         }
