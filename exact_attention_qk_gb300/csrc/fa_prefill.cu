@@ -690,29 +690,35 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         if (slot) ++sw1; else ++sw0;
         tc_fence_after();
         uint32_t r[128];
-        tmem_ld128(tmem + lane_off + slot * 128, r);
         float* s = reinterpret_cast<float*>(r);
-        if (needs_mask(p, T, R, n)) {
+        float bmax;
+        if (needs_mask(p, T, R, n)) {   // (warp-uniform)
+          tmem_ld128(tmem + lane_off + slot * 128, r);
           const int jb = n * kBN;
           const int c_lo = (p.wl >= 0) ? i + off - p.wl - jb : INT32_MIN / 2;
           int c_hi = T.sk - 1 - jb;
           if (p.wr >= 0) c_hi = min(c_hi, i + off + p.wr - jb);
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < c_lo || c > c_hi) ? -INFINITY : s[c];
+          // row max: eight independent chains of 3-input max
+          float mx[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mx[j] = s[j];
+#pragma unroll
+          for (int c = 8; c + 16 <= 128; c += 16) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mx[j] = fmax3(mx[j], s[c + j], s[c + 8 + j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], s[120 + j]);
+          bmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+                 p.scale_log2;
+        } else {
+          // every column is visible: the load returns the row max with the row
+          float hw;
+          tmem_ld128_max(tmem + lane_off + slot * 128, r, hw);
+          bmax = hw * p.scale_log2;
         }
-        // row max: eight independent chains of 3-input max
-        float mx[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mx[j] = s[j];
-#pragma unroll
-        for (int c = 8; c + 16 <= 128; c += 16) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) mx[j] = fmax3(mx[j], s[c + j], s[c + 8 + j]);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], s[120 + j]);
-        const float bmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
-                           p.scale_log2;
         const float m_new = fmaxf(m, bmax);
         // The previous P.V of this O (if any in this tile) has a phase on o_bar
         // that is consumed exactly once: before O is rescaled, or else just

@@ -273,6 +273,31 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "memory");
 }
 
+#define FA_F8(i) "=f"(f[i + 0]), "=f"(f[i + 1]), "=f"(f[i + 2]), "=f"(f[i + 3]), \
+                 "=f"(f[i + 4]), "=f"(f[i + 5]), "=f"(f[i + 6]), "=f"(f[i + 7])
+
+// 32x32b.x128 load that also returns the maximum of the thread's 128 loaded
+// values (its row), computed by the load itself (tcgen05.ld.red, sm_103a);
+// -inf is an ordinary value and NaN is ignored, as in max.f32. Wait fused.
+__device__ __forceinline__ void tmem_ld128_max(uint32_t taddr, uint32_t (&r)[128], float& mx) {
+  float(&f)[128] = reinterpret_cast<float(&)[128]>(r);
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x128.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,"
+      "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+      "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, %128, [%129];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FA_F8(0), FA_F8(8), FA_F8(16), FA_F8(24), FA_F8(32), FA_F8(40), FA_F8(48), FA_F8(56),
+        FA_F8(64), FA_F8(72), FA_F8(80), FA_F8(88), FA_F8(96), FA_F8(104), FA_F8(112), FA_F8(120), "=f"(mx)
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
