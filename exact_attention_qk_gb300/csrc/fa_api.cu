@@ -325,7 +325,8 @@ int run_decode(const fa_fwd_args* a, const Resolved& r, int ns, float* opart, fl
   p.lse_partial = lpart;
   if (!p.status) return FA_ERR_CUDA;
   CUtensorMap mk, mv;
-  if (!kv_maps(a, r, 64, &mk, &mv)) return FA_ERR_CUDA;
+  // decode tiles: 64 keys of bf16, 128 keys of one-byte elements
+  if (!kv_maps(a, r, fp8_kv(a) ? 128 : 64, &mk, &mv)) return FA_ERR_CUDA;
   cudaError_t e = launch_decode(p, a->head_dim_qk, a->head_dim_v, mk, mv, st);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }

@@ -40,8 +40,6 @@ namespace {
 
 constexpr int kDecWarps = 4;            // compute warps
 constexpr int kDecThreads = (kDecWarps + 1) * 32;
-constexpr int kTileKeys = 64;
-constexpr int kBoxBytes = kTileKeys * 128;   // one 128-byte x 64-key box
 constexpr int kRows = 8;                     // packed query rows per CTA (the MMAs' N)
 
 // Widen four fp8 codes (one 32-bit word, lowest byte first) to fp32 pairs.
@@ -63,16 +61,20 @@ __device__ __forceinline__ void fp8x4_to_f32(uint32_t w, float2& lo, float2& hi)
 
 template <int DK, int DV, int KVT>
 struct DecodeCfg {
+  // keys per tile: 64 with bf16 elements; 128 with one-byte elements, so a
+  // tile moves the same bytes and each warp takes two 16-key groups
+  static constexpr int TK = KVT ? 128 : 64;
+  static constexpr int G = TK / 64;               // 16-key groups per warp and tile
+  static constexpr int BOX = TK * 128;            // one 128-byte x TK-key box
   static constexpr int ES = KVT ? 1 : 2;          // bytes per K/V element
   static constexpr int KCH = DK * ES / 128;       // 128-byte boxes per K row
   static constexpr int VCH = DV * ES / 128;
-  static constexpr int STAGE_BYTES = (KCH + VCH) * kBoxBytes;
-  // Two bf16 stages keep a D<=192 CTA near 70 KB of shared memory, so three
-  // CTAs share an SM; fp8 tiles are half the bytes: four stages keep the same
-  // bytes in flight in the same space.
-  static constexpr int NSTAGE = KVT ? 4 : 2;
+  static constexpr int STAGE_BYTES = (KCH + VCH) * BOX;
+  // Two stages keep a D<=192 CTA near 70 KB of shared memory, so three CTAs
+  // share an SM.
+  static constexpr int NSTAGE = 2;
   static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
-  static constexpr int P_BYTES = kDecWarps * kRows * 16 * 2;          // per warp: P[row][16 keys], 16-bit
+  static constexpr int P_BYTES = kDecWarps * kRows * 16 * G * 2;      // per warp: P[row][16 G keys], 16-bit
   static constexpr int MROW = DV + 4;                                 // merge row: O, m, l, pad
   static constexpr int MERGE_BYTES = kDecWarps * kRows * MROW * 4;
   static constexpr int OFF_P = RING_BYTES;
@@ -216,8 +218,9 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
     return;
   }
 
-  const int key_base = (klo / kTileKeys) * kTileKeys;
-  const int ntiles = (khi - key_base + kTileKeys - 1) / kTileKeys;
+  constexpr int TK = C::TK;
+  const int key_base = (klo / TK) * TK;
+  const int ntiles = (khi - key_base + TK - 1) / TK;
 
   if (tid == 0) {
     for (int s = 0; s < C::NSTAGE; ++s) {
@@ -239,11 +242,14 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
       const int kb = varlen ? 0 : b;
       constexpr int INNER = 128 / C::ES;   // elements per box row
       const bool paged = p.page_table != nullptr;
-      const int rpl = paged ? min(kTileKeys, p.page_size) : kTileKeys;   // rows per load
+      // rows per load: a piece inside one page, the same rule as the host's map
+      // (the whole tile, else 64 rows, else one page)
+      const int ps = p.page_size;
+      const int rpl = !paged ? TK : (ps % TK == 0 ? TK : (ps % 64 == 0 ? 64 : ps));
       int t = 0;
       for (; t < ntiles; ++t) {
         const int st = t % C::NSTAGE;
-        const int key = key_base + t * kTileKeys;
+        const int key = key_base + t * TK;
         if (!paged) {
           if (t >= C::NSTAGE && !mbar_wait(&empty[st], ((t / C::NSTAGE) - 1) & 1, guard)) break;
           uint8_t* dst = smem + st * C::STAGE_BYTES;
@@ -251,10 +257,10 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
           const int row = k_row0 + key;
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(dst + c * kBoxBytes, &mapK, &full[st], c * INNER, row, g, kb);
+            tma_load_4d(dst + c * C::BOX, &mapK, &full[st], c * INNER, row, g, kb);
 #pragma unroll
           for (int c = 0; c < C::VCH; ++c)
-            tma_load_4d(dst + (C::KCH + c) * kBoxBytes, &mapV, &full[st], c * INNER, row, g, kb);
+            tma_load_4d(dst + (C::KCH + c) * C::BOX, &mapV, &full[st], c * INNER, row, g, kb);
         } else {
           // the page of the tile's first key, read before the slot wait so
           // that its latency overlaps it (pages of 64+ keys: one per tile)
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
           if (t >= C::NSTAGE && !mbar_wait(&empty[st], ((t / C::NSTAGE) - 1) & 1, guard)) break;
           uint8_t* dst = smem + st * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
-          for (int sub = 0; sub < kTileKeys; sub += rpl) {
+          for (int sub = 0; sub < TK; sub += rpl) {
             const int kk = key + sub;
             const int pi = kk / p.page_size;
             const int page =
@@ -271,10 +277,10 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
             const int r = kk - pi * p.page_size;
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-              tma_load_4d(dst + c * kBoxBytes + sub * 128, &mapK, &full[st], c * INNER, r, g, page);
+              tma_load_4d(dst + c * C::BOX + sub * 128, &mapK, &full[st], c * INNER, r, g, page);
 #pragma unroll
             for (int c = 0; c < C::VCH; ++c)
-              tma_load_4d(dst + (C::KCH + c) * kBoxBytes + sub * 128, &mapV, &full[st], c * INNER, r, g, page);
+              tma_load_4d(dst + (C::KCH + c) * C::BOX + sub * 128, &mapV, &full[st], c * INNER, r, g, page);
           }
         }
       }
@@ -355,9 +361,10 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
   float o[MT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  uint16_t* pw = p_s + warp * (NR * 16);          // this warp's P[row][16 keys]
+  constexpr int G = C::G;
+  constexpr int WK = 16 * G;                      // keys per warp and tile
+  uint16_t* pw = p_s + warp * (NR * WK);          // this warp's P[row][WK keys]
   const int key_end = min(sk, s_hi);              // keys at or past this are never used
-  const int ka = warp * 16 + g8, kb = ka + 8;     // this thread's two S keys (tile rows)
 
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
@@ -367,57 +374,82 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
       break;
     }
     const uint8_t* stage = smem + st * C::STAGE_BYTES;
-    const int tkey0 = key_base + t * kTileKeys;
+    const int tkey0 = key_base + t * TK;
 
-    // ---- S^T = K q^T over this warp's 16 keys ----
-    float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S^T = K q^T over this warp's WK keys, in 16-key groups ----
+    float sv[G][4];
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      if constexpr (KVT == 0) {
-        // dims 16kk + 4t4 .. +3: 8 bytes in box kk/4, granule 2(kk%4) + t4/2
-        const int gran = 2 * (kk & 3) + (t4 >> 1), byt = 8 * (t4 & 1);
-        const uint8_t* kbox = stage + (kk >> 2) * kBoxBytes;
-        const uint2 x = *reinterpret_cast<const uint2*>(kbox + ka * 128 + ((gran ^ (ka & 7)) << 4) + byt);
-        const uint2 y = *reinterpret_cast<const uint2*>(kbox + kb * 128 + ((gran ^ (kb & 7)) << 4) + byt);
-        mma_16816_bf16(sacc, x.x, y.x, x.y, y.y, qf[kk][0], qf[kk][1]);
-      } else {
-        // dims 16kk + 4t4 .. +3: 4 bytes in box kk/8, granule kk%8
-        const uint8_t* kbox = stage + (kk >> 3) * kBoxBytes;
-        const uint32_t x = *reinterpret_cast<const uint32_t*>(kbox + ka * 128 + (((kk & 7) ^ (ka & 7)) << 4) + 4 * t4);
-        const uint32_t y = *reinterpret_cast<const uint32_t*>(kbox + kb * 128 + (((kk & 7) ^ (kb & 7)) << 4) + 4 * t4);
-        mma_16816_f16(sacc, fp8x2_to_f16x2<KVT>(x), fp8x2_to_f16x2<KVT>(y), fp8x2_to_f16x2<KVT>(x >> 16),
-                      fp8x2_to_f16x2<KVT>(y >> 16), qf[kk][0], qf[kk][1]);
+    for (int grp = 0; grp < G; ++grp) {
+      const int ka = warp * WK + grp * 16 + g8, kb = ka + 8;   // this thread's two keys (tile rows)
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        if constexpr (KVT == 0) {
+          // dims 16kk + 4t4 .. +3: 8 bytes in box kk/4, granule 2(kk%4) + t4/2
+          const int gran = 2 * (kk & 3) + (t4 >> 1), byt = 8 * (t4 & 1);
+          const uint8_t* kbox = stage + (kk >> 2) * C::BOX;
+          const uint2 x = *reinterpret_cast<const uint2*>(kbox + ka * 128 + ((gran ^ (ka & 7)) << 4) + byt);
+          const uint2 y = *reinterpret_cast<const uint2*>(kbox + kb * 128 + ((gran ^ (kb & 7)) << 4) + byt);
+          mma_16816_bf16(sacc, x.x, y.x, x.y, y.y, qf[kk][0], qf[kk][1]);
+        } else {
+          // dims 16kk + 4t4 .. +3: 4 bytes in box kk/8, granule kk%8
+          const uint8_t* kbox = stage + (kk >> 3) * C::BOX;
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(kbox + ka * 128 + (((kk & 7) ^ (ka & 7)) << 4) + 4 * t4);
+          const uint32_t y = *reinterpret_cast<const uint32_t*>(kbox + kb * 128 + (((kk & 7) ^ (kb & 7)) << 4) + 4 * t4);
+          mma_16816_f16(sacc, fp8x2_to_f16x2<KVT>(x), fp8x2_to_f16x2<KVT>(y), fp8x2_to_f16x2<KVT>(x >> 16),
+                        fp8x2_to_f16x2<KVT>(y >> 16), qf[kk][0], qf[kk][1]);
+        }
       }
+      // sacc: (key ka, row 2t4), (ka, 2t4+1), (kb, 2t4), (kb, 2t4+1); base-2 scores
+      const int ja = tkey0 + ka, jb = tkey0 + kb;
+      sv[grp][0] = (ja >= lo0 && ja <= hi0) ? sacc[0] * sscale : -INFINITY;
+      sv[grp][1] = (ja >= lo1 && ja <= hi1) ? sacc[1] * sscale : -INFINITY;
+      sv[grp][2] = (jb >= lo0 && jb <= hi0) ? sacc[2] * sscale : -INFINITY;
+      sv[grp][3] = (jb >= lo1 && jb <= hi1) ? sacc[3] * sscale : -INFINITY;
     }
-    // sacc: (key ka, row 2t4), (ka, 2t4+1), (kb, 2t4), (kb, 2t4+1); base-2 scores
-    const int ja = tkey0 + ka, jb = tkey0 + kb;
-    const float sa0 = (ja >= lo0 && ja <= hi0) ? sacc[0] * sscale : -INFINITY;
-    const float sa1 = (ja >= lo1 && ja <= hi1) ? sacc[1] * sscale : -INFINITY;
-    const float sb0 = (jb >= lo0 && jb <= hi0) ? sacc[2] * sscale : -INFINITY;
-    const float sb1 = (jb >= lo1 && jb <= hi1) ? sacc[3] * sscale : -INFINITY;
-    // ---- online softmax over the warp's 16 keys (rows 2t4 and 2t4+1) ----
-    float bm0 = fmaxf(sa0, sb0), bm1 = fmaxf(sa1, sb1);
+    // ---- online softmax over the warp's keys (rows 2t4 and 2t4+1) ----
+    float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+    for (int grp = 0; grp < G; ++grp) {
+      bm0 = fmax3(bm0, sv[grp][0], sv[grp][2]);
+      bm1 = fmax3(bm1, sv[grp][1], sv[grp][3]);
+    }
 #pragma unroll
     for (int x = 4; x < 32; x <<= 1) {
       bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, x));
       bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, x));
     }
     const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-    float f0 = 1.f, f1 = 1.f, pa0 = 0.f, pb0 = 0.f, pa1 = 0.f, pb1 = 0.f;
+    float f0 = 1.f, f1 = 1.f;
+    float pv[G][4];
+#pragma unroll
+    for (int grp = 0; grp < G; ++grp) pv[grp][0] = pv[grp][1] = pv[grp][2] = pv[grp][3] = 0.f;
     if (mn0 != -INFINITY) {
       f0 = ex2_approx(m0 - mn0);
-      pa0 = ex2_approx(sa0 - mn0);
-      pb0 = ex2_approx(sb0 - mn0);
+#pragma unroll
+      for (int grp = 0; grp < G; ++grp) {
+        pv[grp][0] = ex2_approx(sv[grp][0] - mn0);
+        pv[grp][2] = ex2_approx(sv[grp][2] - mn0);
+      }
     }
     if (mn1 != -INFINITY) {
       f1 = ex2_approx(m1 - mn1);
-      pa1 = ex2_approx(sa1 - mn1);
-      pb1 = ex2_approx(sb1 - mn1);
+#pragma unroll
+      for (int grp = 0; grp < G; ++grp) {
+        pv[grp][1] = ex2_approx(sv[grp][1] - mn1);
+        pv[grp][3] = ex2_approx(sv[grp][3] - mn1);
+      }
     }
     m0 = mn0;
     m1 = mn1;
-    l0 = l0 * f0 + (pa0 + pb0);
-    l1 = l1 * f1 + (pa1 + pb1);
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int grp = 0; grp < G; ++grp) {
+      ps0 += pv[grp][0] + pv[grp][2];
+      ps1 += pv[grp][1] + pv[grp][3];
+    }
+    l0 = l0 * f0 + ps0;
+    l1 = l1 * f1 + ps1;
     if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
@@ -435,51 +467,57 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
         return __half_as_ushort(__float2half_rn(v));
       }
     };
-    pw[(2 * t4) * 16 + g8] = p16(pa0);
-    pw[(2 * t4 + 1) * 16 + g8] = p16(pa1);
-    pw[(2 * t4) * 16 + g8 + 8] = p16(pb0);
-    pw[(2 * t4 + 1) * 16 + g8 + 8] = p16(pb1);
+#pragma unroll
+    for (int grp = 0; grp < G; ++grp) {
+      pw[(2 * t4) * WK + grp * 16 + g8] = p16(pv[grp][0]);
+      pw[(2 * t4 + 1) * WK + grp * 16 + g8] = p16(pv[grp][1]);
+      pw[(2 * t4) * WK + grp * 16 + g8 + 8] = p16(pv[grp][2]);
+      pw[(2 * t4 + 1) * WK + grp * 16 + g8 + 8] = p16(pv[grp][3]);
+    }
     __syncwarp();
-    // P^T as the B operand of O^T += V^T P^T: row g8, keys 4t4 .. +3
-    const uint2 pf = *reinterpret_cast<const uint2*>(pw + g8 * 16 + 4 * t4);
-    // ---- O^T += V^T P^T: this thread's V rows are keys 4t4 .. +3 of the warp ----
-    const int kv0 = warp * 16 + 4 * t4;
-    // keys at or past key_end may hold anything (NaN included): zero them
-    const bool vtail = tkey0 + warp * 16 + 16 > key_end;
+    // ---- O^T += V^T P^T, one 16-key group at a time ----
 #pragma unroll
-    for (int j = 0; j < DV / 32; ++j) {
-      // columns 32j + 4g8 .. +3: m tile 2j holds (4g8, 4g8+1), m tile 2j+1 (4g8+2, 4g8+3)
-      if constexpr (KVT == 0) {
-        const int gran = 4 * (j & 1) + (g8 >> 1), byt = 8 * (g8 & 1);
-        const uint8_t* vbox = stage + (C::KCH + (j >> 1)) * kBoxBytes;
-        uint2 r[4];
+    for (int grp = 0; grp < G; ++grp) {
+      // P^T as the B operand: row g8, keys 16 grp + 4t4 .. +3
+      const uint2 pf = *reinterpret_cast<const uint2*>(pw + g8 * WK + grp * 16 + 4 * t4);
+      const int kv0 = warp * WK + grp * 16 + 4 * t4;   // this thread's V rows (tile keys)
+      // keys at or past key_end may hold anything (NaN included): zero them
+      const bool vtail = tkey0 + warp * WK + grp * 16 + 16 > key_end;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int kr = kv0 + i;
-          r[i] = *reinterpret_cast<const uint2*>(vbox + kr * 128 + ((gran ^ (kr & 7)) << 4) + byt);
-          if (vtail && tkey0 + kr >= key_end) r[i] = make_uint2(0u, 0u);
+      for (int j = 0; j < DV / 32; ++j) {
+        // columns 32j + 4g8 .. +3: m tile 2j holds (4g8, 4g8+1), m tile 2j+1 (4g8+2, 4g8+3)
+        if constexpr (KVT == 0) {
+          const int gran = 4 * (j & 1) + (g8 >> 1), byt = 8 * (g8 & 1);
+          const uint8_t* vbox = stage + (C::KCH + (j >> 1)) * C::BOX;
+          uint2 r[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kr = kv0 + i;
+            r[i] = *reinterpret_cast<const uint2*>(vbox + kr * 128 + ((gran ^ (kr & 7)) << 4) + byt);
+            if (vtail && tkey0 + kr >= key_end) r[i] = make_uint2(0u, 0u);
+          }
+          mma_16816_bf16(o[2 * j], __byte_perm(r[0].x, r[1].x, 0x5410), __byte_perm(r[0].x, r[1].x, 0x7632),
+                         __byte_perm(r[2].x, r[3].x, 0x5410), __byte_perm(r[2].x, r[3].x, 0x7632), pf.x, pf.y);
+          mma_16816_bf16(o[2 * j + 1], __byte_perm(r[0].y, r[1].y, 0x5410), __byte_perm(r[0].y, r[1].y, 0x7632),
+                         __byte_perm(r[2].y, r[3].y, 0x5410), __byte_perm(r[2].y, r[3].y, 0x7632), pf.x, pf.y);
+        } else {
+          const int gran = 2 * (j & 3) + (g8 >> 2), byt = 4 * (g8 & 3);
+          const uint8_t* vbox = stage + (C::KCH + (j >> 2)) * C::BOX;
+          uint32_t r[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kr = kv0 + i;
+            r[i] = *reinterpret_cast<const uint32_t*>(vbox + kr * 128 + ((gran ^ (kr & 7)) << 4) + byt);
+            if (vtail && tkey0 + kr >= key_end) r[i] = 0u;
+          }
+          // byte pairs (key 4t4 + 2c, key 4t4 + 2c + 1) of one column
+          const uint32_t c01a = __byte_perm(r[0], r[1], 0x5140), c23a = __byte_perm(r[0], r[1], 0x7362);
+          const uint32_t c01b = __byte_perm(r[2], r[3], 0x5140), c23b = __byte_perm(r[2], r[3], 0x7362);
+          mma_16816_f16(o[2 * j], fp8x2_to_f16x2<KVT>(c01a), fp8x2_to_f16x2<KVT>(c01a >> 16),
+                        fp8x2_to_f16x2<KVT>(c01b), fp8x2_to_f16x2<KVT>(c01b >> 16), pf.x, pf.y);
+          mma_16816_f16(o[2 * j + 1], fp8x2_to_f16x2<KVT>(c23a), fp8x2_to_f16x2<KVT>(c23a >> 16),
+                        fp8x2_to_f16x2<KVT>(c23b), fp8x2_to_f16x2<KVT>(c23b >> 16), pf.x, pf.y);
         }
-        mma_16816_bf16(o[2 * j], __byte_perm(r[0].x, r[1].x, 0x5410), __byte_perm(r[0].x, r[1].x, 0x7632),
-                       __byte_perm(r[2].x, r[3].x, 0x5410), __byte_perm(r[2].x, r[3].x, 0x7632), pf.x, pf.y);
-        mma_16816_bf16(o[2 * j + 1], __byte_perm(r[0].y, r[1].y, 0x5410), __byte_perm(r[0].y, r[1].y, 0x7632),
-                       __byte_perm(r[2].y, r[3].y, 0x5410), __byte_perm(r[2].y, r[3].y, 0x7632), pf.x, pf.y);
-      } else {
-        const int gran = 2 * (j & 3) + (g8 >> 2), byt = 4 * (g8 & 3);
-        const uint8_t* vbox = stage + (C::KCH + (j >> 2)) * kBoxBytes;
-        uint32_t r[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int kr = kv0 + i;
-          r[i] = *reinterpret_cast<const uint32_t*>(vbox + kr * 128 + ((gran ^ (kr & 7)) << 4) + byt);
-          if (vtail && tkey0 + kr >= key_end) r[i] = 0u;
-        }
-        // byte pairs (key 4t4 + 2c, key 4t4 + 2c + 1) of one column
-        const uint32_t c01a = __byte_perm(r[0], r[1], 0x5140), c23a = __byte_perm(r[0], r[1], 0x7362);
-        const uint32_t c01b = __byte_perm(r[2], r[3], 0x5140), c23b = __byte_perm(r[2], r[3], 0x7362);
-        mma_16816_f16(o[2 * j], fp8x2_to_f16x2<KVT>(c01a), fp8x2_to_f16x2<KVT>(c01a >> 16),
-                      fp8x2_to_f16x2<KVT>(c01b), fp8x2_to_f16x2<KVT>(c01b >> 16), pf.x, pf.y);
-        mma_16816_f16(o[2 * j + 1], fp8x2_to_f16x2<KVT>(c23a), fp8x2_to_f16x2<KVT>(c23a >> 16),
-                      fp8x2_to_f16x2<KVT>(c23b), fp8x2_to_f16x2<KVT>(c23b >> 16), pf.x, pf.y);
       }
     }
     __syncwarp();

@@ -144,3 +144,11 @@ def test_full_size_kvcache_decode_sampled_sequences(name):
         k, v = gu.oracle_kv(s)
         ro, rl = oracle.attention_forward(s.q, k, v, **gu.oracle_kw(s))
         print(gu.compare(o[b:b + 1], l[b:b + 1], ro, rl, f"{name} sequence {b}"))
+
+
+@pytest.mark.parametrize("page_size", [32, 64, 192, 256])
+def test_paged_fp8_page_sizes(page_size):
+    # fp8 tiles are 128 keys: pages of 64 or 192 keys are moved in 64-row pieces
+    w = inputs.fp8_batched("pgfp8ps", 250 + page_size, 2, 1, 768, 8, 2, 128, "e5m2",
+                           seqused_k=np.array([768, 333], np.int32))
+    print(gu.check_workload(inputs.to_paged(w, page_size)))
