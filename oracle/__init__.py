@@ -16,3 +16,4 @@ from .attention import (  # noqa: F401
     widen,
 )
 from .kvcache import dequant_kv, fp8_to_float, gather_pages, plain_kv  # noqa: F401,E402
+from .backward import attention_backward  # noqa: F401,E402
