@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 
-LIB_SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_decode.cu"]
+LIB_SOURCES = ["fa_api.cu", "fa_prefill.cu", "fa_decode.cu", "fa_backward.cu"]
 SELFTEST_SOURCES = ["fa_selftest.cu"]
 LIB_NAME = "libfa.so"
 SELFTEST_NAME = "libfa_selftest.so"

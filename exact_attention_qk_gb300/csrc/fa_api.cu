@@ -403,6 +403,30 @@ bool no_work(const fa_fwd_args* a, const Resolved& r) {
   return a->seqlen_q == 0;
 }
 
+struct BwdWs {
+  int sq_pad;
+  size_t lse2_off, dsum_off, total;
+};
+
+BwdWs bwd_ws(const fa_fwd_args* a) {
+  BwdWs w{};
+  w.sq_pad = ((a->seqlen_q + 127) / 128) * 128;
+  const size_t n = static_cast<size_t>(a->batch) * a->num_heads_q * w.sq_pad;
+  w.lse2_off = 0;
+  w.dsum_off = align256(n * sizeof(float));
+  w.total = w.dsum_off + align256(n * sizeof(float));
+  return w;
+}
+
+int check_bwd_args(const fa_fwd_args* a, Resolved* r) {
+  const int rc = check_args(a, r);
+  if (rc != FA_OK) return rc;
+  if (r->varlen || a->seqused_k != nullptr || a->page_table != nullptr || a->kv_format != FA_KV_BF16)
+    return FA_ERR_UNSUPPORTED;
+  if (!bwd_supported(a->head_dim_qk, a->head_dim_v)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -410,7 +434,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_abi_version(void) { return 200; }
+int fa_abi_version(void) { return 201; }
 
 const char* fa_status_string(int s) {
   switch (s) {
@@ -550,6 +574,93 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* a, void* stream) {
   return fa_combine(opart, lpart, ns, a->batch, r.varlen ? 0 : a->seqlen_q, a->num_heads_q, a->head_dim_v,
                     a->cu_seqlens_q, r.varlen ? a->total_q : 0, a->out, a->o_batch_stride, a->o_row_stride,
                     a->o_head_stride, a->lse, stream);
+}
+
+size_t fa_bwd_workspace_size(const fa_fwd_args* a) {
+  Resolved r;
+  if (check_bwd_args(a, &r) != FA_OK) return 0;
+  return bwd_ws(a).total;
+}
+
+int fa_bwd(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+           size_t workspace_bytes, void* stream) {
+  Resolved r;
+  int rc = check_bwd_args(a, &r);
+  if (rc != FA_OK) return rc;
+  if (a->batch == 0 || (a->seqlen_q == 0 && a->seqlen_k == 0)) return FA_OK;
+  // With no query rows only dK = dV = 0 is written, and with no keys only
+  // dQ = 0: the tensors of the empty side are never touched and may be NULL
+  // (as an empty tensor's storage is).
+  const bool has_q = a->seqlen_q > 0, has_k = a->seqlen_k > 0;
+  fa_fwd_args c = *a;
+  if (!has_q) {
+    c.q = c.k;
+    c.out = const_cast<void*>(c.k);
+  }
+  if (!has_k) c.k = c.v = c.q;
+  rc = check_tensors(&c, true);
+  if (rc != FA_OK) return rc;
+  if ((has_q && (!a->lse || !dout || !dq)) || (has_k && (!dk || !dv))) return FA_ERR_INVALID_ARG;
+  if ((has_q && (!aligned16(dout) || !aligned16(dq) || (reinterpret_cast<uintptr_t>(a->lse) & 3u))) ||
+      (has_k && (!aligned16(dk) || !aligned16(dv))))
+    return FA_ERR_ALIGNMENT;
+  const BwdWs w = bwd_ws(a);
+  if (w.total > 0 && (workspace == nullptr || workspace_bytes < w.total)) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_ALIGNMENT;
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.out = a->out;
+  p.dout = dout;
+  p.lse = a->lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lse2_off);
+  p.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dsum_off);
+  p.q_bs = a->q_batch_stride;
+  p.q_rs = a->q_row_stride;
+  p.q_hs = a->q_head_stride;
+  p.k_bs = a->k_batch_stride;
+  p.k_rs = a->k_row_stride;
+  p.k_hs = a->k_head_stride;
+  p.v_bs = a->v_batch_stride;
+  p.v_rs = a->v_row_stride;
+  p.v_hs = a->v_head_stride;
+  p.o_bs = a->o_batch_stride;
+  p.o_rs = a->o_row_stride;
+  p.o_hs = a->o_head_stride;
+  p.batch = a->batch;
+  p.seqlen_q = a->seqlen_q;
+  p.seqlen_k = a->seqlen_k;
+  p.sq_pad = w.sq_pad;
+  p.hq = a->num_heads_q;
+  p.hkv = a->num_heads_kv;
+  p.r = r.r;
+  p.scale = r.scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(r.scale) * 1.4426950408889634);
+  p.wl = r.wl;
+  p.wr = r.wr;
+  p.status = status_ptr();
+  p.timeout_ns = g_timeout_ns.load();
+  if (!p.status) return FA_ERR_CUDA;
+  const int64_t sq = a->seqlen_q, sk = a->seqlen_k;
+  const int d = a->head_dim_qk;
+  // the maps of an empty side are stand-ins (copies of the other side's), never read
+  CUtensorMap mq, mk, mv, mdo;
+  if (has_q && (!make_map(&mq, a->q, d, sq, a->num_heads_q, a->batch, a->q_row_stride, a->q_head_stride,
+                          a->q_batch_stride, 128) ||
+                !make_map(&mdo, dout, d, sq, a->num_heads_q, a->batch, a->o_row_stride, a->o_head_stride,
+                          a->o_batch_stride, 128)))
+    return FA_ERR_CUDA;
+  if (has_k && (!make_map(&mk, a->k, d, sk, a->num_heads_kv, a->batch, a->k_row_stride, a->k_head_stride,
+                          a->k_batch_stride, 128) ||
+                !make_map(&mv, a->v, d, sk, a->num_heads_kv, a->batch, a->v_row_stride, a->v_head_stride,
+                          a->v_batch_stride, 128)))
+    return FA_ERR_CUDA;
+  if (!has_q) mq = mdo = mk;
+  if (!has_k) mk = mv = mq;
+  cudaError_t e = launch_bwd(p, d, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_get_status(void* stream) {

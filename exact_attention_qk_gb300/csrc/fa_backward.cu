@@ -1,0 +1,593 @@
+// fa_backward.cu - attention backward (dQ, dK, dV) on tcgen05.
+//
+// The backward of "mslk/attention/flash_attn/flash_bwd_sm100.py": a
+// preprocess pass forms D = rowsum(dO * O) from the forward's output; the main
+// loop recomputes P = exp(scale * Q K^T - LSE) from the stored LSE, then
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+// The page's kernel accumulates dQ of every key block through global fp32
+// atomics; here dQ has a kernel of its own instead, which recomputes S and dP
+// per query tile and keeps dQ in tensor memory. That costs two extra GEMMs per
+// (query tile, key block) pair but needs no atomics, no fp32 dQ buffer and no
+// conversion pass, and the result does not depend on the order blocks finish.
+//
+//   bwd_preprocess_kernel: lse2 = LSE * log2(e) (+inf for rows without keys
+//     and for the padding rows) and D, per (sequence, q head, row).
+//   bwd_dq_kernel: one CTA per (128-row query tile, q head, sequence);
+//     S = Q K^T and dP = dO V^T for each visible key block, dS in bf16 back
+//     into tensor memory, dQ += dS K.
+//   bwd_dkdv_kernel: one CTA per (128-key block, KV head, sequence), looping
+//     over the q heads of its group and the query tiles that see the block;
+//     S^T = K Q^T and dP^T = V dO^T, P^T and dS^T in bf16 back into tensor
+//     memory, dV += P^T dO and dK += dS^T Q.
+//
+// Tensor memory (512 columns, one CTA per SM): S [0,128), dP [128,256),
+// accumulators from 256 (dQ; or dV then dK). The compute warps take each
+// 128-column score block in two 64-column halves; the bf16 result of half h
+// lands in columns [64h, 64h+32) of its own fp32 half, which that half has
+// already read, and the accumulating GEMM of half h runs while the warps work
+// on half h+1. Every GEMM has the operand forms of the forward kernel: SS with
+// two K-major 128B-swizzled tiles, and TS with the bf16 A operand in tensor
+// memory and an MN-major B tile.
+//
+// Warps 0-3 compute (thread t owns row t of the tile, tensor-memory lane t),
+// warp 4 issues the TMA loads, warp 5 the MMAs (one thread). Every wait is
+// bounded; on a timeout the CTA raises its abort flag, records the failure in
+// the device status word, drains its copies and MMAs, frees tensor memory and
+// returns.
+#include <cuda_bf16.h>
+
+#include "fa_kernels.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kB = 128;                 // rows of a query tile and of a key block
+constexpr int kChunk = 128 * 128;       // bytes of 128 rows x 64 bf16 columns (one 128B-swizzle chunk)
+
+template <int D>
+struct BwdCfg {
+  static constexpr int CH = D / 64;                    // 64-column chunks of a row
+  static constexpr int T_BYTES = CH * kChunk;          // one 128-row tile
+  static constexpr int ST = 2;                         // stages of the streamed tile pair
+  static constexpr int OFF_RES = 0;                    // resident pair: Q, dO (dQ) or K, V (dK/dV)
+  static constexpr int OFF_STR = 2 * T_BYTES;          // streamed pairs: K, V (dQ) or Q, dO (dK/dV)
+  static constexpr int OFF_VEC = OFF_STR + ST * 2 * T_BYTES;   // dK/dV: lse2[128], D[128] per stage
+  static constexpr int OFF_BAR = OFF_VEC + ST * 1024;
+  static constexpr int NBAR = 16;
+  static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
+  // at least half the SM's shared memory: one CTA (owning all 512 tensor-memory
+  // columns) per SM
+  static constexpr int SMEM = (SMEM_USED + 1024 < 120 * 1024) ? 120 * 1024 : SMEM_USED + 1024;
+  static constexpr int THREADS = 192;
+  static constexpr int TMA_WARP = 4, MMA_WARP = 5;
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(256 + 2 * D <= 512, "tensor memory budget");
+};
+
+struct BBars {
+  uint64_t* res_full;   // resident pair landed
+  uint64_t* str_full;   // [ST]
+  uint64_t* str_empty;  // [ST]
+  uint64_t* s_full;     // [2] per 64-column half: S and dP of the half complete
+  uint64_t* ds_full;    // [2] per half: bf16 operand written (4 arrivals, one per compute warp)
+  uint64_t* acc_full;   // accumulators final
+  uint64_t* drain;
+};
+
+template <class Cfg>
+__device__ __forceinline__ BBars carve(uint8_t* smem) {
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+  BBars B;
+  B.res_full = b; b += 1;
+  B.str_full = b; b += Cfg::ST;
+  B.str_empty = b; b += Cfg::ST;
+  B.s_full = b; b += 2;
+  B.ds_full = b; b += 2;
+  B.acc_full = b; b += 1;
+  B.drain = b; b += 1;
+  return B;
+}
+
+template <class Cfg>
+__device__ __forceinline__ void init_bars(const BBars& B) {
+  mbar_init(B.res_full, 1);
+  for (int i = 0; i < Cfg::ST; ++i) {
+    mbar_init(&B.str_full[i], 1);
+    mbar_init(&B.str_empty[i], 1);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&B.s_full[i], 1);
+    mbar_init(&B.ds_full[i], 4);
+  }
+  mbar_init(B.acc_full, 1);
+  mbar_init(B.drain, 1);
+  fence_barrier_init();
+}
+
+// Spin (bounded, ignoring the abort flag) until the given phase completed:
+// used to drain copies / MMAs in flight before the CTA exits.
+__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity) && global_timer_ns() - t0 < timeout_ns) {
+  }
+}
+
+// D[128 x 128] = A[128 x kdim] B[128 x kdim]^T, both K-major 128B-swizzled
+// tiles of 64-column chunks (16 bf16 per instruction).
+__device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, int kdim, uint32_t idesc) {
+  const uint64_t ad = sdesc_sw128(a_base, 16, 1024), bd = sdesc_sw128(b_base, 16, 1024);
+  for (int kk = 0; kk < kdim / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+    mma_bf16_ss(d_tmem, ad + off, bd + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[128 x N] (+)= A_h B_h for half h of the 128-deep contraction: A is bf16 in
+// tensor memory (columns [64h, 64h+32) of a_tmem, two values per column), B is
+// rows [64h, 64h+64) of an MN-major tile (64-column chunks kChunk bytes apart).
+__device__ __forceinline__ void issue_ts_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, int h,
+                                              uint32_t idesc, bool acc) {
+  const uint64_t bd = sdesc_sw128(b_base, kChunk, 1024);
+#pragma unroll
+  for (int k4 = 0; k4 < 4; ++k4) {
+    const int kk = h * 4 + k4;
+    mma_bf16_ts(d_tmem, a_tmem + h * 64 + k4 * 8, bd + ((kk * 16 * 128) >> 4), idesc, (acc || k4 > 0) ? 1u : 0u);
+  }
+}
+
+// 32 fp32 accumulator columns of one row, times f, to 64 bytes of bf16
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&o)[32], float f) {
+  uint32_t w[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * f, __uint_as_float(o[2 * e + 1]) * f);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
+  d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+}
+
+__device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int d) {
+  for (int c = 0; c < d / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------------------
+// preprocess: 8 threads per row
+__global__ void bwd_preprocess_kernel(const BwdParams p, int dv) {
+  const int sub = threadIdx.x & 7;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 3) + (threadIdx.x >> 3);
+  // rows = batch * hq * sq_pad, a multiple of 128, and the grid covers it
+  // exactly, so every warp is whole for the shuffles below
+  const int i = static_cast<int>(row % p.sq_pad);
+  const int64_t bh = row / p.sq_pad;
+  const int h = static_cast<int>(bh % p.hq), b = static_cast<int>(bh / p.hq);
+  float acc = 0.f;
+  if (i < p.seqlen_q) {
+    const int64_t o_off = int64_t(b) * p.o_bs + int64_t(i) * p.o_rs + int64_t(h) * p.o_hs;
+    const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.out) + o_off;
+    const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + o_off;
+    for (int c = sub * 8; c < dv; c += 64) {
+      const uint4 a = *reinterpret_cast<const uint4*>(o + c), d = *reinterpret_cast<const uint4*>(g + c);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, dw[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(bf16lo_to_f32(aw[e]), bf16lo_to_f32(dw[e]), acc);
+        acc = fmaf(bf16hi_to_f32(aw[e]), bf16hi_to_f32(dw[e]), acc);
+      }
+    }
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  if (sub == 0) {
+    float l2 = INFINITY;   // P = exp2(... - inf) = 0
+    if (i < p.seqlen_q) {
+      const float lse = p.lse[(int64_t(b) * p.hq + h) * p.seqlen_q + i];
+      if (lse != -INFINITY) l2 = lse * 1.4426950408889634f;
+    }
+    p.lse2[row] = l2;
+    p.dsum[row] = acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                  const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
+                  const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const BBars B = carve<Cfg>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_BAR + Cfg::NBAR * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int b = blockIdx.x / p.hq, h = blockIdx.x % p.hq, g = h / p.r;
+  const int mb = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);   // longest tiles first
+  const int off = p.seqlen_k - p.seqlen_q;
+  const int i0 = mb * kB, ilast = min(i0 + kB - 1, p.seqlen_q - 1);
+  int klo = 0, khi = p.seqlen_k;
+  if (p.wl >= 0) klo = max(klo, i0 + off - p.wl);
+  if (p.wr >= 0) khi = min(khi, ilast + off + p.wr + 1);
+  const int nlo = klo / kB, nhi = (khi > klo) ? (khi + kB - 1) / kB : nlo;
+  const bool has = nhi > nlo;
+
+  if (threadIdx.x == 0) {
+    init_bars<Cfg>(B);
+    *abort_flag = 0;
+  }
+  if (warp == Cfg::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitGuard guard{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == Cfg::TMA_WARP) {
+    if (lane == 0 && has) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      tma_prefetch_desc(&mapDO);
+      uint8_t* res = smem + Cfg::OFF_RES;
+      mbar_arrive_expect_tx(B.res_full, 2 * Cfg::T_BYTES);
+#pragma unroll
+      for (int c = 0; c < Cfg::CH; ++c) {
+        tma_load_4d(res + c * kChunk, &mapQ, B.res_full, c * 64, i0, h, b);
+        tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapDO, B.res_full, c * 64, i0, h, b);
+      }
+      uint32_t u = 0;
+      for (int n = nhi - 1; n >= nlo; --n, ++u) {
+        const int st = u % Cfg::ST;
+        if (u >= Cfg::ST && !mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard)) break;
+        uint8_t* dst = smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES;
+        mbar_arrive_expect_tx(&B.str_full[st], 2 * Cfg::T_BYTES);
+#pragma unroll
+        for (int c = 0; c < Cfg::CH; ++c) {
+          tma_load_4d(dst + c * kChunk, &mapK, &B.str_full[st], c * 64, n * kB, g, b);
+          tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapV, &B.str_full[st], c * 64, n * kB, g, b);
+        }
+      }
+      // drain the copies still in flight (only after an abort can any be)
+      for (uint32_t x = (u > (uint32_t)Cfg::ST ? u - Cfg::ST : 0); x < u; ++x)
+        drain_phase(&B.str_full[x % Cfg::ST], (x / Cfg::ST) & 1, p.timeout_ns);
+      drain_phase(B.res_full, 0, p.timeout_ns);
+    }
+  } else if (warp == Cfg::MMA_WARP) {
+    if (lane == 0 && has) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
+      constexpr uint32_t IDESC_DQ = idesc_bf16_f32(kB, D, false, true);
+      const uint32_t q_base = smem_u32(smem + Cfg::OFF_RES), do_base = q_base + Cfg::T_BYTES;
+      bool ok = mbar_wait(B.res_full, 0, guard);
+      uint32_t u = 0;
+      for (int n = nhi - 1; ok && n >= nlo; --n, ++u) {
+        const int st = u % Cfg::ST;
+        const uint32_t kb = smem_u32(smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES), vb = kb + Cfg::T_BYTES;
+        if (!mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard)) { ok = false; break; }
+        issue_ss(tmem, q_base, kb, D, IDESC_S);          // S  = Q K^T
+        issue_ss(tmem + 128, do_base, vb, D, IDESC_S);   // dP = dO V^T
+        mma_commit(&B.s_full[0]);
+        mma_commit(&B.s_full[1]);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&B.ds_full[hh], u & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+          issue_ts_half(tmem + 256, tmem, kb, hh, IDESC_DQ, u > 0 || hh > 0);   // dQ += dS_h K_h
+        }
+        if (!ok) break;
+        mma_commit(&B.str_empty[st]);
+      }
+      if (ok) mma_commit(B.acc_full);
+      mma_commit(B.drain);
+      drain_phase(B.drain, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ================= compute warps: thread t <-> query row i0 + t =================
+    const int t = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int i = i0 + t;
+    const int64_t vrow = (int64_t(b) * p.hq + h) * p.sq_pad + i;
+    __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(p.dq) + int64_t(b) * p.q_bs + int64_t(i) * p.q_rs +
+                        int64_t(h) * p.q_hs;
+    if (has) {
+      const float nl2 = -p.lse2[vrow], dsum = p.dsum[vrow];
+      bool ok = true;
+      uint32_t u = 0;
+      for (int n = nhi - 1; n >= nlo; --n, ++u) {
+        const int jb = n * kB;
+        // every (row, key) of the block visible?  (uniform over the CTA)
+        const bool full = (jb + kB <= p.seqlen_k) && (p.wr < 0 || jb + kB - 1 <= i0 + off + p.wr) &&
+                          (p.wl < 0 || jb >= i0 + kB - 1 + off - p.wl);
+        // visible columns [c_lo, c_hi] of this row
+        const int c_lo = (p.wl >= 0) ? i + off - p.wl - jb : INT32_MIN / 2;
+        int c_hi = p.seqlen_k - 1 - jb;
+        if (p.wr >= 0) c_hi = min(c_hi, i + off + p.wr - jb);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&B.s_full[hh], u & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t s[64], dp[64];
+          tmem_ld64(tmem + lane_off + hh * 64, s);
+          tmem_ld64(tmem + lane_off + 128 + hh * 64, dp);
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), p.scale_log2, nl2));
+            float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), p.scale_log2, nl2));
+            if (!full) {
+              const int cc = hh * 64 + c;
+              p0 = (cc < c_lo || cc > c_hi) ? 0.f : p0;
+              p1 = (cc + 1 < c_lo || cc + 1 > c_hi) ? 0.f : p1;
+            }
+            w[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[c]) - dsum), p1 * (__uint_as_float(dp[c + 1]) - dsum));
+          }
+          tmem_st32(tmem + lane_off + hh * 64, w);   // dS_h over the half's first 32 columns
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.ds_full[hh]);
+        }
+        if (!ok) break;
+      }
+      if (ok && mbar_wait(B.acc_full, 0, guard)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + 256 + c * 32, o);
+          if (i < p.seqlen_q) store_row32(dq + c * 32, o, p.scale);
+        }
+      }
+    } else if (i < p.seqlen_q) {
+      zero_row(dq, D);   // no visible key: dQ = 0
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Cfg::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                    const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
+                    const BwdParams p) {
+  using Cfg = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const BBars B = carve<Cfg>(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_BAR + Cfg::NBAR * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int b = blockIdx.x / p.hkv, g = blockIdx.x % p.hkv;
+  const int n = blockIdx.y;   // low key blocks first: under a causal mask they see the most query tiles
+  const int off = p.seqlen_k - p.seqlen_q;
+  const int j0 = n * kB, jlast = min(j0 + kB - 1, p.seqlen_k - 1);
+  // query rows that see some key of the block
+  int ilo = 0, ihi = p.seqlen_q - 1;
+  if (p.wr >= 0) ilo = max(ilo, j0 - off - p.wr);
+  if (p.wl >= 0) ihi = min(ihi, jlast - off + p.wl);
+  const int mlo = ilo / kB, nm = (ihi >= ilo) ? ihi / kB + 1 - mlo : 0;
+  const int jobs = nm * p.r;   // (q head of the group, query tile) pairs, head-major
+
+  if (threadIdx.x == 0) {
+    init_bars<Cfg>(B);
+    *abort_flag = 0;
+  }
+  if (warp == Cfg::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitGuard guard{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == Cfg::TMA_WARP) {
+    if (lane == 0 && jobs > 0) {
+      tma_prefetch_desc(&mapQ);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      tma_prefetch_desc(&mapDO);
+      uint8_t* res = smem + Cfg::OFF_RES;
+      mbar_arrive_expect_tx(B.res_full, 2 * Cfg::T_BYTES);
+#pragma unroll
+      for (int c = 0; c < Cfg::CH; ++c) {
+        tma_load_4d(res + c * kChunk, &mapK, B.res_full, c * 64, j0, g, b);
+        tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapV, B.res_full, c * 64, j0, g, b);
+      }
+      uint32_t u = 0;
+      for (; u < static_cast<uint32_t>(jobs); ++u) {
+        const int st = u % Cfg::ST;
+        const int hh = g * p.r + static_cast<int>(u) / nm, m = mlo + static_cast<int>(u) % nm;
+        if (u >= Cfg::ST && !mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard)) break;
+        uint8_t* dst = smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES;
+        float* vec = reinterpret_cast<float*>(smem + Cfg::OFF_VEC + st * 1024);
+        const int64_t vrow = (int64_t(b) * p.hq + hh) * p.sq_pad + m * kB;
+        mbar_arrive_expect_tx(&B.str_full[st], 2 * Cfg::T_BYTES + 1024);
+#pragma unroll
+        for (int c = 0; c < Cfg::CH; ++c) {
+          tma_load_4d(dst + c * kChunk, &mapQ, &B.str_full[st], c * 64, m * kB, hh, b);
+          tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapDO, &B.str_full[st], c * 64, m * kB, hh, b);
+        }
+        bulk_load(vec, p.lse2 + vrow, 512, &B.str_full[st]);
+        bulk_load(vec + 128, p.dsum + vrow, 512, &B.str_full[st]);
+      }
+      for (uint32_t x = (u > (uint32_t)Cfg::ST ? u - Cfg::ST : 0); x < u; ++x)
+        drain_phase(&B.str_full[x % Cfg::ST], (x / Cfg::ST) & 1, p.timeout_ns);
+      drain_phase(B.res_full, 0, p.timeout_ns);
+    }
+  } else if (warp == Cfg::MMA_WARP) {
+    if (lane == 0 && jobs > 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
+      constexpr uint32_t IDESC_ACC = idesc_bf16_f32(kB, D, false, true);
+      const uint32_t k_base = smem_u32(smem + Cfg::OFF_RES), v_base = k_base + Cfg::T_BYTES;
+      bool ok = mbar_wait(B.res_full, 0, guard);
+      for (uint32_t u = 0; ok && u < static_cast<uint32_t>(jobs); ++u) {
+        const int st = u % Cfg::ST;
+        const uint32_t qb = smem_u32(smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES), dob = qb + Cfg::T_BYTES;
+        if (!mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard)) { ok = false; break; }
+        issue_ss(tmem, k_base, qb, D, IDESC_S);           // S^T  = K Q^T
+        issue_ss(tmem + 128, v_base, dob, D, IDESC_S);    // dP^T = V dO^T
+        mma_commit(&B.s_full[0]);
+        mma_commit(&B.s_full[1]);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&B.ds_full[hh], u & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+          const bool acc = u > 0 || hh > 0;
+          issue_ts_half(tmem + 256, tmem, dob, hh, IDESC_ACC, acc);            // dV += P^T_h dO_h
+          issue_ts_half(tmem + 256 + D, tmem + 128, qb, hh, IDESC_ACC, acc);   // dK += dS^T_h Q_h
+        }
+        if (!ok) break;
+        mma_commit(&B.str_empty[st]);
+      }
+      if (ok) mma_commit(B.acc_full);
+      mma_commit(B.drain);
+      drain_phase(B.drain, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ================= compute warps: thread t <-> key row j0 + t =================
+    const int t = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int j = j0 + t;
+    __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk) + int64_t(b) * p.k_bs + int64_t(j) * p.k_rs +
+                        int64_t(g) * p.k_hs;
+    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv) + int64_t(b) * p.v_bs + int64_t(j) * p.v_rs +
+                        int64_t(g) * p.v_hs;
+    if (jobs > 0) {
+      bool ok = true;
+      for (uint32_t u = 0; u < static_cast<uint32_t>(jobs); ++u) {
+        const int st = u % Cfg::ST;
+        const int m = mlo + static_cast<int>(u) % nm;
+        const int ib = m * kB;
+        const bool full = (j0 + kB <= p.seqlen_k) && (ib + kB <= p.seqlen_q) &&
+                          (p.wr < 0 || j0 + kB - 1 <= ib + off + p.wr) && (p.wl < 0 || j0 >= ib + kB - 1 + off - p.wl);
+        // visible query columns [c_lo, c_hi] of this key row
+        const int c_lo = (p.wr >= 0) ? j - off - p.wr - ib : INT32_MIN / 2;
+        int c_hi = p.seqlen_q - 1 - ib;
+        if (p.wl >= 0) c_hi = min(c_hi, j - off + p.wl - ib);
+        if (j >= p.seqlen_k) c_hi = -1;
+        // the stage's lse2 / D landed with its tiles
+        if (!mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard)) { ok = false; break; }
+        const float* vec = reinterpret_cast<const float*>(smem + Cfg::OFF_VEC + st * 1024);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&B.s_full[hh], u & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t s[64], dp[64];
+          tmem_ld64(tmem + lane_off + hh * 64, s);
+          tmem_ld64(tmem + lane_off + 128 + hh * 64, dp);
+          uint32_t pw[32], dw[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(vec + hh * 64 + c);
+            const float4 d4 = *reinterpret_cast<const float4*>(vec + 128 + hh * 64 + c);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pr[4], dsr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float pe = ex2_approx(fmaf(__uint_as_float(s[c + e]), p.scale_log2, -lv[e]));
+              if (!full) {
+                const int cc = hh * 64 + c + e;
+                pe = (cc < c_lo || cc > c_hi) ? 0.f : pe;
+              }
+              pr[e] = pe;
+              dsr[e] = pe * (__uint_as_float(dp[c + e]) - dv4[e]);
+            }
+            pw[c >> 1] = pack_bf16x2(pr[0], pr[1]);
+            pw[(c >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
+            dw[c >> 1] = pack_bf16x2(dsr[0], dsr[1]);
+            dw[(c >> 1) + 1] = pack_bf16x2(dsr[2], dsr[3]);
+          }
+          tmem_st32(tmem + lane_off + hh * 64, pw);         // P^T_h
+          tmem_st32(tmem + lane_off + 128 + hh * 64, dw);   // dS^T_h
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.ds_full[hh]);
+        }
+        if (!ok) break;
+      }
+      if (ok && mbar_wait(B.acc_full, 0, guard)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + 256 + c * 32, o);
+          if (j < p.seqlen_k) store_row32(dv + c * 32, o, 1.f);
+        }
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + 256 + D + c * 32, o);
+          if (j < p.seqlen_k) store_row32(dk + c * 32, o, p.scale);
+        }
+      }
+    } else if (j < p.seqlen_k) {
+      zero_row(dv, D);   // no query sees these keys
+      zero_row(dk, D);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == Cfg::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mdo, cudaStream_t stream) {
+  using Cfg = BwdCfg<D>;
+  const int64_t rows = int64_t(p.batch) * p.hq * p.sq_pad;
+  if (rows > 0) {
+    bwd_preprocess_kernel<<<static_cast<unsigned>(rows / 32), 256, 0, stream>>>(p, D);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int mblocks = (p.seqlen_q + kB - 1) / kB, nblocks = (p.seqlen_k + kB - 1) / kB;
+  if (mblocks > 0) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    bwd_dq_kernel<D><<<dim3(p.batch * p.hq, mblocks), Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (nblocks > 0) {
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    bwd_dkdv_kernel<D><<<dim3(p.batch * p.hkv, nblocks), Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+bool bwd_supported(int dk, int dv) { return (dk == 64 && dv == 64) || (dk == 128 && dv == 128); }
+
+cudaError_t launch_bwd(const BwdParams& p, int d, const CUtensorMap& mq, const CUtensorMap& mk,
+                       const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream) {
+  if (d == 64) return launch_bwd_t<64>(p, mq, mk, mv, mdo, stream);
+  if (d == 128) return launch_bwd_t<128>(p, mq, mk, mv, mdo, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -56,6 +56,34 @@ cudaError_t launch_decode(const FwdParams& p, int dk, int dv, const CUtensorMap&
 bool decode_supported(int dk, int dv);
 int decode_max_rows();
 
+// Backward (dQ, dK, dV): batched layout, head dims 64 or 128 (dk == dv).
+// dq / dk / dv take q's / k's / v's strides, dout and out take the o strides;
+// lse2 and dsum are workspace arrays [batch][hq][sq_pad] (sq_pad = 128-row
+// multiple of seqlen_q).
+struct BwdParams {
+  const void* out;
+  const void* dout;
+  const float* lse;              // forward LSE [batch][hq][seqlen_q], natural log
+  void* dq;
+  void* dk;
+  void* dv;
+  float* lse2;                   // LSE * log2(e); +inf where P must be 0
+  float* dsum;                   // rowsum(dO * O)
+  int64_t q_bs, q_rs, q_hs;
+  int64_t k_bs, k_rs, k_hs;
+  int64_t v_bs, v_rs, v_hs;
+  int64_t o_bs, o_rs, o_hs;
+  int batch, seqlen_q, seqlen_k, sq_pad;
+  int hq, hkv, r;
+  float scale, scale_log2;
+  int wl, wr;                    // -1 = unbounded; wr is 0 when causal
+  int* status;
+  unsigned long long timeout_ns;
+};
+cudaError_t launch_bwd(const BwdParams& p, int d, const CUtensorMap& mq, const CUtensorMap& mk,
+                       const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream);
+bool bwd_supported(int dk, int dv);
+
 struct CombineParams {
   const float* out_partial;
   const float* lse_partial;

@@ -102,6 +102,10 @@ _lib.fa_status_string.argtypes = [ctypes.c_int]
 _lib.fa_status_string.restype = ctypes.c_char_p
 _lib.fa_fwd_decode_noalloc.argtypes = [_P, _vp]
 _lib.fa_fwd_decode_noalloc.restype = ctypes.c_int
+_lib.fa_bwd.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.fa_bwd.restype = ctypes.c_int
+_lib.fa_bwd_workspace_size.argtypes = [_P]
+_lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
 _lib.fa_abi_version.argtypes = []
 _lib.fa_abi_version.restype = ctypes.c_int
 
@@ -260,6 +264,37 @@ def fa_combine(out_partial, lse_partial, out=None, lse=None, *, cu_seqlens_q=Non
                            _ptr(cu_seqlens_q), total_q, _ptr(out), obs, ors, ohs, _ptr(lse),
                            _vp(_stream_handle(stream))), "fa_combine")
     return out, lse
+
+
+def fa_bwd_workspace_size(args: FwdArgs) -> int:
+    return int(_lib.fa_bwd_workspace_size(ctypes.byref(args)))
+
+
+def fa_bwd(q, k, v, out, lse, dout, dq=None, dk=None, dv=None, *, workspace=None, stream=None, **kw):
+    """dQ, dK, dV of the forward (q, k, v) -> (out, lse), given dO.
+
+    Batched layout. out and lse are the forward's results; dout has out's
+    shape and strides; dq / dk / dv (allocated when None) take q's / k's / v's.
+    kw: the forward's mask and scale keywords (see make_args).
+    """
+    if dq is None:
+        dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    if dv is None:
+        dv = torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=v.device)
+    for name, a, b in (("dout", dout, out), ("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if a.shape != b.shape or a.stride() != b.stride():
+            raise ValueError(f"{name} must have the shape and strides of its forward tensor")
+    args = make_args(q, k, v, out, lse, **kw)
+    need = fa_bwd_workspace_size(args)
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace) if need > 0 else None
+    ws_bytes = workspace.numel() * workspace.element_size() if need > 0 else 0
+    _check(_lib.fa_bwd(ctypes.byref(args), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), ws_ptr, ws_bytes,
+                       _vp(_stream_handle(stream))), "fa_bwd")
+    return dq, dk, dv
 
 
 def default_scale(head_dim_qk: int) -> float:

@@ -40,8 +40,8 @@ from typing import Optional
 
 import numpy as np
 
-# tensor ids inside a workload's SeedSequence
-_Q, _K, _V = 0, 1, 2
+# tensor ids inside a workload's SeedSequence (_DO: the output gradient of a backward)
+_Q, _K, _V, _DO = 0, 1, 2, 3
 
 # bfloat16 bit pattern of a quiet NaN; written into KV-cache slots past
 # seqused_k so that any read of them that reaches the arithmetic shows up.
@@ -168,6 +168,15 @@ def batched(name, seed, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale=None, causal=False,
                     seqlen_q=Sq, seqlen_k=Sk,
                     seqused_k=None if seqused_k is None else np.asarray(seqused_k, np.int32),
                     max_seqlen_q=Sq, max_seqlen_k=Sk, seed=seed)
+
+
+def grad_out(w: Workload) -> np.ndarray:
+    """dO for the backward of a batched workload: N(0,1) bf16 bits with the
+    output's shape (B, Sq, Hq, Dv), one stream per sequence."""
+    do = np.empty((w.batch, w.seqlen_q, w.num_heads_q, w.head_dim_v), np.uint16)
+    for b in range(w.batch):
+        do[b] = normal_bf16(w.seed, _DO, b, (w.seqlen_q, w.num_heads_q, w.head_dim_v))
+    return do
 
 
 def fp8_batched(name, seed, B, Sq, Sk, Hq, Hkv, D, fmt, seqused_k=None, scale=None, causal=False):

@@ -1,5 +1,6 @@
 /*
- * fa.h - C ABI of the GB300 (sm_103a) exact attention forward library (libfa.so).
+ * fa.h - C ABI of the GB300 (sm_103a) exact attention library (libfa.so): the
+ * forward with its per-row LSE, and its backward.
  *
  * The operation is the exact scaled-dot-product attention forward with a
  * per-row log-sum-exp, as defined by the FlashAttention pages:
@@ -214,6 +215,30 @@ int fa_combine(const float* out_partial, const float* lse_partial, int num_split
 #define FA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
 
+/*
+ * fa_bwd - gradients dQ, dK, dV of the forward described by args, given dO
+ * ("mslk/attention/flash_attn/flash_bwd_sm100.py": the preprocess forms
+ * D = rowsum(dO * O); the main loop recomputes P from the stored LSE and forms
+ *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q;
+ * with GQA, dK and dV of KV head g sum over the q heads that read it).
+ * args: the forward's arguments, batched layout. args->out must hold the
+ *   forward's O and args->lse its LSE (both read, not written).
+ * dout: dO, bf16, out's shape and strides (o_*_stride).
+ * dq / dk / dv: written, bf16, with q's / k's / v's shapes and strides. Keys
+ *   that no query sees get dK = dV = 0; rows that see no key get dQ = 0.
+ * Supported: (head_dim_qk, head_dim_v) (64,64) or (128,128); causal, sliding
+ *   window and GQA/MQA as in the forward. cu_seqlens, seqused_k, a page table
+ *   or an fp8 cache give FA_ERR_UNSUPPORTED.
+ * workspace: at least fa_bwd_workspace_size(args) bytes, 256-byte aligned
+ *   (fp32 LSE * log2(e) and D for every padded query row). The call is
+ *   deterministic: no atomics, the same inputs give the same bits.
+ */
+int fa_bwd(const fa_fwd_args* args, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+           size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fa_bwd needs for args (0 when fa_bwd would reject args). */
+size_t fa_bwd_workspace_size(const fa_fwd_args* args);
+
 /* Bytes of workspace fa_fwd needs for args (with args->num_splits resolved as fa_fwd does). */
 size_t fa_workspace_size(const fa_fwd_args* args);
 
@@ -242,7 +267,8 @@ void fa_set_wait_timeout_ns(uint64_t ns);
 /* Static text for a status code. */
 const char* fa_status_string(int status);
 
-/* ABI version (major*100 + minor): 200 since fa_fwd_args gained the KV-cache fields. */
+/* ABI version (major*100 + minor): 200 since fa_fwd_args gained the KV-cache
+ * fields, 201 since fa_bwd. */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

@@ -59,7 +59,7 @@ def test_struct_layout_matches_header(fa, tmp_path):
     assert int(got["sizeof"]) == ctypes.sizeof(fa.FwdArgs)
     for n in fields:
         assert int(got[n]) == getattr(fa.FwdArgs, n).offset, n
-    assert fa.fa_abi_version() == 200
+    assert fa.fa_abi_version() == 201
 
 
 def _args(fa, **over):
@@ -137,3 +137,32 @@ def test_status_strings(fa):
     for c in range(8):
         assert fa.fa_status_string(c)
     assert "unknown" in fa.fa_status_string(99)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(cu_seqlens_q=0x50000, cu_seqlens_k=0x60000, total_q=600, total_k=600, max_seqlen_q=300,
+          max_seqlen_k=300), 2),                         # varlen
+    (dict(seqused_k=0x50000), 2),
+    (dict(page_table=0x50000, max_pages_per_seq=3, page_size=128, num_pages=6), 2),
+    (dict(kv_format=1), 2),                               # fp8 cache
+    (dict(head_dim_qk=192, head_dim_v=128), 2),           # forward-only head dims
+    (dict(head_dim_qk=256, head_dim_v=256), 2),
+    (dict(num_heads_q=6, num_heads_kv=4), 1),
+    (dict(out=0), 1),
+    (dict(lse=0), 1),                                     # the forward's LSE is an input
+])
+def test_backward_rejections_before_launch(fa, over, code):
+    a = _args(fa, **over)
+    if "lse" not in over:
+        a.lse = 0x70000
+    assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == code
+
+
+def test_backward_workspace(fa):
+    a = _args(fa, lse=0x70000)
+    # lse2 and D for 2 x 8 heads x 384 padded rows, 256-byte aligned
+    assert fa.fa_bwd_workspace_size(a) == 2 * 2 * 8 * 384 * 4
+    assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 4
+    assert fa.lib().fa_bwd(ctypes.byref(a), 0x80008, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 3
+    assert fa.fa_bwd_workspace_size(_args(fa, head_dim_qk=192, head_dim_v=128)) == 0
+    assert fa.lib().fa_bwd(ctypes.byref(_args(fa, batch=0)), 0, 0, 0, 0, None, 0, None) == 0

@@ -1,0 +1,166 @@
+"""Attention backward through the C ABI vs the fp64 oracle: dQ, dK, dV for
+head dims 64 and 128, causal and sliding-window masks with Sq != Sk, GQA and
+MQA, ragged tails, empty axes, determinism, and the full-size causal workload
+checked on one KV head group.
+
+Tolerance. The kernels round P and dS to bf16 (relative error at most 2^-9 per
+element) before the GEMMs that accumulate them in fp32, take D = rowsum(dO * O)
+from the bf16 O of the forward, and round dQ, dK and dV to bf16 (again at most
+2^-9 relative). The sums run over many terms of both signs, so an element's
+error is about 2^-9 of its magnitude: per tensor, max|err| <= 1.5e-2 max|ref|
+and mean|err| <= 4e-3 mean|ref| leave a margin of about 3 over that."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+from exact_attention_qk_gb300 import inputs  # noqa: E402
+import gpu_util as gu  # noqa: E402
+
+TOL_MAX_REL = 1.5e-2
+TOL_MEAN_REL = 4e-3
+# An all-zero reference that comes from cancellation (a row seeing one key:
+# P = 1 and dS = dP - D = dO.v - dO.O = 0 exactly) leaves fp32 rounding behind:
+# dP and D are dot products of at most 128 N(0,1) bf16 pairs (|.| <~ 50) summed
+# in different orders, so |dP - D| <~ 50 x 2^-20 ~ 5e-5, and dQ / dK take it
+# times scale (<= 1/8) times one key or query row (|.| <~ 5): below 1e-4.
+TOL_CANCELLED_ZERO = 1e-4
+
+
+def run_bwd(w, do_bits):
+    from exact_attention_qk_gb300 import fa
+    q, k, v, do = gu.to_dev(w.q), gu.to_dev(w.k), gu.to_dev(w.v), gu.to_dev(do_bits)
+    o, lse = fa.fa_fwd(q, k, v, **gu.kw_of(w))
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, **gu.kw_of(w))
+    assert fa.fa_get_status() == fa.FA_OK
+    return dq, dk, dv
+
+
+def oracle_bwd(w, do_bits):
+    return oracle.attention_backward(w.q, w.k, w.v, do_bits, scale=w.softmax_scale, causal=w.causal,
+                                     window_left=w.window_left, window_right=w.window_right)
+
+
+def compare(got, ref, what):
+    g = gu.to64(got)
+    assert np.isfinite(g).all(), f"{what}: non-finite values"
+    err = np.abs(g - ref)
+    mx, mean = float(np.abs(ref).max()) if ref.size else 0.0, float(np.abs(ref).mean()) if ref.size else 0.0
+    if mx == 0.0:
+        assert err.size == 0 or err.max() <= TOL_CANCELLED_ZERO, f"{what}: expected ~0, max|got| {err.max():.3e}"
+        return f"{what}: zeros (max|got| {err.max() if err.size else 0.0:.1e})"
+    assert err.max() <= TOL_MAX_REL * mx, f"{what}: max|err| {err.max():.3e} > {TOL_MAX_REL} x {mx:.3e}"
+    assert err.mean() <= TOL_MEAN_REL * mean, f"{what}: mean|err| {err.mean():.3e} > {TOL_MEAN_REL} x {mean:.3e}"
+    return f"{what}: max {err.max() / mx:.2e} mean {err.mean() / mean:.2e} (relative)"
+
+
+def check_bwd(w):
+    do = inputs.grad_out(w)
+    got = run_bwd(w, do)
+    ref = oracle_bwd(w, do)
+    return "; ".join(compare(g, r, n) for g, r, n in zip(got, ref, ("dQ", "dK", "dV")))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dims_gqa(d, causal):
+    # 300 rows: two full 128-row tiles and a 44-row tail; GQA 4/2
+    w = inputs.batched("bwd", 400 + d, 2, 300, 300, 4, 2, d, d, causal=causal)
+    print(check_bwd(w))
+
+
+@pytest.mark.parametrize("sq,sk", [(200, 520), (520, 200), (1, 300), (300, 1), (128, 129), (129, 128)])
+def test_causal_unequal_lengths(sq, sk):
+    # bottom-right causal: with sq > sk the first sq - sk rows see no key (dQ = 0)
+    w = inputs.batched("bwdne", 410 + sq % 97 + sk % 89, 1, sq, sk, 4, 1, 128, 128, causal=True)
+    print(check_bwd(w))
+
+
+@pytest.mark.parametrize("wl,wr", [(100, 0), (50, 70), (0, 0), (300, -1), (-1, 40)])
+def test_sliding_window(wl, wr):
+    w = inputs.batched("bwdw", 420 + max(wl, 0) + max(wr, 0), 2, 390, 450, 4, 2, 128, 128, window_left=wl,
+                       window_right=wr)
+    print(check_bwd(w))
+
+
+def test_mqa_and_head_dim_64_window():
+    w = inputs.batched("bwdmqa", 430, 1, 333, 333, 8, 1, 64, 64, causal=True, window_left=77)
+    print(check_bwd(w))
+
+
+def test_explicit_scale_and_several_kv_blocks():
+    w = inputs.batched("bwdsc", 431, 1, 700, 1100, 2, 2, 128, 128, scale=0.05)
+    print(check_bwd(w))
+
+
+def test_tiny_shapes():
+    for sq, sk in ((1, 1), (5, 3), (3, 5), (17, 17)):
+        w = inputs.batched("bwdtiny", 432 + sq, 1, sq, sk, 2, 1, 64, 64, causal=(sq == 17))
+        print(check_bwd(w))
+
+
+def test_empty_query_axis_zeroes_dk_dv():
+    from exact_attention_qk_gb300 import fa
+    w = inputs.batched("bwdeq", 433, 1, 1, 200, 2, 1, 128, 128)
+    q = torch.zeros(1, 0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    k, v = gu.to_dev(w.k), gu.to_dev(w.v)
+    o = torch.zeros(1, 0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 2, 0, dtype=torch.float32, device="cuda")
+    dk = torch.full_like(k, float("nan"))
+    dv = torch.full_like(v, float("nan"))
+    _, dk, dv = fa.fa_bwd(q, k, v, o, lse, o.clone(), dk=dk, dv=dv)
+    assert fa.fa_get_status() == fa.FA_OK
+    assert torch.count_nonzero(dk).item() == 0 and torch.count_nonzero(dv).item() == 0
+
+
+def test_empty_key_axis_zeroes_dq():
+    from exact_attention_qk_gb300 import fa
+    w = inputs.batched("bwdek", 436, 1, 200, 1, 2, 1, 128, 128)
+    q, do = gu.to_dev(w.q), gu.to_dev(inputs.grad_out(w))
+    k = torch.zeros(1, 0, 1, 128, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros_like(q)
+    lse = torch.full((1, 2, 200), float("-inf"), dtype=torch.float32, device="cuda")
+    dq = torch.full_like(q, float("nan"))
+    dq, _, _ = fa.fa_bwd(q, k, k.clone(), o, lse, do, dq=dq)
+    assert fa.fa_get_status() == fa.FA_OK
+    assert torch.count_nonzero(dq).item() == 0
+
+
+def test_keys_no_query_sees_get_zero_gradients():
+    # a 100-key window behind each row: keys past the last row's window never count
+    w = inputs.batched("bwdunseen", 434, 1, 150, 600, 2, 1, 128, 128, window_left=100, window_right=0)
+    do = inputs.grad_out(w)
+    dq, dk, dv = run_bwd(w, do)
+    rq, rk, rv = oracle_bwd(w, do)
+    assert np.all(rk[0, :350] == 0) and np.all(rv[0, :350] == 0)
+    assert torch.count_nonzero(dk[0, :350]).item() == 0 and torch.count_nonzero(dv[0, :350]).item() == 0
+    print(compare(dq, rq, "dQ"), compare(dk, rk, "dK"), compare(dv, rv, "dV"))
+
+
+def test_deterministic():
+    w = inputs.batched("bwddet", 435, 2, 600, 600, 8, 2, 128, 128, causal=True)
+    do = inputs.grad_out(w)
+    a = run_bwd(w, do)
+    b = run_bwd(w, do)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+@pytest.mark.slow
+def test_full_size_causal_one_kv_group():
+    """The causal workload (B=2, S=4096, Hq=32, Hkv=4, D=128): every element of
+    dK and dV of KV head 3 of sequence 1, and dQ of the 8 q heads reading it."""
+    w = inputs.workload("causal")
+    do = inputs.grad_out(w)
+    dq, dk, dv = run_bwd(w, do)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all().item()
+    b, g, r = 1, 3, w.num_heads_q // w.num_heads_kv
+    hs = slice(g * r, (g + 1) * r)
+    rq, rk, rv = oracle.attention_backward(w.q[b:b + 1, :, hs], w.k[b:b + 1, :, g:g + 1], w.v[b:b + 1, :, g:g + 1],
+                                           do[b:b + 1, :, hs], scale=w.softmax_scale, causal=True)
+    print(compare(dq[b:b + 1, :, hs], rq, "dQ"), compare(dk[b:b + 1, :, g:g + 1], rk, "dK"),
+          compare(dv[b:b + 1, :, g:g + 1], rv, "dV"))
