@@ -91,6 +91,18 @@ def is_decode(name):
     return name.startswith("decode")
 
 
+def is_backward(name):
+    return name.endswith("_bwd")
+
+
+def backward_flops(w) -> float:
+    """The five GEMMs of the backward per visible (row, key) pair: S = QK^T
+    recomputed, dP = dO V^T, dV = P^T dO, dQ = dS K, dK = dS^T Q (2.5x the
+    forward's two for equal head dims)."""
+    pairs = sum(visible_pairs(sq, sk, w.causal, w.window_left, w.window_right) for sq, sk in seq_lengths(w))
+    return 2.0 * (3 * w.head_dim_qk + 2 * w.head_dim_v) * pairs * w.num_heads_q
+
+
 # ------------------------------------------------------------- ncu traffic ----
 def kernel_source_hash(files=None) -> str:
     """sha256 over CUDA sources (a changed kernel invalidates old counters):
@@ -243,6 +255,16 @@ class Runner:
             self.lpart = torch.empty((self.ns,) + tuple(lshape), dtype=torch.float32, device=dev)
         self.work = decode_bytes(w) if self.decode else flops(w)
         self.launches_per_step = 2 if (self.decode or w.varlen) else 1
+        self.backward = is_backward(name)
+        if self.backward:
+            # the forward's O and LSE are inputs of the backward: made once, untimed
+            self.step()
+            self.do = up(inputs.grad_out(w))
+            self.dq, self.dk, self.dv = (torch.empty_like(t) for t in (self.q, self.k, self.v))
+            self.bws_bytes = fa.fa_bwd_workspace_size(self.args)
+            self.bws = torch.empty(max(self.bws_bytes, 256), dtype=torch.uint8, device=dev)
+            self.work = backward_flops(w)
+            self.launches_per_step = 3   # preprocess, dQ, dK/dV
 
     def stream_ptr(self):
         import ctypes
@@ -253,6 +275,14 @@ class Runner:
         rc = self.fa.lib().fa_fwd(ctypes.byref(self.args), self.ws.data_ptr(), self.ws_bytes, self.stream_ptr())
         if rc != 0:
             raise RuntimeError(f"fa_fwd: {self.fa.fa_status_string(rc)}")
+
+    def step_bwd(self):
+        import ctypes
+        rc = self.fa.lib().fa_bwd(ctypes.byref(self.args), self.do.data_ptr(), self.dq.data_ptr(),
+                                  self.dk.data_ptr(), self.dv.data_ptr(), self.bws.data_ptr(), self.bws_bytes,
+                                  self.stream_ptr())
+        if rc != 0:
+            raise RuntimeError(f"fa_bwd: {self.fa.fa_status_string(rc)}")
 
     def step_split(self):
         """decode as its two kernels, returning the events around the split-KV kernel."""
@@ -288,6 +318,8 @@ def time_steps(r: Runner, steps: int, warmup: int, flush):
     for _ in range(warmup):
         if r.decode:
             r.step_split()
+        elif r.backward:
+            r.step_bwd()
         else:
             r.step()
     torch.cuda.synchronize()
@@ -301,6 +333,8 @@ def time_steps(r: Runner, steps: int, warmup: int, flush):
         a.record()
         if r.decode:
             e0, e1 = r.step_split()
+        elif r.backward:
+            r.step_bwd()
         else:
             r.step()
         b.record()
@@ -483,7 +517,8 @@ def main():
         torch.cuda.synchronize()
 
     names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode",
-                                                                 "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa")
+                                                                 "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
+                                                                 "causal_bwd", "dense_bwd")
                                                       if n != args.workload])
     results = {}
     clocks = None
@@ -509,6 +544,8 @@ def main():
                     "unit": "TFLOP/s"}
         roof["frac"] = roof["achieved"] / roof["peak"]
         roof["peak_source"] = peaks["source"] + (" (HBM copy)" if r.decode else " (dense bf16 burst)")
+        if r.backward:
+            roof["scope"] = "the whole fa_bwd call (preprocess, dQ and dK/dV kernels)"
         roof["traffic"] = measured_traffic(n)
         res = {"value": value, "unit": unit_of(n), "ms_per_step": ms_step, "kernel_ms": kern_avg,
                "work_per_step": r.work, "roofline": roof, "launches_per_step": r.launches_per_step,

@@ -21,19 +21,22 @@
 //     memory, dV += P^T dO and dK += dS^T Q.
 //
 // Tensor memory (512 columns, one CTA per SM): S [0,128), dP [128,256),
-// accumulators from 256 (dQ; or dV then dK). The compute warps take each
-// 128-column score block in two 64-column halves; the bf16 result of half h
-// lands in columns [64h, 64h+32) of its own fp32 half, which that half has
-// already read, and the accumulating GEMM of half h runs while the warps work
-// on half h+1. Every GEMM has the operand forms of the forward kernel: SS with
-// two K-major 128B-swizzled tiles, and TS with the bf16 A operand in tensor
-// memory and an MN-major B tile.
+// accumulators from 256 (dQ; or dV then dK). Two warpgroups share each
+// 128 x 128 score block, warpgroup c taking columns [64c, 64c+64) for all 128
+// rows, in two phases: P from S (the dK/dV kernel writes P^T back in bf16),
+// then dS from dP and the P kept in registers, back in bf16. A bf16 result of
+// half c lands in columns [64c, 64c+32) of its own fp32 half, which only that
+// warpgroup reads. The MMA thread orders its GEMMs so that each phase of the
+// warps overlaps two GEMMs of the tensor pipe (see the issue orders below).
+// Every GEMM has the operand forms of the forward kernel: SS with two K-major
+// 128B-swizzled tiles, and TS with the bf16 A operand in tensor memory and an
+// MN-major B tile.
 //
-// Warps 0-3 compute (thread t owns row t of the tile, tensor-memory lane t),
-// warp 4 issues the TMA loads, warp 5 the MMAs (one thread). Every wait is
-// bounded; on a timeout the CTA raises its abort flag, records the failure in
-// the device status word, drains its copies and MMAs, frees tensor memory and
-// returns.
+// Warps 0-7 compute (thread t of a warpgroup owns row t of the tile, tensor-
+// memory lane t), warp 8 issues the TMA loads, warp 9 the MMAs (one thread).
+// Every wait is bounded; on a timeout the CTA raises its abort flag, records
+// the failure in the device status word, drains its copies and MMAs, frees
+// tensor memory and returns.
 #include <cuda_bf16.h>
 
 #include "fa_kernels.h"
@@ -59,8 +62,8 @@ struct BwdCfg {
   // at least half the SM's shared memory: one CTA (owning all 512 tensor-memory
   // columns) per SM
   static constexpr int SMEM = (SMEM_USED + 1024 < 120 * 1024) ? 120 * 1024 : SMEM_USED + 1024;
-  static constexpr int THREADS = 192;
-  static constexpr int TMA_WARP = 4, MMA_WARP = 5;
+  static constexpr int THREADS = 320;
+  static constexpr int TMA_WARP = 8, MMA_WARP = 9;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(256 + 2 * D <= 512, "tensor memory budget");
 };
@@ -69,8 +72,10 @@ struct BBars {
   uint64_t* res_full;   // resident pair landed
   uint64_t* str_full;   // [ST]
   uint64_t* str_empty;  // [ST]
-  uint64_t* s_full;     // [2] per 64-column half: S and dP of the half complete
-  uint64_t* ds_full;    // [2] per half: bf16 operand written (4 arrivals, one per compute warp)
+  uint64_t* s_full;     // S of the current job complete
+  uint64_t* dp_full;    // dP of the current job complete
+  uint64_t* p_done;     // [2] per column half: S read (and P^T written) by its warpgroup (4 arrivals)
+  uint64_t* ds_full;    // [2] per column half: dS written by its warpgroup (4 arrivals)
   uint64_t* acc_full;   // accumulators final
   uint64_t* drain;
 };
@@ -82,7 +87,9 @@ __device__ __forceinline__ BBars carve(uint8_t* smem) {
   B.res_full = b; b += 1;
   B.str_full = b; b += Cfg::ST;
   B.str_empty = b; b += Cfg::ST;
-  B.s_full = b; b += 2;
+  B.s_full = b; b += 1;
+  B.dp_full = b; b += 1;
+  B.p_done = b; b += 2;
   B.ds_full = b; b += 2;
   B.acc_full = b; b += 1;
   B.drain = b; b += 1;
@@ -96,8 +103,10 @@ __device__ __forceinline__ void init_bars(const BBars& B) {
     mbar_init(&B.str_full[i], 1);
     mbar_init(&B.str_empty[i], 1);
   }
+  mbar_init(B.s_full, 1);
+  mbar_init(B.dp_full, 1);
   for (int i = 0; i < 2; ++i) {
-    mbar_init(&B.s_full[i], 1);
+    mbar_init(&B.p_done[i], 4);
     mbar_init(&B.ds_full[i], 4);
   }
   mbar_init(B.acc_full, 1);
@@ -262,26 +271,42 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (warp == Cfg::MMA_WARP) {
     if (lane == 0 && has) {
+      // Issue order, block u:  S(0) dP(0) | [S(u) read] S(u+1) [dS(u)] dQ(u) dP(u+1) | ...
+      // so that dP(u) runs while the warps form P(u), S(u+1) while they form
+      // dS(u), and dQ(u) and dP(u+1) while they form P(u+1). dS(u) lives in
+      // dP's columns, which dP(u+1) only overwrites after dQ(u) has read them
+      // (the tensor pipe runs one thread's MMAs in order).
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
       constexpr uint32_t IDESC_DQ = idesc_bf16_f32(kB, D, false, true);
       const uint32_t q_base = smem_u32(smem + Cfg::OFF_RES), do_base = q_base + Cfg::T_BYTES;
-      bool ok = mbar_wait(B.res_full, 0, guard);
-      uint32_t u = 0;
-      for (int n = nhi - 1; ok && n >= nlo; --n, ++u) {
-        const int st = u % Cfg::ST;
-        const uint32_t kb = smem_u32(smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES), vb = kb + Cfg::T_BYTES;
-        if (!mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard)) { ok = false; break; }
-        issue_ss(tmem, q_base, kb, D, IDESC_S);          // S  = Q K^T
-        issue_ss(tmem + 128, do_base, vb, D, IDESC_S);   // dP = dO V^T
-        mma_commit(&B.s_full[0]);
-        mma_commit(&B.s_full[1]);
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&B.ds_full[hh], u & 1, guard)) { ok = false; break; }
+      const uint32_t nb = static_cast<uint32_t>(nhi - nlo);
+      auto kv = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * 2 * Cfg::T_BYTES); };
+      bool ok = mbar_wait(B.res_full, 0, guard) && mbar_wait(&B.str_full[0], 0, guard);
+      if (ok) {
+        issue_ss(tmem, q_base, kv(0), D, IDESC_S);                          // S  = Q K^T
+        mma_commit(B.s_full);
+        issue_ss(tmem + 128, do_base, kv(0) + Cfg::T_BYTES, D, IDESC_S);    // dP = dO V^T
+        mma_commit(B.dp_full);
+      }
+      for (uint32_t u = 0; ok && u < nb; ++u) {
+        if (!mbar_wait(&B.p_done[0], u & 1, guard) || !mbar_wait(&B.p_done[1], u & 1, guard)) { ok = false; break; }
+        if (u + 1 < nb) {
+          if (!mbar_wait(&B.str_full[(u + 1) % Cfg::ST], ((u + 1) / Cfg::ST) & 1, guard)) { ok = false; break; }
           tc_fence_after();
-          issue_ts_half(tmem + 256, tmem, kb, hh, IDESC_DQ, u > 0 || hh > 0);   // dQ += dS_h K_h
+          issue_ss(tmem, q_base, kv(u + 1), D, IDESC_S);
+          mma_commit(B.s_full);
+        }
+        for (int c = 0; c < 2; ++c) {
+          if (!mbar_wait(&B.ds_full[c], u & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+          issue_ts_half(tmem + 256, tmem + 128, kv(u), c, IDESC_DQ, u > 0 || c > 0);   // dQ += dS_c K_c
         }
         if (!ok) break;
-        mma_commit(&B.str_empty[st]);
+        mma_commit(&B.str_empty[u % Cfg::ST]);
+        if (u + 1 < nb) {
+          issue_ss(tmem + 128, do_base, kv(u + 1) + Cfg::T_BYTES, D, IDESC_S);
+          mma_commit(B.dp_full);
+        }
       }
       if (ok) mma_commit(B.acc_full);
       mma_commit(B.drain);
@@ -289,13 +314,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ================= compute warps: thread t <-> query row i0 + t =================
-    const int t = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ====== compute warps: warpgroup c takes key columns [64c, 64c+64) of every
+    // block; thread t of a warpgroup owns query row i0 + t (tensor-memory lane t)
+    const int c = warp >> 2;
+    const int t = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int i = i0 + t;
     const int64_t vrow = (int64_t(b) * p.hq + h) * p.sq_pad + i;
     __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(p.dq) + int64_t(b) * p.q_bs + int64_t(i) * p.q_rs +
-                        int64_t(h) * p.q_hs;
+                        int64_t(h) * p.q_hs + c * (D / 2);
     if (has) {
       const float nl2 = -p.lse2[vrow], dsum = p.dsum[vrow];
       bool ok = true;
@@ -305,47 +332,56 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         // every (row, key) of the block visible?  (uniform over the CTA)
         const bool full = (jb + kB <= p.seqlen_k) && (p.wr < 0 || jb + kB - 1 <= i0 + off + p.wr) &&
                           (p.wl < 0 || jb >= i0 + kB - 1 + off - p.wl);
-        // visible columns [c_lo, c_hi] of this row
-        const int c_lo = (p.wl >= 0) ? i + off - p.wl - jb : INT32_MIN / 2;
+        // visible columns [c_lo, c_hi] of this row, relative to this warpgroup's first column
+        const int c_lo = ((p.wl >= 0) ? i + off - p.wl - jb : INT32_MIN / 2) - 64 * c;
         int c_hi = p.seqlen_k - 1 - jb;
         if (p.wr >= 0) c_hi = min(c_hi, i + off + p.wr - jb);
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&B.s_full[hh], u & 1, guard)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t s[64], dp[64];
-          tmem_ld64(tmem + lane_off + hh * 64, s);
-          tmem_ld64(tmem + lane_off + 128 + hh * 64, dp);
-          uint32_t w[32];
+        c_hi -= 64 * c;
+        // P = exp2(S scale log2(e) - LSE log2(e)), masked
+        if (!mbar_wait(B.s_full, u & 1, guard)) { ok = false; break; }
+        tc_fence_after();
+        float pf[64];
+        {
+          uint32_t sv[64];
+          tmem_ld64(tmem + lane_off + 64 * c, sv);
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), p.scale_log2, nl2));
-            float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), p.scale_log2, nl2));
-            if (!full) {
-              const int cc = hh * 64 + c;
-              p0 = (cc < c_lo || cc > c_hi) ? 0.f : p0;
-              p1 = (cc + 1 < c_lo || cc + 1 > c_hi) ? 0.f : p1;
-            }
-            w[c >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[c]) - dsum), p1 * (__uint_as_float(dp[c + 1]) - dsum));
+          for (int e = 0; e < 64; ++e) {
+            const float x = ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, nl2));
+            pf[e] = (full || (e >= c_lo && e <= c_hi)) ? x : 0.f;
           }
-          tmem_st32(tmem + lane_off + hh * 64, w);   // dS_h over the half's first 32 columns
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&B.ds_full[hh]);
         }
-        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.p_done[c]);
+        // dS = P (dP - D), bf16, into the first 32 columns of this half of dP
+        if (!mbar_wait(B.dp_full, u & 1, guard)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t dp[64], w[32];
+          tmem_ld64(tmem + lane_off + 128 + 64 * c, dp);
+#pragma unroll
+          for (int e = 0; e < 64; e += 2)
+            w[e >> 1] = pack_bf16x2(pf[e] * (__uint_as_float(dp[e]) - dsum),
+                                    pf[e + 1] * (__uint_as_float(dp[e + 1]) - dsum));
+          tmem_st32(tmem + lane_off + 128 + 64 * c, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.ds_full[c]);
       }
       if (ok && mbar_wait(B.acc_full, 0, guard)) {
         tc_fence_after();
+        // warpgroup c writes dQ columns [c D/2, (c+1) D/2)
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int k = 0; k < D / 64; ++k) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + 256 + c * 32, o);
-          if (i < p.seqlen_q) store_row32(dq + c * 32, o, p.scale);
+          tmem_ld32(tmem + lane_off + 256 + c * (D / 2) + k * 32, o);
+          if (i < p.seqlen_q) store_row32(dq + k * 32, o, p.scale);
         }
       }
     } else if (i < p.seqlen_q) {
-      zero_row(dq, D);   // no visible key: dQ = 0
+      zero_row(dq, D / 2);   // no visible key: dQ = 0
     }
   }
 
@@ -432,27 +468,49 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (warp == Cfg::MMA_WARP) {
     if (lane == 0 && jobs > 0) {
+      // Issue order, job u:  S(0) dP(0) | [P(u)] dV(u) S(u+1) [dS(u)] dK(u) dP(u+1) | ...
+      // so that dP(u) runs while the warps form P(u), dV(u) and S(u+1) while
+      // they form dS(u), and dK(u) and dP(u+1) while they form P(u+1). P^T(u)
+      // and dS^T(u) live in S's and dP's columns, which S(u+1) and dP(u+1) only
+      // overwrite after dV(u) and dK(u) have read them (one thread's MMAs run
+      // in order).
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
       constexpr uint32_t IDESC_ACC = idesc_bf16_f32(kB, D, false, true);
       const uint32_t k_base = smem_u32(smem + Cfg::OFF_RES), v_base = k_base + Cfg::T_BYTES;
-      bool ok = mbar_wait(B.res_full, 0, guard);
-      for (uint32_t u = 0; ok && u < static_cast<uint32_t>(jobs); ++u) {
-        const int st = u % Cfg::ST;
-        const uint32_t qb = smem_u32(smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES), dob = qb + Cfg::T_BYTES;
-        if (!mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard)) { ok = false; break; }
-        issue_ss(tmem, k_base, qb, D, IDESC_S);           // S^T  = K Q^T
-        issue_ss(tmem + 128, v_base, dob, D, IDESC_S);    // dP^T = V dO^T
-        mma_commit(&B.s_full[0]);
-        mma_commit(&B.s_full[1]);
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&B.ds_full[hh], u & 1, guard)) { ok = false; break; }
+      const uint32_t nj = static_cast<uint32_t>(jobs);
+      auto qs = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * 2 * Cfg::T_BYTES); };
+      bool ok = mbar_wait(B.res_full, 0, guard) && mbar_wait(&B.str_full[0], 0, guard);
+      if (ok) {
+        issue_ss(tmem, k_base, qs(0), D, IDESC_S);                         // S^T  = K Q^T
+        mma_commit(B.s_full);
+        issue_ss(tmem + 128, v_base, qs(0) + Cfg::T_BYTES, D, IDESC_S);    // dP^T = V dO^T
+        mma_commit(B.dp_full);
+      }
+      for (uint32_t u = 0; ok && u < nj; ++u) {
+        const uint32_t qb = qs(u), dob = qb + Cfg::T_BYTES;
+        const bool acc = u > 0;
+        for (int c = 0; c < 2; ++c) {
+          if (!mbar_wait(&B.p_done[c], u & 1, guard)) { ok = false; break; }
           tc_fence_after();
-          const bool acc = u > 0 || hh > 0;
-          issue_ts_half(tmem + 256, tmem, dob, hh, IDESC_ACC, acc);            // dV += P^T_h dO_h
-          issue_ts_half(tmem + 256 + D, tmem + 128, qb, hh, IDESC_ACC, acc);   // dK += dS^T_h Q_h
+          issue_ts_half(tmem + 256, tmem, dob, c, IDESC_ACC, acc || c > 0);   // dV += P^T_c dO_c
         }
         if (!ok) break;
-        mma_commit(&B.str_empty[st]);
+        if (u + 1 < nj) {
+          if (!mbar_wait(&B.str_full[(u + 1) % Cfg::ST], ((u + 1) / Cfg::ST) & 1, guard)) { ok = false; break; }
+          issue_ss(tmem, k_base, qs(u + 1), D, IDESC_S);
+          mma_commit(B.s_full);
+        }
+        for (int c = 0; c < 2; ++c) {
+          if (!mbar_wait(&B.ds_full[c], u & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+          issue_ts_half(tmem + 256 + D, tmem + 128, qb, c, IDESC_ACC, acc || c > 0);   // dK += dS^T_c Q_c
+        }
+        if (!ok) break;
+        mma_commit(&B.str_empty[u % Cfg::ST]);
+        if (u + 1 < nj) {
+          issue_ss(tmem + 128, v_base, qs(u + 1) + Cfg::T_BYTES, D, IDESC_S);
+          mma_commit(B.dp_full);
+        }
       }
       if (ok) mma_commit(B.acc_full);
       mma_commit(B.drain);
@@ -460,9 +518,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ================= compute warps: thread t <-> key row j0 + t =================
-    const int t = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ====== compute warps: warpgroup c takes query columns [64c, 64c+64) of
+    // every job; thread t of a warpgroup owns key row j0 + t (tensor-memory lane t)
+    const int c = warp >> 2;
+    const int t = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int j = j0 + t;
     __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk) + int64_t(b) * p.k_bs + int64_t(j) * p.k_rs +
                         int64_t(g) * p.k_hs;
@@ -476,69 +536,75 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int ib = m * kB;
         const bool full = (j0 + kB <= p.seqlen_k) && (ib + kB <= p.seqlen_q) &&
                           (p.wr < 0 || j0 + kB - 1 <= ib + off + p.wr) && (p.wl < 0 || j0 >= ib + kB - 1 + off - p.wl);
-        // visible query columns [c_lo, c_hi] of this key row
-        const int c_lo = (p.wr >= 0) ? j - off - p.wr - ib : INT32_MIN / 2;
+        // visible query columns [c_lo, c_hi] of this key row, relative to this warpgroup's first column
+        const int c_lo = ((p.wr >= 0) ? j - off - p.wr - ib : INT32_MIN / 2) - 64 * c;
         int c_hi = p.seqlen_q - 1 - ib;
         if (p.wl >= 0) c_hi = min(c_hi, j - off + p.wl - ib);
-        if (j >= p.seqlen_k) c_hi = -1;
+        if (j >= p.seqlen_k) c_hi = -1 + 64 * c;
+        c_hi -= 64 * c;
         // the stage's lse2 / D landed with its tiles
         if (!mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard)) { ok = false; break; }
-        const float* vec = reinterpret_cast<const float*>(smem + Cfg::OFF_VEC + st * 1024);
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&B.s_full[hh], u & 1, guard)) { ok = false; break; }
-          tc_fence_after();
-          uint32_t s[64], dp[64];
-          tmem_ld64(tmem + lane_off + hh * 64, s);
-          tmem_ld64(tmem + lane_off + 128 + hh * 64, dp);
-          uint32_t pw[32], dw[32];
+        const float* vl = reinterpret_cast<const float*>(smem + Cfg::OFF_VEC + st * 1024) + 64 * c;
+        const float* vd = vl + 128;
+        // P^T = exp2(S^T scale log2(e) - LSE log2(e)), masked; bf16 into the half's first 32 columns
+        if (!mbar_wait(B.s_full, u & 1, guard)) { ok = false; break; }
+        tc_fence_after();
+        float pf[64];
+        {
+          uint32_t sv[64], pw[32];
+          tmem_ld64(tmem + lane_off + 64 * c, sv);
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(vec + hh * 64 + c);
-            const float4 d4 = *reinterpret_cast<const float4*>(vec + 128 + hh * 64 + c);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pr[4], dsr[4];
+          for (int e = 0; e < 64; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(vl + e);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float pe = ex2_approx(fmaf(__uint_as_float(s[c + e]), p.scale_log2, -lv[e]));
-              if (!full) {
-                const int cc = hh * 64 + c + e;
-                pe = (cc < c_lo || cc > c_hi) ? 0.f : pe;
-              }
-              pr[e] = pe;
-              dsr[e] = pe * (__uint_as_float(dp[c + e]) - dv4[e]);
+            for (int q = 0; q < 4; ++q) {
+              const float x = ex2_approx(fmaf(__uint_as_float(sv[e + q]), p.scale_log2, -lv[q]));
+              pf[e + q] = (full || (e + q >= c_lo && e + q <= c_hi)) ? x : 0.f;
             }
-            pw[c >> 1] = pack_bf16x2(pr[0], pr[1]);
-            pw[(c >> 1) + 1] = pack_bf16x2(pr[2], pr[3]);
-            dw[c >> 1] = pack_bf16x2(dsr[0], dsr[1]);
-            dw[(c >> 1) + 1] = pack_bf16x2(dsr[2], dsr[3]);
+            pw[e >> 1] = pack_bf16x2(pf[e], pf[e + 1]);
+            pw[(e >> 1) + 1] = pack_bf16x2(pf[e + 2], pf[e + 3]);
           }
-          tmem_st32(tmem + lane_off + hh * 64, pw);         // P^T_h
-          tmem_st32(tmem + lane_off + 128 + hh * 64, dw);   // dS^T_h
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&B.ds_full[hh]);
+          tmem_st32(tmem + lane_off + 64 * c, pw);
         }
-        if (!ok) break;
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.p_done[c]);
+        // dS^T = P^T (dP^T - D), bf16 into the first 32 columns of this half of dP^T
+        if (!mbar_wait(B.dp_full, u & 1, guard)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t dp[64], dw[32];
+          tmem_ld64(tmem + lane_off + 128 + 64 * c, dp);
+#pragma unroll
+          for (int e = 0; e < 64; e += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(vd + e);
+            dw[e >> 1] = pack_bf16x2(pf[e] * (__uint_as_float(dp[e]) - d4.x), pf[e + 1] * (__uint_as_float(dp[e + 1]) - d4.y));
+            dw[(e >> 1) + 1] = pack_bf16x2(pf[e + 2] * (__uint_as_float(dp[e + 2]) - d4.z),
+                                           pf[e + 3] * (__uint_as_float(dp[e + 3]) - d4.w));
+          }
+          tmem_st32(tmem + lane_off + 128 + 64 * c, dw);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.ds_full[c]);
       }
       if (ok && mbar_wait(B.acc_full, 0, guard)) {
         tc_fence_after();
+        // warpgroup 0 writes dV, warpgroup 1 dK (times the softmax scale)
+        __nv_bfloat16* dst = c == 0 ? dv : dk;
+        const float f = c == 0 ? 1.f : p.scale;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int k = 0; k < D / 32; ++k) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + 256 + c * 32, o);
-          if (j < p.seqlen_k) store_row32(dv + c * 32, o, 1.f);
-        }
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + 256 + D + c * 32, o);
-          if (j < p.seqlen_k) store_row32(dk + c * 32, o, p.scale);
+          tmem_ld32(tmem + lane_off + 256 + c * D + k * 32, o);
+          if (j < p.seqlen_k) store_row32(dst + k * 32, o, f);
         }
       }
     } else if (j < p.seqlen_k) {
-      zero_row(dv, D);   // no query sees these keys
-      zero_row(dk, D);
+      zero_row(c == 0 ? dv : dk, D);   // no query sees these keys
     }
   }
 

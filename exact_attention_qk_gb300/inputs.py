@@ -32,6 +32,11 @@ passages of the FlashAttention pages):
   chunk_gqa     chunked prefill: 8 sequences of 128 new rows against 8192 keys,
                 Hq=32 Hkv=4 D=128, causal (the pack-GQA prefill case)
   decode_*_small  the first 16 sequences of a decode workload (profiling cases)
+
+Backward workloads (dQ, dK, dV given dO; dO is N(0,1) bf16 from its own stream):
+
+  causal_bwd    the causal prefill shape (B=2 Hq=32 Hkv=4 S=4096 D=128)
+  dense_bwd     the same shape without a mask
 """
 from __future__ import annotations
 
@@ -297,6 +302,9 @@ def workload(name: str) -> Workload:
         return fp8_batched("decode_fp8_small", 5, 16, 1, 16384, 32, 8, 128, "e4m3", seqused_k=decode_seqused()[:16])
     if name == "decode_paged_small":
         return to_paged(workload("decode_small"), 128)
+    if name in ("causal_bwd", "dense_bwd"):
+        # the backward of the causal prefill shape (same q, k, v draws), and its unmasked twin
+        return batched(name, 2, 2, 4096, 4096, 32, 4, 128, 128, causal=(name == "causal_bwd"))
     if name == "decode_small":
         # the decode shape with 16 sequences (about 1 GB of cache): a profiling case
         return batched("decode_small", 5, 16, 1, 16384, 32, 8, 128, 128, seqused_k=decode_seqused()[:16])
@@ -305,4 +313,4 @@ def workload(name: str) -> Workload:
 
 WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode", "decode_small",
              "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
-             "decode_fp8_small", "decode_paged_small")
+             "decode_fp8_small", "decode_paged_small", "causal_bwd", "dense_bwd")
