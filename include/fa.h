@@ -232,6 +232,11 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
  * workspace: at least fa_bwd_workspace_size(args) bytes, 256-byte aligned
  *   (fp32 LSE * log2(e) and D for every padded query row). The call is
  *   deterministic: no atomics, the same inputs give the same bits.
+ * The dK/dV kernel runs on a second stream of the library's (one per device,
+ * created by the device's first fa_bwd call, highest priority), forked from
+ * and joined back into `stream` with events: to the caller the work is
+ * ordered on `stream` alone, and a captured `stream` captures both. Make a
+ * device's first fa_bwd call outside stream capture.
  */
 int fa_bwd(const fa_fwd_args* args, const void* dout, void* dq, void* dk, void* dv, void* workspace,
            size_t workspace_bytes, void* stream);
