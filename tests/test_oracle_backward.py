@@ -87,3 +87,42 @@ def test_rows_without_keys_have_zero_gradients():
     dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=True)
     assert np.abs(dq[0, :3]).max() == 0.0
     assert np.isfinite(dk).all() and np.isfinite(dv).all()
+
+
+def test_zero_output_gradient_gives_zero_gradients():
+    rng = np.random.default_rng(7)
+    q, k, v = (rng.standard_normal((1, 5, 2, 4)) for _ in range(3))
+    grads = oracle.attention_backward(q, k, v, np.zeros((1, 5, 2, 4)), causal=True)
+    assert all(np.abs(g).max() == 0.0 for g in grads)
+
+
+def test_rows_seeing_one_key():
+    # window [i, i] (causal, window_left 0): P is the identity, so O = V,
+    # dV = dO, and dS = P (dP - D) = dO.v - dO.v = 0 gives dQ = dK = 0
+    rng = np.random.default_rng(8)
+    q, k, v, do = (rng.standard_normal((1, 6, 1, 4)) for _ in range(4))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=True, window_left=0)
+    np.testing.assert_allclose(dv, do, rtol=0, atol=1e-15)
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+
+
+def test_constant_values_give_zero_query_and_key_gradients():
+    # every v_j = c: O = c whatever P is, so the loss does not depend on q or k
+    rng = np.random.default_rng(9)
+    q, k, do = (rng.standard_normal((2, 5, 2, 4)) for _ in range(3))
+    v = np.broadcast_to(rng.standard_normal(4), (2, 5, 2, 4)).copy()
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=True)
+    assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
+    # dV_j = sum_i P_ij dO_i still holds; its sum over keys is the sum of dO over rows
+    np.testing.assert_allclose(dv.sum(axis=1), do.sum(axis=1), rtol=0, atol=1e-12)
+
+
+def test_gqa_equals_explicit_repetition():
+    rng = np.random.default_rng(10)
+    q, do = (rng.standard_normal((1, 5, 4, 3)) for _ in range(2))
+    k, v = (rng.standard_normal((1, 6, 2, 3)) for _ in range(2))
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=True)
+    rq, rk, rv = oracle.attention_backward(q, np.repeat(k, 2, axis=2), np.repeat(v, 2, axis=2), do, causal=True)
+    np.testing.assert_allclose(dq, rq, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dk, rk.reshape(1, 6, 2, 2, 3).sum(axis=3), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dv, rv.reshape(1, 6, 2, 2, 3).sum(axis=3), rtol=0, atol=1e-14)
