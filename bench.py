@@ -348,9 +348,12 @@ def time_steps(r: Runner, steps: int, warmup: int, flush):
 
 
 def time_e2e(r: Runner, steps: int, warmup: int):
-    """Public API end to end: pinned host inputs -> H2D, fa_fwd, O and LSE -> host."""
+    """Public API end to end: pinned host inputs -> H2D, fa_fwd, O and LSE -> host
+    (for a backward workload: q, k, v, O, LSE and dO -> H2D, fa_bwd, dQ, dK, dV -> host)."""
     torch, fa = r.torch, r.fa
     w = r.w
+    if r.backward:
+        return time_e2e_bwd(r, steps, warmup)
     def host(a):
         a = np.ascontiguousarray(a)
         return torch.from_numpy(a if a.dtype == np.uint8 else a.view(np.int16)).pin_memory()
@@ -379,6 +382,33 @@ def time_e2e(r: Runner, steps: int, warmup: int):
         fa.fa_fwd(r.q, r.k, r.v, out=r.out, lse=r.lse, workspace=r.ws, **r.kw, **r.extra)
         ho.copy_(r.out.view(torch.int16), non_blocking=True)
         hl.copy_(r.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def time_e2e_bwd(r: Runner, steps: int, warmup: int):
+    torch, fa = r.torch, r.fa
+    dev_in = [r.q, r.k, r.v, r.out, r.lse, r.do]
+    host_in = [(t.view(torch.int16) if t.dtype == torch.bfloat16 else t).cpu().pin_memory() for t in dev_in]
+    host_out = [torch.empty(t.shape, dtype=torch.int16).pin_memory() for t in (r.dq, r.dk, r.dv)]
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = sum(h.numel() * 2 for h in host_out)
+
+    def one():
+        for h, d in zip(host_in, dev_in):
+            (d.view(torch.int16) if d.dtype == torch.bfloat16 else d).copy_(h, non_blocking=True)
+        fa.fa_bwd(r.q, r.k, r.v, r.out, r.lse, r.do, dq=r.dq, dk=r.dk, dv=r.dv, workspace=r.bws, **r.kw)
+        for h, d in zip(host_out, (r.dq, r.dk, r.dv)):
+            h.copy_(d.view(torch.int16), non_blocking=True)
 
     for _ in range(warmup):
         one()
@@ -436,11 +466,20 @@ def oracle_sample(w, budget_s: float, max_pairs=None):
             k = kk[bb:bb + 1, :s.sk, h // r:h // r + 1]
             v = vv[bb:bb + 1, :s.sk, h // r:h // r + 1]
         t0 = time.perf_counter()
-        oracle.attention_forward(q, k, v, scale=w.softmax_scale, causal=w.causal, window_left=w.window_left,
-                                 window_right=w.window_right)
+        if is_backward(w.name):
+            do = inputs.grad_out(dataclasses.replace(w, q=q, batch=1, num_heads_q=1))
+            t0 = time.perf_counter()
+            oracle.attention_backward(q, k, v, do, scale=w.softmax_scale, causal=w.causal,
+                                      window_left=w.window_left, window_right=w.window_right)
+        else:
+            oracle.attention_forward(q, k, v, scale=w.softmax_scale, causal=w.causal, window_left=w.window_left,
+                                     window_right=w.window_right)
         t_total += time.perf_counter() - t0
         pairs += 1
-        if is_decode(w.name):
+        if is_backward(w.name):
+            done_work += 2.0 * (3 * w.head_dim_qk + 2 * w.head_dim_v) * visible_pairs(
+                s.sq, s.sk, w.causal, w.window_left, w.window_right)
+        elif is_decode(w.name):
             es = 2 if w.kv_format == "bf16" else 1
             done_work += s.sq * w.head_dim_qk * 2 + s.sk * (w.head_dim_qk + w.head_dim_v) * es / r + \
                 s.sq * (w.head_dim_v * 2 + 4)
@@ -518,7 +557,7 @@ def main():
 
     names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode",
                                                                  "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
-                                                                 "causal_bwd", "dense_bwd")
+                                                                 "chunk_single", "causal_bwd", "dense_bwd")
                                                       if n != args.workload])
     results = {}
     clocks = None
@@ -569,8 +608,7 @@ def main():
         cpu = {"value": rate(work, secs * 1e3, args.workload), "unit": unit_of(args.workload),
                "cores": os.cpu_count(), "kind": "oracle", "sample": desc, "seconds": secs}
     if rank == 0:
-        metric = ("attn fwd TFLOP/s (prefill, causal GQA B=2 Hq=32 Hkv=4 S=4096 D=128)"
-                  if not is_decode(args.workload) else "split-KV decode KV GB/s")
+        metric = metric_name(args.workload)
         line = {
             "metric": metric,
             "value": p["value"],
@@ -597,6 +635,14 @@ def main():
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def metric_name(name):
+    if is_decode(name):
+        return "split-KV decode KV GB/s"
+    if is_backward(name):
+        return "attn bwd TFLOP/s (dQ, dK, dV; B=2 Hq=32 Hkv=4 S=4096 D=128)"
+    return "attn fwd TFLOP/s (prefill, causal GQA B=2 Hq=32 Hkv=4 S=4096 D=128)"
 
 
 def workload_desc(w):
@@ -630,8 +676,7 @@ def run_reference(args):
     value = rate(works, secs * 1e3, args.workload)
     line = {
         "impl": "reference",
-        "metric": ("attn fwd TFLOP/s (prefill, causal GQA B=2 Hq=32 Hkv=4 S=4096 D=128)"
-                   if not is_decode(args.workload) else "split-KV decode KV GB/s"),
+        "metric": metric_name(args.workload),
         "value": value,
         "unit": unit_of(args.workload),
         "n_gpus": 1,

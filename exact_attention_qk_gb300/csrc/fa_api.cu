@@ -200,9 +200,38 @@ bool decode_shaped(const fa_fwd_args* a, const Resolved& r) {
 // divides 128 and no sequence has more than 128 query rows.
 bool pack_gqa(const Resolved& r) { return r.r > 1 && 128 % r.r == 0 && r.rows_q <= 128; }
 
+// Prefill grid that would leave more than half of the SMs idle (few sequences
+// x heads x query tiles against long keys): its keys are split so that the
+// work items (tile, split) fill the GPU, at least 4 key blocks per split and
+// no split empty for every tile. The combine merges the fp32 partials.
+int prefill_splits(const fa_fwd_args* a, const Resolved& r, int num_sms) {
+  if (kv_special(a) || decode_shaped(a, r) || r.kmax <= 0) return 1;
+  if (num_sms <= 0) num_sms = device_sms();
+  if (num_sms <= 0) return 1;
+  const int rpt = prefill_rows_per_tile(a->head_dim_qk, a->head_dim_v);
+  const bool pack = pack_gqa(r);
+  const long long rows = static_cast<long long>(r.rows_q) * (pack ? r.r : 1);
+  const long long tiles = static_cast<long long>(a->batch) * (pack ? a->num_heads_kv : a->num_heads_q) *
+                          ((rows + rpt - 1) / rpt);
+  if (tiles <= 0 || 2 * tiles > num_sms) return 1;
+  const int nkb = (r.kmax + 127) / 128;
+  long long ns = num_sms / tiles;
+  if (ns > nkb / 4) ns = nkb / 4;
+  if (ns > 32) ns = 32;
+  if (ns < 2) return 1;
+  const int per = static_cast<int>((nkb + ns - 1) / ns);
+  return (nkb + per - 1) / per;
+}
+
+// keys per split of the prefill kernel: whole 128-key blocks
+int prefill_split_len(int kmax, int ns) {
+  const int nkb = (kmax + 127) / 128;
+  return ((nkb + ns - 1) / ns) * 128;
+}
+
 int resolve_splits(const fa_fwd_args* a, const Resolved& r, int num_sms) {
   if (a->num_splits > 0) return a->num_splits;
-  if (!decode_shaped(a, r) || r.kmax <= 0) return 1;
+  if (!decode_shaped(a, r) || r.kmax <= 0) return prefill_splits(a, r, num_sms);
   if (num_sms <= 0) num_sms = device_sms();
   constexpr int kTarget = 2048;
   int ns = (r.kmax + kTarget - 1) / kTarget;
@@ -233,7 +262,7 @@ struct WsLayout {
 WsLayout ws_layout(const fa_fwd_args* a, const Resolved& r, int ns) {
   WsLayout w{};
   size_t off = 0;
-  const bool prefill = ns <= 1 && !decode_shaped(a, r) && !kv_special(a);
+  const bool prefill = !decode_shaped(a, r) && !kv_special(a);
   if (prefill && r.varlen) {
     w.prefix_off = off;
     w.prefix_bytes = align256(sizeof(int) * (static_cast<size_t>(a->batch) + 1));
@@ -331,10 +360,18 @@ int run_decode(const fa_fwd_args* a, const Resolved& r, int ns, float* opart, fl
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-int run_prefill(const fa_fwd_args* a, const Resolved& r, void* ws, const WsLayout& w, cudaStream_t st) {
+int run_prefill(const fa_fwd_args* a, const Resolved& r, void* ws, const WsLayout& w, cudaStream_t st,
+                int ns = 1, float* opart = nullptr, float* lpart = nullptr) {
   FwdParams p;
   fill_common(&p, a, r);
   if (!p.status) return FA_ERR_CUDA;
+  if (ns > 1) {   // key splits into fp32 partials (the combine follows)
+    p.num_splits = ns;
+    p.split_len = prefill_split_len(r.kmax, ns);
+    p.write_partial = 1;
+    p.out_partial = opart;
+    p.lse_partial = lpart;
+  }
   const int rpt = prefill_rows_per_tile(a->head_dim_qk, a->head_dim_v);
   // Pack-GQA for short query sequences: with at most 128 query rows a head's
   // tile would be mostly empty and each K/V block would be read once per head
@@ -488,7 +525,10 @@ int fa_fwd(const fa_fwd_args* a, void* workspace, size_t workspace_bytes, void* 
   if (ns > 1) {
     float* opart = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.opart_off);
     float* lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lpart_off);
-    rc = run_decode(a, r, ns, opart, lpart, st);
+    // decode shapes and fp8 caches split on the decode kernel, prefill shapes
+    // on the prefill kernel (whole 128-key blocks per split)
+    rc = (decode_shaped(a, r) || kv_special(a)) ? run_decode(a, r, ns, opart, lpart, st)
+                                                : run_prefill(a, r, workspace, w, st, ns, opart, lpart);
     if (rc != FA_OK) return rc;
     return fa_combine(opart, lpart, ns, a->batch, r.varlen ? 0 : a->seqlen_q, a->num_heads_q, a->head_dim_v,
                       a->cu_seqlens_q, r.varlen ? a->total_q : 0, a->out, a->o_batch_stride, a->o_row_stride,
@@ -557,7 +597,8 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* a, void* stream) {
   if (no_work(a, r)) return FA_OK;
   rc = check_tensors(a, true);
   if (rc != FA_OK) return rc;
-  const int ns = resolve_splits(a, r, 0);
+  // the decode kernel for every shape here (prefill shapes are not split)
+  const int ns = (a->num_splits > 0 || decode_shaped(a, r)) ? resolve_splits(a, r, 0) : 1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (ns <= 1) return run_decode(a, r, 1, nullptr, nullptr, st);
   const size_t rows = r.varlen ? static_cast<size_t>(a->total_q)

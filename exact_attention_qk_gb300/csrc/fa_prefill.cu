@@ -86,6 +86,7 @@ struct PrefillCfg {
 // K/V block once for r heads. Otherwise tile rows are query rows of head h.
 struct Tile {
   int b, h, g, mb;      // h: q head (unpacked) or the KV head (packed)
+  int split;            // SPLIT instances: the key split this tile covers
   int q_row0, k_row0;   // first row of the sequence in q's / k's row axis
   int sq, sk;
   int rows;             // tile rows of the sequence: sq, or sq * r packed
@@ -106,8 +107,14 @@ __device__ __forceinline__ int tile_of(int k) {
   return k * g + ((k & 1) ? g - 1 - c : c);
 }
 
-template <int ROWS_PER_TILE, bool PACK>
+template <int ROWS_PER_TILE, bool PACK, bool SPLIT>
 __device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
+  // SPLIT instances: consecutive work items are the key splits of one tile
+  T.split = 0;
+  if constexpr (SPLIT) {
+    T.split = t % p.num_splits;
+    t /= p.num_splits;
+  }
   if (p.cu_seqlens_q == nullptr) {
     if (t >= p.num_tiles) return false;
     const int nh = PACK ? p.hkv : p.hq;
@@ -144,7 +151,7 @@ __device__ __forceinline__ bool fetch_tile(const FwdParams& p, int t, Tile& T) {
   return true;
 }
 
-template <bool PACK>
+template <bool PACK, bool SPLIT>
 __device__ __forceinline__ Range stage_range(const FwdParams& p, const Tile& T, int r0) {
   Range R;
   R.r0 = r0;
@@ -166,6 +173,10 @@ __device__ __forceinline__ Range stage_range(const FwdParams& p, const Tile& T, 
   int klo = 0, khi = T.sk;
   if (p.wl >= 0) klo = max(klo, R.i0 + off - p.wl);
   if (p.wr >= 0) khi = min(khi, ilast + off + p.wr + 1);
+  if constexpr (SPLIT) {   // split s covers keys [s L, (s+1) L), L a multiple of kBN
+    klo = max(klo, T.split * p.split_len);
+    khi = min(khi, (T.split + 1) * p.split_len);
+  }
   if (khi > klo) {
     R.nlo = klo / kBN;
     R.nhi = (khi + kBN - 1) / kBN;
@@ -264,7 +275,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-template <int DK, int DV, bool TAIL, bool PACK>
+template <int DK, int DV, bool TAIL, bool PACK, bool SPLIT>
 __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                    const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
@@ -342,12 +353,12 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       };
       for (int k = 0; ok; ++k) {
         Tile T;
-        if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK>(p, tile_of(k), T)) break;
+        if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK, SPLIT>(p, tile_of(k), T)) break;
         Range R[NQ];
         int nlo = INT32_MAX, nhi = INT32_MIN;
 #pragma unroll
         for (int s = 0; s < NQ; ++s) {
-          R[s] = stage_range<PACK>(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
+          R[s] = stage_range<PACK, SPLIT>(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
           if (has_work(R[s])) {
             nlo = min(nlo, R[s].nlo);
             nhi = max(nhi, R[s].nhi);
@@ -489,12 +500,12 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       bool ok = true;
       for (int k = 0; ok; ++k) {
         Tile T;
-        if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK>(p, tile_of(k), T)) break;
+        if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK, SPLIT>(p, tile_of(k), T)) break;
         Range R[NQ];
         int nlo = INT32_MAX, nhi = INT32_MIN;
 #pragma unroll
         for (int s = 0; s < NQ; ++s) {
-          R[s] = stage_range<PACK>(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
+          R[s] = stage_range<PACK, SPLIT>(p, T, T.mb * Cfg::ROWS_PER_TILE + s * kBM);
           if (has_work(R[s])) {
             nlo = min(nlo, R[s].nlo);
             nhi = max(nhi, R[s].nhi);
@@ -662,8 +673,8 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
     bool ok = true;
     for (int k = 0; ok; ++k) {
       Tile T;
-      if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK>(p, tile_of(k), T)) break;
-      const Range R = stage_range<PACK>(p, T, T.mb * Cfg::ROWS_PER_TILE + wg * kBM);
+      if (!fetch_tile<Cfg::ROWS_PER_TILE, PACK, SPLIT>(p, tile_of(k), T)) break;
+      const Range R = stage_range<PACK, SPLIT>(p, T, T.mb * Cfg::ROWS_PER_TILE + wg * kBM);
       if (!R.active) continue;
       const int trow = R.r0 + row_local;                       // tile row
       const bool valid = PACK ? trow < T.rows : trow < T.sq;
@@ -673,12 +684,31 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
                            int64_t(hh) * p.o_hs;
       const int64_t lrow = varlen ? int64_t(hh) * p.total_q + T.q_row0 + i
                                   : (int64_t(T.b) * p.hq + hh) * p.seqlen_q + i;
+      // SPLIT instances write fp32 partials: O_s (normalised by its own row
+      // sum) at [split][row][head][d] and LSE_s at [split][head-major row],
+      // the layouts the combine reads
+      float* opart = nullptr;
+      float* lpart = nullptr;
+      if constexpr (SPLIT) {
+        const int64_t rows_total = varlen ? int64_t(p.total_q) : int64_t(p.batch) * p.seqlen_q;
+        const int64_t ri = varlen ? int64_t(T.q_row0 + i) : int64_t(T.b) * p.seqlen_q + i;
+        opart = p.out_partial + ((int64_t(T.split) * rows_total + ri) * p.hq + hh) * DV;
+        lpart = p.lse_partial + (varlen ? (int64_t(T.split) * p.hq + hh) * p.total_q + T.q_row0 + i
+                                        : ((int64_t(T.split) * p.batch + T.b) * p.hq + hh) * p.seqlen_q + i);
+      }
       if (!has_work(R)) {
         if (valid) {
-          uint4 z = make_uint4(0, 0, 0, 0);
+          if constexpr (SPLIT) {
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < DV / 8; ++c) *reinterpret_cast<uint4*>(out + orow + c * 8) = z;
-          if (p.lse) p.lse[lrow] = -INFINITY;
+            for (int c = 0; c < DV / 4; ++c) reinterpret_cast<float4*>(opart)[c] = z;
+            *lpart = -INFINITY;
+          } else {
+            uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int c = 0; c < DV / 8; ++c) *reinterpret_cast<uint4*>(out + orow + c * 8) = z;
+            if (p.lse) p.lse[lrow] = -INFINITY;
+          }
         }
         continue;
       }
@@ -797,8 +827,22 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       // and packed groups of more than 32 heads, are written row by row.
       const int wrow0 = R.r0 + (warp & 3) * 32;   // first tile row of this warp
       bool staged = false;
-      if constexpr (Cfg::OSTAGE) staged = (!varlen || wrow0 + 32 <= T.rows) && (!PACK || p.r <= 32);
-      if (staged) {
+      if constexpr (Cfg::OSTAGE && !SPLIT) staged = (!varlen || wrow0 + 32 <= T.rows) && (!PACK || p.r <= 32);
+      if constexpr (SPLIT) {
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(opart + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
+                                   __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
+          }
+        }
+        if (valid) *lpart = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+      } else if (staged) {
         uint8_t* stg = smem + Cfg::OFF_OST + wg * kChunkBytes + (warp & 3) * (kChunkBytes / 4);
         const int cb = varlen ? 0 : T.b;
 #pragma unroll 1
@@ -845,7 +889,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           }
         }
       }
-      if (valid && p.lse) p.lse[lrow] = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+      if (!SPLIT && valid && p.lse) p.lse[lrow] = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.o_empty[o_idx]);
@@ -898,8 +942,11 @@ cudaError_t launch_prefill_t(const FwdParams& p, const CUtensorMap& mq, const CU
   using Cfg = PrefillCfg<DK, DV>;
   // the TAIL instances clear cache rows past seqused_k, the PACK ones fold q
   // heads into tile rows; the plain instance has neither
-  auto kern = p.seqused_k != nullptr ? (p.pack ? prefill_kernel<DK, DV, true, true> : prefill_kernel<DK, DV, true, false>)
-                                     : (p.pack ? prefill_kernel<DK, DV, false, true> : prefill_kernel<DK, DV, false, false>);
+  // (the SPLIT instances, for grids that would leave SMs idle, take the TAIL
+  // form whether or not the cache has unused slots)
+  auto kern = p.write_partial ? (p.pack ? prefill_kernel<DK, DV, true, true, true> : prefill_kernel<DK, DV, true, false, true>)
+            : p.seqused_k != nullptr ? (p.pack ? prefill_kernel<DK, DV, true, true, false> : prefill_kernel<DK, DV, true, false, false>)
+                                     : (p.pack ? prefill_kernel<DK, DV, false, true, false> : prefill_kernel<DK, DV, false, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   long long tiles;
@@ -909,6 +956,7 @@ cudaError_t launch_prefill_t(const FwdParams& p, const CUtensorMap& mq, const CU
     const long long rows = (long long)p.max_seqlen_q * (p.pack ? p.r : 1);
     tiles = (long long)p.batch * (p.pack ? p.hkv : p.hq) * ((rows + Cfg::ROWS_PER_TILE - 1) / Cfg::ROWS_PER_TILE);
   }
+  if (p.write_partial) tiles *= p.num_splits;
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
   if (grid <= 0) return cudaSuccess;
   kern<<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mo, p);

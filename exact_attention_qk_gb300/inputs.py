@@ -31,6 +31,8 @@ passages of the FlashAttention pages):
   causal_paged  the causal prefill workload with its K/V cache paged the same way
   chunk_gqa     chunked prefill: 8 sequences of 128 new rows against 8192 keys,
                 Hq=32 Hkv=4 D=128, causal (the pack-GQA prefill case)
+  chunk_single  one sequence's 256 new rows against 16384 keys, Hq=32 Hkv=8
+                D=128, causal (a grid of 32 tiles: the key-split prefill case)
   decode_*_small  the first 16 sequences of a decode workload (profiling cases)
 
 Backward workloads (dQ, dK, dV given dO; dO is N(0,1) bf16 from its own stream):
@@ -295,6 +297,10 @@ def workload(name: str) -> Workload:
         # chunked prefill: 128 new query rows of each of 8 sequences against an
         # 8192-key cache (bottom-right causal), GQA 32/4
         return batched("chunk_gqa", 6, 8, 128, 8192, 32, 4, 128, 128, causal=True)
+    if name == "chunk_single":
+        # one request's 256-row prefill chunk against a 16384-key cache, GQA
+        # 32/8: 32 packed tiles, a grid the library splits over the keys
+        return batched("chunk_single", 7, 1, 256, 16384, 32, 8, 128, 128, causal=True)
     if name == "causal_paged":
         # the causal prefill workload with its K/V cache in shuffled 128-key pages
         return to_paged(workload("causal"), 128)
@@ -313,4 +319,4 @@ def workload(name: str) -> Workload:
 
 WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode", "decode_small",
              "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
-             "decode_fp8_small", "decode_paged_small", "causal_bwd", "dense_bwd")
+             "decode_fp8_small", "decode_paged_small", "causal_bwd", "dense_bwd", "chunk_single")

@@ -77,6 +77,9 @@ enum {
  * softmax_scale <= 0 (or NaN) selects 1/sqrt(head_dim_qk).
  * num_splits: 0 = let the library choose (fa_num_splits), 1 = no split,
  *   > 1 = split-KV with that many splits followed by the combine (<= 256).
+ *   Decode shapes and fp8 caches split on the decode kernel at the
+ *   boundaries of fa_split_len; prefill shapes split on the prefill kernel at
+ *   whole 128-key blocks (ceil(key blocks / num_splits) blocks per split).
  * Supported (head_dim_qk, head_dim_v): (64,64), (128,128), (192,128), (256,256).
  * Element type: bf16 for q and out; k and v are bf16 unless kv_format says otherwise.
  *
@@ -250,7 +253,11 @@ size_t fa_workspace_size(const fa_fwd_args* args);
 /*
  * Split count fa_fwd uses when args->num_splits == 0. Decode-shaped problems
  * (seqlen_q * Hq/Hkv <= 16) are split into chunks of about 2048 keys so that
- * sequences of very different length spread over the SMs; others are not split.
+ * sequences of very different length spread over the SMs. Prefill shapes with
+ * a bf16 cache are split only when their grid of 256-row (128 for head dim
+ * 256) query tiles would fill at most half of the SMs: then into
+ * min(num_sms / tiles, key blocks / 4, 32) splits of whole 128-key blocks,
+ * run by the prefill kernel and merged by the combine. Others are not split.
  * num_sms <= 0 queries the current device.
  */
 int fa_num_splits(const fa_fwd_args* args, int num_sms);

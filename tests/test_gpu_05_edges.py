@@ -16,7 +16,7 @@ import gpu_util as gu  # noqa: E402
 
 @pytest.mark.parametrize("ns", [0, 4])
 def test_mqa_decode_32_heads_per_kv(ns):
-    # Hq/Hkv = 32 packed rows: the prefill path (ns=0) or decode in 8-row chunks (ns=4)
+    # Hq/Hkv = 32 packed rows: the prefill kernel, unsplit (ns=0) or in 4 key splits + combine
     w = inputs.batched("mqa", 101, 3, 1, 600, 32, 1, 128, 128,
                        seqused_k=np.array([600, 77, 300], np.int32))
     print(gu.check_workload(w, num_splits=ns))
@@ -63,8 +63,8 @@ def test_odd_heads_and_lengths():
 
 @pytest.mark.parametrize("ns", [2, 5])
 def test_split_kv_on_prefill_shape(ns):
-    # fa_fwd with an explicit split count on a prefill-shaped problem: decode
-    # kernel over 8-row chunks + combine (correct, not the fast path)
+    # fa_fwd with an explicit split count on a prefill-shaped problem: the
+    # prefill kernel over whole 128-key blocks per split, then the combine
     w = inputs.batched("pfsplit", 107, 1, 70, 700, 4, 2, 128, 128, causal=True, window_left=200)
     print(gu.check_workload(w, num_splits=ns))
 
