@@ -299,7 +299,8 @@ def workload(name: str) -> Workload:
         return batched("chunk_gqa", 6, 8, 128, 8192, 32, 4, 128, 128, causal=True)
     if name == "chunk_single":
         # one request's 256-row prefill chunk against a 16384-key cache, GQA
-        # 32/8: 32 packed tiles, a grid the library splits over the keys
+        # 32/8: 32 tiles of 256 rows (one per q head; 256 rows are too many to
+        # pack), a grid the library splits over the keys
         return batched("chunk_single", 7, 1, 256, 16384, 32, 8, 128, 128, causal=True)
     if name == "causal_paged":
         # the causal prefill workload with its K/V cache in shuffled 128-key pages
