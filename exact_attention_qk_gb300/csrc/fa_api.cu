@@ -441,14 +441,20 @@ bool no_work(const fa_fwd_args* a, const Resolved& r) {
 }
 
 struct BwdWs {
-  int sq_pad;
+  int sq_pad;         // batched: 128-row multiple of seqlen_q
+  int64_t ws_rows;    // varlen: rows per q head (each sequence's padded region at bwd_ws_row0)
   size_t lse2_off, dsum_off, total;
 };
 
 BwdWs bwd_ws(const fa_fwd_args* a) {
   BwdWs w{};
-  w.sq_pad = ((a->seqlen_q + 127) / 128) * 128;
-  const size_t n = static_cast<size_t>(a->batch) * a->num_heads_q * w.sq_pad;
+  const bool varlen = a->cu_seqlens_q != nullptr;
+  w.sq_pad = varlen ? 0 : ((a->seqlen_q + 127) / 128) * 128;
+  // (a multiple of 32, so that every head's region starts 16-byte aligned)
+  w.ws_rows = varlen ? ((static_cast<int64_t>(a->total_q) + 132 * static_cast<int64_t>(a->batch) + 4 + 31) / 32) * 32
+                     : 0;
+  const size_t n = varlen ? static_cast<size_t>(a->num_heads_q) * static_cast<size_t>(w.ws_rows)
+                          : static_cast<size_t>(a->batch) * a->num_heads_q * w.sq_pad;
   w.lse2_off = 0;
   w.dsum_off = align256(n * sizeof(float));
   w.total = w.dsum_off + align256(n * sizeof(float));
@@ -458,8 +464,7 @@ BwdWs bwd_ws(const fa_fwd_args* a) {
 int check_bwd_args(const fa_fwd_args* a, Resolved* r) {
   const int rc = check_args(a, r);
   if (rc != FA_OK) return rc;
-  if (r->varlen || a->seqused_k != nullptr || a->page_table != nullptr || a->kv_format != FA_KV_BF16)
-    return FA_ERR_UNSUPPORTED;
+  if (a->seqused_k != nullptr || a->page_table != nullptr || a->kv_format != FA_KV_BF16) return FA_ERR_UNSUPPORTED;
   if (!bwd_supported(a->head_dim_qk, a->head_dim_v)) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -628,11 +633,12 @@ int fa_bwd(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv,
   Resolved r;
   int rc = check_bwd_args(a, &r);
   if (rc != FA_OK) return rc;
-  if (a->batch == 0 || (a->seqlen_q == 0 && a->seqlen_k == 0)) return FA_OK;
   // With no query rows only dK = dV = 0 is written, and with no keys only
   // dQ = 0: the tensors of the empty side are never touched and may be NULL
   // (as an empty tensor's storage is).
-  const bool has_q = a->seqlen_q > 0, has_k = a->seqlen_k > 0;
+  const bool has_q = r.varlen ? a->total_q > 0 : a->seqlen_q > 0;
+  const bool has_k = r.varlen ? a->total_k > 0 : a->seqlen_k > 0;
+  if (a->batch == 0 || (!has_q && !has_k)) return FA_OK;
   fa_fwd_args c = *a;
   if (!has_q) {
     c.q = c.k;
@@ -671,9 +677,16 @@ int fa_bwd(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv,
   p.o_rs = a->o_row_stride;
   p.o_hs = a->o_head_stride;
   p.batch = a->batch;
-  p.seqlen_q = a->seqlen_q;
-  p.seqlen_k = a->seqlen_k;
+  p.seqlen_q = r.varlen ? a->max_seqlen_q : a->seqlen_q;
+  p.seqlen_k = r.varlen ? a->max_seqlen_k : a->seqlen_k;
   p.sq_pad = w.sq_pad;
+  p.cu_seqlens_q = a->cu_seqlens_q;
+  p.cu_seqlens_k = a->cu_seqlens_k;
+  p.total_q = r.varlen ? a->total_q : 0;
+  p.ws_rows = w.ws_rows;
+  if (r.varlen) {   // batch strides are ignored in the packed layout
+    p.q_bs = p.k_bs = p.v_bs = p.o_bs = 0;
+  }
   p.hq = a->num_heads_q;
   p.hkv = a->num_heads_kv;
   p.r = r.r;
@@ -684,19 +697,22 @@ int fa_bwd(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv,
   p.status = status_ptr();
   p.timeout_ns = g_timeout_ns.load();
   if (!p.status) return FA_ERR_CUDA;
-  const int64_t sq = a->seqlen_q, sk = a->seqlen_k;
+  // batched: (d, rows, heads, batch); packed varlen: (d, total rows, heads, 1)
+  // with the batch stride a stand-in (one batch)
+  const int64_t sq = r.varlen ? a->total_q : a->seqlen_q, sk = r.varlen ? a->total_k : a->seqlen_k;
+  const int64_t nb = r.varlen ? 1 : a->batch;
+  const int64_t qbs = r.varlen ? a->q_row_stride * sq : a->q_batch_stride;
+  const int64_t obs = r.varlen ? a->o_row_stride * sq : a->o_batch_stride;
+  const int64_t kbs = r.varlen ? a->k_row_stride * sk : a->k_batch_stride;
+  const int64_t vbs = r.varlen ? a->v_row_stride * sk : a->v_batch_stride;
   const int d = a->head_dim_qk;
   // the maps of an empty side are stand-ins (copies of the other side's), never read
   CUtensorMap mq, mk, mv, mdo;
-  if (has_q && (!make_map(&mq, a->q, d, sq, a->num_heads_q, a->batch, a->q_row_stride, a->q_head_stride,
-                          a->q_batch_stride, 128) ||
-                !make_map(&mdo, dout, d, sq, a->num_heads_q, a->batch, a->o_row_stride, a->o_head_stride,
-                          a->o_batch_stride, 128)))
+  if (has_q && (!make_map(&mq, a->q, d, sq, a->num_heads_q, nb, a->q_row_stride, a->q_head_stride, qbs, 128) ||
+                !make_map(&mdo, dout, d, sq, a->num_heads_q, nb, a->o_row_stride, a->o_head_stride, obs, 128)))
     return FA_ERR_CUDA;
-  if (has_k && (!make_map(&mk, a->k, d, sk, a->num_heads_kv, a->batch, a->k_row_stride, a->k_head_stride,
-                          a->k_batch_stride, 128) ||
-                !make_map(&mv, a->v, d, sk, a->num_heads_kv, a->batch, a->v_row_stride, a->v_head_stride,
-                          a->v_batch_stride, 128)))
+  if (has_k && (!make_map(&mk, a->k, d, sk, a->num_heads_kv, nb, a->k_row_stride, a->k_head_stride, kbs, 128) ||
+                !make_map(&mv, a->v, d, sk, a->num_heads_kv, nb, a->v_row_stride, a->v_head_stride, vbs, 128)))
     return FA_ERR_CUDA;
   if (!has_q) mq = mdo = mk;
   if (!has_k) mk = mv = mq;

@@ -164,19 +164,46 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int d) {
   for (int c = 0; c < d / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
 }
 
+// One sequence of the call: its lengths, its first rows in q's and k's row
+// axes (0 when batched), the batch coordinate of the tensor maps and the
+// first workspace row of q head h.
+struct BSeq {
+  int sq, sk, q_row0, k_row0, bc;
+};
+
+__device__ __forceinline__ BSeq bwd_seq(const BwdParams& p, int b) {
+  BSeq S;
+  if (p.cu_seqlens_q != nullptr) {
+    S.q_row0 = p.cu_seqlens_q[b];
+    S.sq = p.cu_seqlens_q[b + 1] - S.q_row0;
+    S.k_row0 = p.cu_seqlens_k[b];
+    S.sk = p.cu_seqlens_k[b + 1] - S.k_row0;
+    S.bc = 0;
+  } else {
+    S.q_row0 = S.k_row0 = 0;
+    S.sq = p.seqlen_q;
+    S.sk = p.seqlen_k;
+    S.bc = b;
+  }
+  return S;
+}
+
+__device__ __forceinline__ int64_t ws_row0(const BwdParams& p, int b, int h) {
+  return p.cu_seqlens_q != nullptr ? int64_t(h) * p.ws_rows + bwd_ws_row0(p.cu_seqlens_q, b)
+                                   : (int64_t(b) * p.hq + h) * p.sq_pad;
+}
+
 // ---------------------------------------------------------------------------
-// preprocess: 8 threads per row
-__global__ void bwd_preprocess_kernel(const BwdParams p, int dv) {
+// preprocess: one CTA per (sequence, 128-row block, q head), 8 threads per row
+__global__ void __launch_bounds__(1024) bwd_preprocess_kernel(const BwdParams p, int dv, int max_mb) {
+  const int b = blockIdx.x / max_mb, m = blockIdx.x % max_mb, h = blockIdx.y;
+  const BSeq S = bwd_seq(p, b);
+  if (m * 128 >= S.sq) return;   // (whole CTA)
   const int sub = threadIdx.x & 7;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 3) + (threadIdx.x >> 3);
-  // rows = batch * hq * sq_pad, a multiple of 128, and the grid covers it
-  // exactly, so every warp is whole for the shuffles below
-  const int i = static_cast<int>(row % p.sq_pad);
-  const int64_t bh = row / p.sq_pad;
-  const int h = static_cast<int>(bh % p.hq), b = static_cast<int>(bh / p.hq);
+  const int i = m * 128 + (threadIdx.x >> 3);
   float acc = 0.f;
-  if (i < p.seqlen_q) {
-    const int64_t o_off = int64_t(b) * p.o_bs + int64_t(i) * p.o_rs + int64_t(h) * p.o_hs;
+  if (i < S.sq) {
+    const int64_t o_off = int64_t(S.bc) * p.o_bs + int64_t(S.q_row0 + i) * p.o_rs + int64_t(h) * p.o_hs;
     const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.out) + o_off;
     const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + o_off;
     for (int c = sub * 8; c < dv; c += 64) {
@@ -193,13 +220,16 @@ __global__ void bwd_preprocess_kernel(const BwdParams p, int dv) {
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   if (sub == 0) {
-    float l2 = INFINITY;   // P = exp2(... - inf) = 0
-    if (i < p.seqlen_q) {
-      const float lse = p.lse[(int64_t(b) * p.hq + h) * p.seqlen_q + i];
+    float l2 = INFINITY;   // P = exp2(... - inf) = 0 (padding rows, rows without keys)
+    if (i < S.sq) {
+      const int64_t li = p.cu_seqlens_q != nullptr ? int64_t(h) * p.total_q + S.q_row0 + i
+                                                   : (int64_t(b) * p.hq + h) * p.seqlen_q + i;
+      const float lse = p.lse[li];
       if (lse != -INFINITY) l2 = lse * 1.4426950408889634f;
     }
-    p.lse2[row] = l2;
-    p.dsum[row] = acc;
+    const int64_t w = ws_row0(p, b, h) + i;
+    p.lse2[w] = l2;
+    p.dsum[w] = acc;
   }
 }
 
@@ -219,9 +249,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   const int b = blockIdx.x / p.hq, h = blockIdx.x % p.hq, g = h / p.r;
   const int mb = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);   // longest tiles first
-  const int off = p.seqlen_k - p.seqlen_q;
-  const int i0 = mb * kB, ilast = min(i0 + kB - 1, p.seqlen_q - 1);
-  int klo = 0, khi = p.seqlen_k;
+  const BSeq S = bwd_seq(p, b);
+  if (mb * kB >= S.sq) return;   // a tile past this sequence's end (whole CTA, before any barrier)
+  const int off = S.sk - S.sq;
+  const int i0 = mb * kB, ilast = min(i0 + kB - 1, S.sq - 1);
+  int klo = 0, khi = S.sk;
   if (p.wl >= 0) klo = max(klo, i0 + off - p.wl);
   if (p.wr >= 0) khi = min(khi, ilast + off + p.wr + 1);
   const int nlo = klo / kB, nhi = (khi > klo) ? (khi + kB - 1) / kB : nlo;
@@ -251,8 +283,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive_expect_tx(B.res_full, 2 * Cfg::T_BYTES);
 #pragma unroll
       for (int c = 0; c < Cfg::CH; ++c) {
-        tma_load_4d(res + c * kChunk, &mapQ, B.res_full, c * 64, i0, h, b);
-        tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapDO, B.res_full, c * 64, i0, h, b);
+        tma_load_4d(res + c * kChunk, &mapQ, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
+        tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapDO, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
       }
       uint32_t u = 0;
       for (int n = nhi - 1; n >= nlo; --n, ++u) {
@@ -262,8 +294,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&B.str_full[st], 2 * Cfg::T_BYTES);
 #pragma unroll
         for (int c = 0; c < Cfg::CH; ++c) {
-          tma_load_4d(dst + c * kChunk, &mapK, &B.str_full[st], c * 64, n * kB, g, b);
-          tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapV, &B.str_full[st], c * 64, n * kB, g, b);
+          tma_load_4d(dst + c * kChunk, &mapK, &B.str_full[st], c * 64, S.k_row0 + n * kB, g, S.bc);
+          tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapV, &B.str_full[st], c * 64, S.k_row0 + n * kB, g, S.bc);
         }
       }
       // drain the copies still in flight (only after an abort can any be)
@@ -322,9 +354,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int t = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int i = i0 + t;
-    const int64_t vrow = (int64_t(b) * p.hq + h) * p.sq_pad + i;
-    __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(p.dq) + int64_t(b) * p.q_bs + int64_t(i) * p.q_rs +
-                        int64_t(h) * p.q_hs + c * (D / 2);
+    const int64_t vrow = ws_row0(p, b, h) + i;   // inside the sequence's 128-row padded region
+    __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(p.dq) + int64_t(S.bc) * p.q_bs +
+                        int64_t(S.q_row0 + i) * p.q_rs + int64_t(h) * p.q_hs + c * (D / 2);
     if (has) {
       const float nl2 = -p.lse2[vrow], dsum = p.dsum[vrow];
       bool ok = true;
@@ -332,11 +364,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       for (int n = nhi - 1; n >= nlo; --n, ++u) {
         const int jb = n * kB;
         // every (row, key) of the block visible?  (uniform over the CTA)
-        const bool full = (jb + kB <= p.seqlen_k) && (p.wr < 0 || jb + kB - 1 <= i0 + off + p.wr) &&
+        const bool full = (jb + kB <= S.sk) && (p.wr < 0 || jb + kB - 1 <= i0 + off + p.wr) &&
                           (p.wl < 0 || jb >= i0 + kB - 1 + off - p.wl);
         // visible columns [c_lo, c_hi] of this row, relative to this warpgroup's first column
         const int c_lo = ((p.wl >= 0) ? i + off - p.wl - jb : INT32_MIN / 2) - 64 * c;
-        int c_hi = p.seqlen_k - 1 - jb;
+        int c_hi = S.sk - 1 - jb;
         if (p.wr >= 0) c_hi = min(c_hi, i + off + p.wr - jb);
         c_hi -= 64 * c;
         // P = exp2(S scale log2(e) - LSE log2(e)), masked
@@ -379,10 +411,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int k = 0; k < D / 64; ++k) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_off + 256 + c * (D / 2) + k * 32, o);
-          if (i < p.seqlen_q) store_row32(dq + k * 32, o, p.scale);
+          if (i < S.sq) store_row32(dq + k * 32, o, p.scale);
         }
       }
-    } else if (i < p.seqlen_q) {
+    } else if (i < S.sq) {
       zero_row(dq, D / 2);   // no visible key: dQ = 0
     }
   }
@@ -411,10 +443,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   const int b = blockIdx.x / p.hkv, g = blockIdx.x % p.hkv;
   const int n = blockIdx.y;   // low key blocks first: under a causal mask they see the most query tiles
-  const int off = p.seqlen_k - p.seqlen_q;
-  const int j0 = n * kB, jlast = min(j0 + kB - 1, p.seqlen_k - 1);
+  const BSeq S = bwd_seq(p, b);
+  if (n * kB >= S.sk) return;   // a block past this sequence's keys (whole CTA, before any barrier)
+  const int off = S.sk - S.sq;
+  const int j0 = n * kB, jlast = min(j0 + kB - 1, S.sk - 1);
   // query rows that see some key of the block
-  int ilo = 0, ihi = p.seqlen_q - 1;
+  int ilo = 0, ihi = S.sq - 1;
   if (p.wr >= 0) ilo = max(ilo, j0 - off - p.wr);
   if (p.wl >= 0) ihi = min(ihi, jlast - off + p.wl);
   const int mlo = ilo / kB, nm = (ihi >= ilo) ? ihi / kB + 1 - mlo : 0;
@@ -444,8 +478,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive_expect_tx(B.res_full, 2 * Cfg::T_BYTES);
 #pragma unroll
       for (int c = 0; c < Cfg::CH; ++c) {
-        tma_load_4d(res + c * kChunk, &mapK, B.res_full, c * 64, j0, g, b);
-        tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapV, B.res_full, c * 64, j0, g, b);
+        tma_load_4d(res + c * kChunk, &mapK, B.res_full, c * 64, S.k_row0 + j0, g, S.bc);
+        tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapV, B.res_full, c * 64, S.k_row0 + j0, g, S.bc);
       }
       uint32_t u = 0;
       for (; u < static_cast<uint32_t>(jobs); ++u) {
@@ -454,12 +488,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (u >= Cfg::ST && !mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard)) break;
         uint8_t* dst = smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES;
         float* vec = reinterpret_cast<float*>(smem + Cfg::OFF_VEC + st * 1024);
-        const int64_t vrow = (int64_t(b) * p.hq + hh) * p.sq_pad + m * kB;
+        const int64_t vrow = ws_row0(p, b, hh) + m * kB;
         mbar_arrive_expect_tx(&B.str_full[st], 2 * Cfg::T_BYTES + 1024);
 #pragma unroll
         for (int c = 0; c < Cfg::CH; ++c) {
-          tma_load_4d(dst + c * kChunk, &mapQ, &B.str_full[st], c * 64, m * kB, hh, b);
-          tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapDO, &B.str_full[st], c * 64, m * kB, hh, b);
+          tma_load_4d(dst + c * kChunk, &mapQ, &B.str_full[st], c * 64, S.q_row0 + m * kB, hh, S.bc);
+          tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapDO, &B.str_full[st], c * 64, S.q_row0 + m * kB, hh, S.bc);
         }
         bulk_load(vec, p.lse2 + vrow, 512, &B.str_full[st]);
         bulk_load(vec + 128, p.dsum + vrow, 512, &B.str_full[st]);
@@ -526,23 +560,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int t = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int j = j0 + t;
-    __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk) + int64_t(b) * p.k_bs + int64_t(j) * p.k_rs +
-                        int64_t(g) * p.k_hs;
-    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv) + int64_t(b) * p.v_bs + int64_t(j) * p.v_rs +
-                        int64_t(g) * p.v_hs;
+    __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(p.dk) + int64_t(S.bc) * p.k_bs +
+                        int64_t(S.k_row0 + j) * p.k_rs + int64_t(g) * p.k_hs;
+    __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv) + int64_t(S.bc) * p.v_bs +
+                        int64_t(S.k_row0 + j) * p.v_rs + int64_t(g) * p.v_hs;
     if (jobs > 0) {
       bool ok = true;
       for (uint32_t u = 0; u < static_cast<uint32_t>(jobs); ++u) {
         const int st = u % Cfg::ST;
         const int m = mlo + static_cast<int>(u) % nm;
         const int ib = m * kB;
-        const bool full = (j0 + kB <= p.seqlen_k) && (ib + kB <= p.seqlen_q) &&
+        const bool full = (j0 + kB <= S.sk) && (ib + kB <= S.sq) &&
                           (p.wr < 0 || j0 + kB - 1 <= ib + off + p.wr) && (p.wl < 0 || j0 >= ib + kB - 1 + off - p.wl);
         // visible query columns [c_lo, c_hi] of this key row, relative to this warpgroup's first column
         const int c_lo = ((p.wr >= 0) ? j - off - p.wr - ib : INT32_MIN / 2) - 64 * c;
-        int c_hi = p.seqlen_q - 1 - ib;
+        int c_hi = S.sq - 1 - ib;
         if (p.wl >= 0) c_hi = min(c_hi, j - off + p.wl - ib);
-        if (j >= p.seqlen_k) c_hi = -1 + 64 * c;
+        if (j >= S.sk) c_hi = -1 + 64 * c;
         c_hi -= 64 * c;
         // the stage's lse2 / D landed with its tiles
         if (!mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard)) { ok = false; break; }
@@ -602,10 +636,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int k = 0; k < D / 32; ++k) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_off + 256 + c * D + k * 32, o);
-          if (j < p.seqlen_k) store_row32(dst + k * 32, o, f);
+          if (j < S.sk) store_row32(dst + k * 32, o, f);
         }
       }
-    } else if (j < p.seqlen_k) {
+    } else if (j < S.sk) {
       zero_row(c == 0 ? dv : dk, D);   // no query sees these keys
     }
   }
@@ -648,13 +682,14 @@ template <int D>
 cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, cudaStream_t stream) {
   using Cfg = BwdCfg<D>;
-  const int64_t rows = int64_t(p.batch) * p.hq * p.sq_pad;
-  if (rows > 0) {
-    bwd_preprocess_kernel<<<static_cast<unsigned>(rows / 32), 256, 0, stream>>>(p, D);
+  // batched: every sequence's lengths; varlen: the longest (CTAs past a
+  // shorter sequence's end return at once)
+  const int mblocks = (p.seqlen_q + kB - 1) / kB, nblocks = (p.seqlen_k + kB - 1) / kB;
+  if (mblocks > 0 && p.batch > 0) {
+    bwd_preprocess_kernel<<<dim3(p.batch * mblocks, p.hq), 1024, 0, stream>>>(p, D, mblocks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int mblocks = (p.seqlen_q + kB - 1) / kB, nblocks = (p.seqlen_k + kB - 1) / kB;
   cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);

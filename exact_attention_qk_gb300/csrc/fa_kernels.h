@@ -56,10 +56,12 @@ cudaError_t launch_decode(const FwdParams& p, int dk, int dv, const CUtensorMap&
 bool decode_supported(int dk, int dv);
 int decode_max_rows();
 
-// Backward (dQ, dK, dV): batched layout, head dims 64 or 128 (dk == dv).
-// dq / dk / dv take q's / k's / v's strides, dout and out take the o strides;
-// lse2 and dsum are workspace arrays [batch][hq][sq_pad] (sq_pad = 128-row
-// multiple of seqlen_q).
+// Backward (dQ, dK, dV): batched or packed varlen layout, head dims 64 or
+// 128 (dk == dv). dq / dk / dv take q's / k's / v's strides, dout and out
+// take the o strides. lse2 and dsum are workspace arrays: batched
+// [batch][hq][sq_pad] (sq_pad = 128-row multiple of seqlen_q); varlen
+// [hq][ws_rows], sequence b's rows starting at bwd_ws_row0(b) (a multiple of
+// 4, and 128-row padded regions that do not overlap).
 struct BwdParams {
   const void* out;
   const void* dout;
@@ -73,13 +75,22 @@ struct BwdParams {
   int64_t k_bs, k_rs, k_hs;
   int64_t v_bs, v_rs, v_hs;
   int64_t o_bs, o_rs, o_hs;
-  int batch, seqlen_q, seqlen_k, sq_pad;
+  int batch, seqlen_q, seqlen_k, sq_pad;  // batched sizes (varlen: max_seqlen_q / _k, and sq_pad unused)
   int hq, hkv, r;
   float scale, scale_log2;
   int wl, wr;                    // -1 = unbounded; wr is 0 when causal
+  const int* cu_seqlens_q;       // varlen: int32 [batch+1], else NULL
+  const int* cu_seqlens_k;
+  int total_q;                   // varlen: rows of q (LSE row stride)
+  int64_t ws_rows;               // varlen: workspace rows per head
   int* status;
   unsigned long long timeout_ns;
 };
+// first workspace row of sequence b (varlen): 4-aligned, and far enough past
+// sequence b-1's padded region (which ends before cu_seqlens_q[b] + 132 b)
+__host__ __device__ inline int64_t bwd_ws_row0(const int* cu_seqlens_q, int b) {
+  return ((int64_t(cu_seqlens_q[b]) + 132 * int64_t(b) + 3) / 4) * 4;
+}
 cudaError_t launch_bwd(const BwdParams& p, int d, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream);
 bool bwd_supported(int dk, int dv);

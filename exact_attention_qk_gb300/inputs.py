@@ -178,8 +178,14 @@ def batched(name, seed, B, Sq, Sk, Hq, Hkv, Dqk, Dv, scale=None, causal=False,
 
 
 def grad_out(w: Workload) -> np.ndarray:
-    """dO for the backward of a batched workload: N(0,1) bf16 bits with the
-    output's shape (B, Sq, Hq, Dv), one stream per sequence."""
+    """dO for the backward of a workload: N(0,1) bf16 bits with the output's
+    shape, (B, Sq, Hq, Dv) or packed (T, Hq, Dv), one stream per sequence."""
+    if w.varlen:
+        cu = w.cu_seqlens_q
+        do = np.empty((int(cu[-1]), w.num_heads_q, w.head_dim_v), np.uint16)
+        for b in range(len(cu) - 1):
+            do[cu[b]:cu[b + 1]] = normal_bf16(w.seed, _DO, b, (int(cu[b + 1] - cu[b]), w.num_heads_q, w.head_dim_v))
+        return do
     do = np.empty((w.batch, w.seqlen_q, w.num_heads_q, w.head_dim_v), np.uint16)
     for b in range(w.batch):
         do[b] = normal_bf16(w.seed, _DO, b, (w.seqlen_q, w.num_heads_q, w.head_dim_v))

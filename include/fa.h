@@ -224,14 +224,15 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
  * D = rowsum(dO * O); the main loop recomputes P from the stored LSE and forms
  *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q;
  * with GQA, dK and dV of KV head g sum over the q heads that read it).
- * args: the forward's arguments, batched layout. args->out must hold the
- *   forward's O and args->lse its LSE (both read, not written).
+ * args: the forward's arguments, batched or packed varlen layout (as for
+ *   fa_fwd). args->out must hold the forward's O and args->lse its LSE (both
+ *   read, not written).
  * dout: dO, bf16, out's shape and strides (o_*_stride).
  * dq / dk / dv: written, bf16, with q's / k's / v's shapes and strides. Keys
  *   that no query sees get dK = dV = 0; rows that see no key get dQ = 0.
  * Supported: (head_dim_qk, head_dim_v) (64,64) or (128,128); causal, sliding
- *   window and GQA/MQA as in the forward. cu_seqlens, seqused_k, a page table
- *   or an fp8 cache give FA_ERR_UNSUPPORTED.
+ *   window, GQA/MQA and varlen (cu_seqlens_q / cu_seqlens_k) as in the
+ *   forward. seqused_k, a page table or an fp8 cache give FA_ERR_UNSUPPORTED.
  * workspace: at least fa_bwd_workspace_size(args) bytes, 256-byte aligned
  *   (fp32 LSE * log2(e) and D for every padded query row). The call is
  *   deterministic: no atomics, the same inputs give the same bits.

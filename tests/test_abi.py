@@ -140,8 +140,6 @@ def test_status_strings(fa):
 
 
 @pytest.mark.parametrize("over,code", [
-    (dict(cu_seqlens_q=0x50000, cu_seqlens_k=0x60000, total_q=600, total_k=600, max_seqlen_q=300,
-          max_seqlen_k=300), 2),                         # varlen
     (dict(seqused_k=0x50000), 2),
     (dict(page_table=0x50000, max_pages_per_seq=3, page_size=128, num_pages=6), 2),
     (dict(kv_format=1), 2),                               # fp8 cache
@@ -166,3 +164,14 @@ def test_backward_workspace(fa):
     assert fa.lib().fa_bwd(ctypes.byref(a), 0x80008, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 3
     assert fa.fa_bwd_workspace_size(_args(fa, head_dim_qk=192, head_dim_v=128)) == 0
     assert fa.lib().fa_bwd(ctypes.byref(_args(fa, batch=0)), 0, 0, 0, 0, None, 0, None) == 0
+
+
+def test_backward_varlen_workspace(fa):
+    # packed varlen: per q head, total_q + 132 rows per sequence + 4, rounded up to 32 rows
+    a = _args(fa, lse=0x70000, cu_seqlens_q=0x50000, cu_seqlens_k=0x60000, total_q=600, total_k=600,
+              max_seqlen_q=300, max_seqlen_k=300)
+    rows = -(-(600 + 132 * 2 + 4) // 32) * 32
+    per = -(-(8 * rows * 4) // 256) * 256
+    assert fa.fa_bwd_workspace_size(a) == 2 * per
+    # accepted: the next check is the missing workspace
+    assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 4

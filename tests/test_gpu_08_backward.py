@@ -33,15 +33,33 @@ TOL_CANCELLED_ZERO = 1e-4
 def run_bwd(w, do_bits):
     from exact_attention_qk_gb300 import fa
     q, k, v, do = gu.to_dev(w.q), gu.to_dev(w.k), gu.to_dev(w.v), gu.to_dev(do_bits)
-    o, lse = fa.fa_fwd(q, k, v, **gu.kw_of(w))
-    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, **gu.kw_of(w))
+    kw = dict(gu.kw_of(w))
+    if w.varlen:
+        kw.update(cu_seqlens_q=gu.i32(w.cu_seqlens_q), cu_seqlens_k=gu.i32(w.cu_seqlens_k),
+                  max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k)
+    o, lse = fa.fa_fwd(q, k, v, **kw)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, **kw)
     assert fa.fa_get_status() == fa.FA_OK
     return dq, dk, dv
 
 
 def oracle_bwd(w, do_bits):
-    return oracle.attention_backward(w.q, w.k, w.v, do_bits, scale=w.softmax_scale, causal=w.causal,
-                                     window_left=w.window_left, window_right=w.window_right)
+    kw = dict(scale=w.softmax_scale, causal=w.causal, window_left=w.window_left, window_right=w.window_right)
+    if not w.varlen:
+        return oracle.attention_backward(w.q, w.k, w.v, do_bits, **kw)
+    # packed varlen: each sequence is its own batched problem of batch 1
+    dq = np.zeros(w.q.shape, np.float64)
+    dk = np.zeros(w.k.shape, np.float64)
+    dv = np.zeros(w.v.shape, np.float64)
+    cq, ck = w.cu_seqlens_q, w.cu_seqlens_k
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        if q1 == q0 or k1 == k0:
+            continue   # no query row or no key: every gradient of the sequence is 0
+        rq, rk, rv = oracle.attention_backward(w.q[None, q0:q1], w.k[None, k0:k1], w.v[None, k0:k1],
+                                               do_bits[None, q0:q1], **kw)
+        dq[q0:q1], dk[k0:k1], dv[k0:k1] = rq[0], rk[0], rv[0]
+    return dq, dk, dv
 
 
 def compare(got, ref, what):
@@ -147,6 +165,30 @@ def test_deterministic():
     b = run_bwd(w, do)
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_self_attention(d):
+    # packed sequences of mixed lengths (one row, tails, several tiles), causal, GQA 8/2
+    lens = [300, 1, 129, 513, 64]
+    w = inputs.packed("bwdvl", 440 + d, lens, lens, 8, 2, d, d, causal=True)
+    print(check_bwd(w))
+
+
+def test_varlen_unequal_lengths_window_and_empty_sequences():
+    # bottom-right causal with a window, Sq != Sk per sequence, a sequence
+    # without keys (its dQ is 0) and one without queries (its dK, dV are 0)
+    lens_q = [200, 77, 0, 300, 40]
+    lens_k = [520, 77, 90, 0, 1000]
+    w = inputs.packed("bwdvl2", 442, lens_q, lens_k, 4, 4, 128, 128, causal=True, window_left=150)
+    print(check_bwd(w))
+
+
+def test_varlen_dense_mqa():
+    lens_q = [130, 257, 1]
+    lens_k = [400, 300, 640]
+    w = inputs.packed("bwdvl3", 443, lens_q, lens_k, 8, 1, 64, 64)
+    print(check_bwd(w))
 
 
 @pytest.mark.slow
