@@ -1,15 +1,19 @@
-"""Benchmark of the exact attention forward on GB300.
+"""Benchmark of the exact attention forward (and its backward) on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload causal|large_dense|large_causal|varlen|decode|tiny] [--only]
+                [--workload <name from inputs.WORKLOADS>] [--only]
 
-One step is one forward of the named workload (inputs resident in HBM): for the
+One step is one call of the named workload (inputs resident in HBM): for the
 prefill workloads one persistent tcgen05 kernel (plus the varlen prepare
-kernel), for decode the split-KV kernel plus the combine kernel. The headline
-line is the causal GQA prefill (B=2, Hq=32, Hkv=4, Sq=Sk=4096, D=128) in
-TFLOP/s with the standard attention FLOP count 2*(Dqk+Dv)*#visible(i,j); the
-other workloads are measured in the same run and reported under "workloads"
-(decode in GB/s of algorithmic bytes: Q + visible K/V rows + O + LSE).
+kernel, or the combine when the library splits a small grid over the keys),
+for decode the split-KV kernel plus the combine kernel, for the backward
+workloads (`*_bwd`) one fa_bwd call (preprocess, dQ and dK/dV kernels; the
+forward's O and LSE are made once, untimed). The headline line is the causal
+GQA prefill (B=2, Hq=32, Hkv=4, Sq=Sk=4096, D=128) in TFLOP/s with the
+standard attention FLOP count 2*(Dqk+Dv)*#visible(i,j); the other workloads
+are measured in the same run and reported under "workloads" (decode in GB/s
+of algorithmic bytes: Q + visible K/V rows + O + LSE; the backward in TFLOP/s
+of its five GEMMs, 2*(3*Dqk+2*Dv)*#visible(i,j)).
 
 Timing: W untimed steps, then K steps each bracketed by CUDA events on the
 launching stream, with an L2 flush (a 512 MB write) before every timed step
