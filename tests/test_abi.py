@@ -126,11 +126,44 @@ def test_split_policy(fa):
     # few units: more splits to fill the SMs
     a = _args(fa, batch=1, seqlen_q=1, seqlen_k=16384, num_heads_q=8, num_heads_kv=8)
     assert fa.fa_num_splits(a, 152) == 32
-    # prefill shapes are not split by default
+    # a prefill grid that fills more than half of the SMs, or has too few key
+    # blocks to split (300 keys: 3 blocks), is not split
     a = _args(fa)
     assert fa.fa_num_splits(a, 152) == 1
+    # the count fa_fwd would choose with num_splits == 0, whatever the field holds
     a = _args(fa, num_splits=5)
-    assert fa.fa_num_splits(a, 152) == 5 or fa.fa_num_splits(a, 152) == 1
+    assert fa.fa_num_splits(a, 152) == 1
+
+
+def _batched(fa, B, sq, sk, hq, hkv, d=128, **over):
+    a = _args(fa, batch=B, seqlen_q=sq, seqlen_k=sk, num_heads_q=hq, num_heads_kv=hkv, head_dim_qk=d, head_dim_v=d)
+    a.q_batch_stride, a.q_row_stride, a.q_head_stride = sq * hq * d, hq * d, d
+    a.o_batch_stride, a.o_row_stride, a.o_head_stride = sq * hq * d, hq * d, d
+    a.k_batch_stride, a.k_row_stride, a.k_head_stride = sk * hkv * d, hkv * d, d
+    a.v_batch_stride, a.v_row_stride, a.v_head_stride = sk * hkv * d, hkv * d, d
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_prefill_split_policy(fa):
+    # 8 tiles (one 256-row tile per head) against 64 key blocks on 152 SMs:
+    # min(152 // 8, 64 // 4, 32) = 16 splits of 4 blocks
+    assert fa.fa_num_splits(_batched(fa, 1, 256, 8192, 8, 8), 152) == 16
+    # one request's chunk: 32 unpacked tiles (256 rows are too many to pack), 128 key blocks
+    assert fa.fa_num_splits(_batched(fa, 1, 256, 16384, 32, 8), 152) == 4
+    # pack-GQA: 100 rows x 8 heads = 4 packed tiles per KV head, 4 KV heads = 16
+    # tiles; 32 key blocks: min(9, 8, 32) = 8 -> 4 blocks per split -> 8
+    assert fa.fa_num_splits(_batched(fa, 1, 100, 4096, 32, 4), 152) == 8
+    # the chunked-prefill workload fills 128 of 152 SMs: not split
+    assert fa.fa_num_splits(_batched(fa, 8, 128, 8192, 32, 4), 152) == 1
+    # the split count shrinks so that no split is empty: 10 blocks, at most
+    # 152 // 8 = 19 and 10 // 4 = 2 splits -> 2 of 5 blocks
+    assert fa.fa_num_splits(_batched(fa, 1, 256, 1280, 8, 8), 152) == 2
+    # fp8 caches stay on the decode kernel, unsplit at prefill shapes
+    assert fa.fa_num_splits(_batched(fa, 1, 256, 8192, 8, 8, kv_format=1), 152) == 1
+    # more SMs, more splits (capped at 32)
+    assert fa.fa_num_splits(_batched(fa, 1, 256, 65536, 2, 2), 152) == 32
 
 
 def test_status_strings(fa):
