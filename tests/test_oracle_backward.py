@@ -126,3 +126,25 @@ def test_gqa_equals_explicit_repetition():
     np.testing.assert_allclose(dq, rq, rtol=0, atol=1e-14)
     np.testing.assert_allclose(dk, rk.reshape(1, 6, 2, 2, 3).sum(axis=3), rtol=0, atol=1e-14)
     np.testing.assert_allclose(dv, rv.reshape(1, 6, 2, 2, 3).sum(axis=3), rtol=0, atol=1e-14)
+
+
+def test_hand_worked_golden_example():
+    """tests/golden/hand_backward.txt: one query, two keys, solved by hand."""
+    import math
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "hand_backward.txt")
+    vals = {}
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if "=" in line:
+            key, val = line.split("=", 1)
+            vals[key.strip()] = val.strip()
+    env = {"log": math.log}
+    q = np.array(eval(vals["q"], env), float).reshape(1, 1, 1, -1)
+    k = np.array(eval(vals["k"], env), float).reshape(1, 2, 1, -1)
+    v = np.array(eval(vals["v"], env), float).reshape(1, 2, 1, -1)
+    do = np.array(eval(vals["dO"], env), float).reshape(1, 1, 1, -1)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, scale=float(vals["scale"]))
+    np.testing.assert_allclose(dq[0, 0, 0], eval(vals["dQ"], env), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dk[0, :, 0], eval(vals["dK"], env), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dv[0, :, 0], eval(vals["dV"], env), rtol=0, atol=1e-14)
