@@ -273,9 +273,11 @@ def fa_bwd_workspace_size(args: FwdArgs) -> int:
 def fa_bwd(q, k, v, out, lse, dout, dq=None, dk=None, dv=None, *, workspace=None, stream=None, **kw):
     """dQ, dK, dV of the forward (q, k, v) -> (out, lse), given dO.
 
-    Batched layout. out and lse are the forward's results; dout has out's
+    Batched or packed varlen layout (pass the forward's cu_seqlens_q/k and
+    max_seqlen_q/k). out and lse are the forward's results; dout has out's
     shape and strides; dq / dk / dv (allocated when None) take q's / k's / v's.
-    kw: the forward's mask and scale keywords (see make_args).
+    kw: the forward's mask, scale and varlen keywords (see make_args).
+    Deterministic: the same inputs give the same bits.
     """
     if dq is None:
         dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
