@@ -10,7 +10,6 @@ from .attention import (  # noqa: F401
     lse_to_row_order,
     sequences,
     split_forward,
-    visible,
     visible_count,
     visible_mask,
     widen,

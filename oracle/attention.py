@@ -80,20 +80,6 @@ def sequences(q_shape, k_shape, cu_seqlens_q=None, cu_seqlens_k=None, seqused_k=
     return [Seq(0, Sq, 0, Sk if seqused_k is None else int(seqused_k[b])) for b in range(B)]
 
 
-def visible(i: int, j: int, sq: int, sk: int, causal: bool, wl: int, wr: int) -> bool:
-    """Scalar visibility rule (bottom-right aligned diagonal)."""
-    if causal:
-        wr = 0
-    off = sk - sq
-    if j < 0 or j >= sk:
-        return False
-    if wl >= 0 and j < i + off - wl:
-        return False
-    if wr >= 0 and j > i + off + wr:
-        return False
-    return True
-
-
 def visible_mask(sq: int, sk: int, causal: bool, wl: int, wr: int,
                  rows: Optional[np.ndarray] = None, key_lo: int = 0, key_hi: Optional[int] = None) -> np.ndarray:
     """Boolean [len(rows), sk] mask; keys outside [key_lo, key_hi) are hidden."""

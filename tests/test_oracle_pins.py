@@ -353,3 +353,55 @@ def test_visible_count_closed_forms():
     wl = 17
     assert oracle.visible_count(n, n, True, wl, -1) == sum(min(i, wl) + 1 for i in range(n))
     assert oracle.visible_count(1, 1000, False, -1, -1) == 1000
+
+
+# ---- widen(): bf16 bit patterns -> float64 ---------------------------------------
+# Every GPU parity check hands the oracle raw bf16 bits (uint16), so the widening
+# is pinned on its own: hand-decoded patterns (sign bit 15, biased exponent bits
+# 14..7 with bias 127, seven mantissa bits), then all 65536 patterns against
+# torch's bfloat16 -> float64 conversion (a library route).
+
+@pytest.mark.parametrize("bits,want", [
+    (0x3F80, 1.0),
+    (0xC000, -2.0),
+    (0x3F81, 1.0 + 2.0 ** -7),
+    (0x4049, 3.140625),                         # 2 * (1 + 73/128)
+    (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127),   # largest finite
+    (0x0080, 2.0 ** -126),                      # smallest normal
+    (0x0001, 2.0 ** -133),                      # smallest subnormal
+    (0x7F80, math.inf),
+    (0xFF80, -math.inf),
+    (0x0000, 0.0),
+])
+def test_widen_bf16_hand_decoded(bits, want):
+    got = oracle.widen(np.array([bits], np.uint16))
+    assert got.dtype == np.float64
+    assert got[0] == want
+
+
+def test_widen_bf16_signed_zero_and_nan():
+    got = oracle.widen(np.array([0x8000, 0x7FC0, 0xFFC1], np.uint16))
+    assert got[0] == 0.0 and math.copysign(1.0, got[0]) == -1.0
+    assert np.isnan(got[1]) and np.isnan(got[2])
+
+
+def test_widen_bf16_all_patterns_match_torch():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.widen(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert (got[~nan] == ref[~nan]).all()
+    assert (np.signbit(got[~nan]) == np.signbit(ref[~nan])).all()
+
+
+def test_forward_on_bf16_bits_equals_forward_on_their_values():
+    """The same tiny case given as bf16 bits and as the float values those bits
+    stand for (decoded by torch) gives identical O and LSE."""
+    w = inputs.batched("t", 11, 2, 9, 13, 4, 2, 16, 8, causal=True, window_left=5)
+    vals = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+            for a in (w.q, w.k, w.v)]
+    o_bits, l_bits = oracle.attention_forward(w.q, w.k, w.v, causal=True, window_left=5)
+    o_vals, l_vals = oracle.attention_forward(*vals, causal=True, window_left=5)
+    assert np.array_equal(o_bits, o_vals)
+    assert np.array_equal(l_bits, l_vals)
