@@ -1,26 +1,33 @@
 """Benchmark of the exact attention forward (and its backward) on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload <name from inputs.WORKLOADS>] [--only]
+                [--workload <name from inputs.WORKLOADS>] [--only] [--dry-run]
 
 One step is one call of the named workload (inputs resident in HBM): for the
 prefill workloads one persistent tcgen05 kernel (plus the varlen prepare
 kernel, or the combine when the library splits a small grid over the keys),
 for decode the split-KV kernel plus the combine kernel, for the backward
-workloads (`*_bwd`) one fa_bwd call (preprocess, dQ and dK/dV kernels; the
-forward's O and LSE are made once, untimed). The headline line is the causal
+workloads (`*_bwd`) one backward call (fa_bwd_two_streams: the preprocess,
+then the dK/dV kernel on a second, torch-owned stream concurrent with the dQ
+kernel; the forward's O and LSE are made once, untimed). The headline line is the causal
 GQA prefill (B=2, Hq=32, Hkv=4, Sq=Sk=4096, D=128) in TFLOP/s with the
-standard attention FLOP count 2*(Dqk+Dv)*#visible(i,j); the other workloads
-are measured in the same run and reported under "workloads" (decode in GB/s
-of algorithmic bytes: Q + visible K/V rows + O + LSE; the backward in TFLOP/s
-of its five GEMMs, 2*(3*Dqk+2*Dv)*#visible(i,j)).
+standard attention FLOP count 2*(Dqk+Dv)*#visible(i,j). The other workloads
+(the same shape without a mask, the tiny case, the large head dim, varlen,
+decode and its cache forms, chunked prefill, the backward) are measured in the
+same run and listed compactly at the end of the line under "workloads" as
+[value, roofline fraction, kernel ms] (decode in GB/s of algorithmic bytes:
+Q + visible K/V rows + O + LSE; the backward in TFLOP/s of its five GEMMs,
+2*(3*Dqk+2*Dv)*#visible(i,j)); their full records go to stderr as one JSON line.
 
 Timing: W untimed steps, then K steps each bracketed by CUDA events on the
 launching stream, with an L2 flush (a 512 MB write) before every timed step
 and a barrier + synchronize around the timed region; max over ranks.
 `--impl reference` times the fp64 CPU oracle on a bounded sample instead.
-With N > 1 (torchrun), every rank runs an independent replica of the
-workload (the path needs no exchange); value = all ranks' work / max time.
+With N > 1 every rank runs an independent replica of the workload (the path
+needs no exchange); value = all ranks' work / max time. Started with
+`--gpus N` outside torchrun, the script re-launches itself under
+torch.distributed.run with N processes. `--dry-run` skips the GPU work and
+only exercises the launch and the rank helpers (gloo; a CPU check).
 """
 from __future__ import annotations
 
@@ -288,11 +295,13 @@ class Runner:
 
     def step_bwd(self):
         import ctypes
-        rc = self.fa.lib().fa_bwd(ctypes.byref(self.args), self.do.data_ptr(), self.dq.data_ptr(),
-                                  self.dk.data_ptr(), self.dv.data_ptr(), self.bws.data_ptr(), self.bws_bytes,
-                                  self.stream_ptr())
+        side, fork, join = self.fa.side_stream_objects(self.dev)
+        rc = self.fa.lib().fa_bwd_two_streams(ctypes.byref(self.args), self.do.data_ptr(), self.dq.data_ptr(),
+                                              self.dk.data_ptr(), self.dv.data_ptr(), self.bws.data_ptr(),
+                                              self.bws_bytes, self.stream_ptr(), ctypes.c_void_p(side.cuda_stream),
+                                              ctypes.c_void_p(fork.cuda_event), ctypes.c_void_p(join.cuda_event))
         if rc != 0:
-            raise RuntimeError(f"fa_bwd: {self.fa.fa_status_string(rc)}")
+            raise RuntimeError(f"fa_bwd_two_streams: {self.fa.fa_status_string(rc)}")
 
     def step_split(self):
         """decode as its two kernels, returning the events around the split-KV kernel."""
@@ -537,13 +546,23 @@ def main():
     ap.add_argument("--workload", default="causal", choices=list(inputs.WORKLOADS))
     ap.add_argument("--only", action="store_true", help="measure the headline workload only")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--dry-run", action="store_true",
+                    help="no GPU work: launch the ranks (gloo) and report the rank count only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and args.impl == "ours":
+        sys.exit(relaunch(args.gpus))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "ours" and world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}")
+
+    if args.dry_run:
+        dry_run(args, world, rank)
+        return
 
     if args.impl == "reference":
         if rank != 0:
@@ -565,10 +584,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    names = [args.workload] + ([] if args.only else [n for n in ("large_dense", "large_causal", "varlen", "decode",
-                                                                 "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
-                                                                 "chunk_single", "causal_bwd", "dense_bwd")
-                                                      if n != args.workload])
+    names = [args.workload] + ([] if args.only else [n for n in SECONDARY if n != args.workload])
     results = {}
     clocks = None
     for n in names:
@@ -618,9 +634,8 @@ def main():
         cpu = {"value": rate(work, secs * 1e3, args.workload), "unit": unit_of(args.workload),
                "cores": os.cpu_count(), "kind": "oracle", "sample": desc, "seconds": secs}
     if rank == 0:
-        metric = metric_name(args.workload)
         line = {
-            "metric": metric,
+            "metric": metric_name(args.workload),
             "value": p["value"],
             "unit": p["unit"],
             "n_gpus": world,
@@ -630,19 +645,62 @@ def main():
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16" if w0.kv_format == "bf16" else f"bf16 q/o, {w0.kv_format} K/V",
-            "data": "synthetic (seeded N(0,1) bf16, numpy PCG64)",
-            "config": {"workload": args.workload, "shape": workload_desc(w0), "l2": "flushed between steps",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "dtype": dtype_of(w0),
+            "data": DATA,
+            "config": config_of(w0, world),
             "roofline": p["roofline"],
             "cpu_baseline": cpu,
             "e2e": p["e2e"],
             "gpu_launches": p["launches_per_step"] * args.steps,
             "clocks": clocks,
-            "workloads": {n: {k: v for k, v in res.items() if k != "e2e"} for n, res in results.items()
-                          if n != args.workload},
         }
+        # every workload's full record on stderr; the compact list last on the line
+        sys.stderr.write(json.dumps({"workload_records": results}) + "\n")
+        line["workloads_fields"] = ["value (TFLOP/s; GB/s for decode*)", "roofline frac of measured peak",
+                                    "kernel ms"]
+        line["workloads"] = {n: [float(f"{res['value']:.5g}"), round(res["roofline"]["frac"], 4),
+                                 float(f"{res['kernel_ms']:.4g}")] for n, res in results.items()}
         print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+SECONDARY = ("dense", "tiny", "large_dense", "large_causal", "varlen", "decode", "decode_fp8", "decode_paged",
+             "causal_paged", "chunk_gqa", "chunk_single", "causal_bwd", "dense_bwd")
+DATA = "synthetic (seeded N(0,1) bf16, numpy PCG64)"
+
+
+def dtype_of(w):
+    return "bf16" if w.kv_format == "bf16" else f"bf16 q/o, {w.kv_format} K/V"
+
+
+def config_of(w, world):
+    """The `config` object of the line, the same for both arms."""
+    return {"workload": w.name, "shape": workload_desc(w), "l2": "flushed between steps",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def relaunch(n):
+    """Run this script under torch.distributed.run with n processes on this node."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def dry_run(args, world, rank):
+    """The launch path without the GPU: gloo ranks agree on a max over ranks and
+    rank 0 prints the line's rank fields."""
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("gloo", init_method="env://")
+    slowest = max_over_ranks(float(rank + 1), world)
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "max_over_ranks": slowest, "config": {"workload": args.workload}}))
     if world > 1:
         dist.destroy_process_group()
 
@@ -650,9 +708,20 @@ def main():
 def metric_name(name):
     if is_decode(name):
         return "split-KV decode KV GB/s"
+    w = inputs.workload(name)
+    if w.varlen:
+        shape = f"varlen {w.batch} seqs Hq={w.num_heads_q} Hkv={w.num_heads_kv} Dqk={w.head_dim_qk} Dv={w.head_dim_v}"
+    else:
+        d = f"D={w.head_dim_qk}" if w.head_dim_qk == w.head_dim_v else f"Dqk={w.head_dim_qk} Dv={w.head_dim_v}"
+        s = f"S={w.seqlen_q}" if w.seqlen_q == w.seqlen_k else f"Sq={w.seqlen_q} Sk={w.seqlen_k}"
+        shape = f"B={w.batch} Hq={w.num_heads_q} Hkv={w.num_heads_kv} {s} {d}"
+    mode = "causal" if w.causal else "dense"
+    if w.window_left >= 0:
+        mode += f" window {w.window_left}"
     if is_backward(name):
-        return "attn bwd TFLOP/s (dQ, dK, dV; B=2 Hq=32 Hkv=4 S=4096 D=128)"
-    return "attn fwd TFLOP/s (prefill, causal GQA B=2 Hq=32 Hkv=4 S=4096 D=128)"
+        return f"attn bwd TFLOP/s (dQ, dK, dV; {mode} {shape})"
+    gqa = "GQA " if w.num_heads_q != w.num_heads_kv else ""
+    return f"attn fwd TFLOP/s (prefill, {mode} {gqa}{shape})"
 
 
 def workload_desc(w):
@@ -697,8 +766,8 @@ def run_reference(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) bf16, numpy PCG64)",
-        "config": {"workload": args.workload, "shape": workload_desc(w)},
+        "data": DATA,
+        "config": config_of(w, 1),
         "cpu_baseline": {"value": value, "unit": unit_of(args.workload), "cores": os.cpu_count(), "kind": "oracle",
                          "sample": desc + " per step"},
         "e2e": {"value": value, "unit": unit_of(args.workload), "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

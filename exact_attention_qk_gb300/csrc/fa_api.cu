@@ -357,6 +357,7 @@ int run_decode(const fa_fwd_args* a, const Resolved& r, int ns, float* opart, fl
   // decode tiles: 64 keys of bf16, 128 keys of one-byte elements
   if (!kv_maps(a, r, fp8_kv(a) ? 128 : 64, &mk, &mv)) return FA_ERR_CUDA;
   cudaError_t e = launch_decode(p, a->head_dim_qk, a->head_dim_v, mk, mv, st);
+  if (e == cudaErrorInvalidConfiguration) return FA_ERR_UNSUPPORTED;   // grid beyond 65535 rows of CTAs
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -476,7 +477,7 @@ using namespace fa;
 
 extern "C" {
 
-int fa_abi_version(void) { return 201; }
+int fa_abi_version(void) { return 202; }
 
 const char* fa_status_string(int s) {
   switch (s) {
@@ -602,8 +603,10 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* a, void* stream) {
   if (no_work(a, r)) return FA_OK;
   rc = check_tensors(a, true);
   if (rc != FA_OK) return rc;
-  // the decode kernel for every shape here (prefill shapes are not split)
-  const int ns = (a->num_splits > 0 || decode_shaped(a, r)) ? resolve_splits(a, r, 0) : 1;
+  // decode shapes and fp8 caches only, on the decode kernel (whose grid is
+  // sized for few rows per KV head)
+  if (!decode_shaped(a, r) && !kv_special(a)) return FA_ERR_UNSUPPORTED;
+  const int ns = resolve_splits(a, r, 0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (ns <= 1) return run_decode(a, r, 1, nullptr, nullptr, st);
   const size_t rows = r.varlen ? static_cast<size_t>(a->total_q)
@@ -628,8 +631,8 @@ size_t fa_bwd_workspace_size(const fa_fwd_args* a) {
   return bwd_ws(a).total;
 }
 
-int fa_bwd(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv, void* workspace,
-           size_t workspace_bytes, void* stream) {
+static int bwd_impl(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                    size_t workspace_bytes, void* stream, const BwdSide& side) {
   Resolved r;
   int rc = check_bwd_args(a, &r);
   if (rc != FA_OK) return rc;
@@ -716,8 +719,24 @@ int fa_bwd(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv,
     return FA_ERR_CUDA;
   if (!has_q) mq = mdo = mk;
   if (!has_k) mk = mv = mq;
-  cudaError_t e = launch_bwd(p, d, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_bwd(p, d, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream), side);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_bwd(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+           size_t workspace_bytes, void* stream) {
+  const BwdSide none{nullptr, nullptr, nullptr};
+  return bwd_impl(a, dout, dq, dk, dv, workspace, workspace_bytes, stream, none);
+}
+
+int fa_bwd_two_streams(const fa_fwd_args* a, const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                       size_t workspace_bytes, void* stream, void* side_stream, void* fork_event,
+                       void* join_event) {
+  if (side_stream == nullptr || fork_event == nullptr || join_event == nullptr || side_stream == stream)
+    return FA_ERR_INVALID_ARG;
+  const BwdSide side{static_cast<cudaStream_t>(side_stream), static_cast<cudaEvent_t>(fork_event),
+                     static_cast<cudaEvent_t>(join_event)};
+  return bwd_impl(a, dout, dq, dk, dv, workspace, workspace_bytes, stream, side);
 }
 
 int fa_get_status(void* stream) {

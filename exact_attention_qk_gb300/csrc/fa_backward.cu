@@ -39,7 +39,6 @@
 // tensor memory and returns.
 #include <cuda_bf16.h>
 
-#include <mutex>
 
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
@@ -652,35 +651,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
-// A second stream per device for the dK/dV kernel, at the device's highest
-// priority, with the events that fork it from and join it back into the
-// caller's stream. Created on a device's first backward call.
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-
-std::mutex g_side_mu;
-
-SideStream* side_stream() {
-  static SideStream side[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  SideStream& x = side[dev];
-  if (x.s == nullptr) {
-    int lo = 0, hi = 0;
-    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
-    if (cudaStreamCreateWithPriority(&x.s, cudaStreamNonBlocking, hi) != cudaSuccess ||
-        cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess)
-      return nullptr;
-  }
-  return &x;
-}
-
 template <int D>
 cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const CUtensorMap& mdo, cudaStream_t stream) {
+                         const CUtensorMap& mdo, cudaStream_t stream, const BwdSide& side) {
   using Cfg = BwdCfg<D>;
   // batched: every sequence's lengths; varlen: the longest (CTAs past a
   // shorter sequence's end return at once)
@@ -695,29 +668,27 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtens
   e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 gq(p.batch * p.hq, mblocks), gk(p.batch * p.hkv, nblocks);
-  if (mblocks > 0 && nblocks > 0) {
+  if (mblocks > 0 && nblocks > 0 && side.stream != nullptr) {
     // The two kernels only share read-only inputs. dK/dV (few long CTAs under
-    // a causal mask, longest first) goes on the high-priority side stream so
-    // that its CTAs are placed first; the many short dQ CTAs fill the SMs it
-    // leaves idle. The caller's stream waits for both.
-    std::lock_guard<std::mutex> lock(g_side_mu);
-    SideStream* side = side_stream();
-    if (side == nullptr) return cudaErrorUnknown;
-    if ((e = cudaEventRecord(side->fork, stream)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(side->s, side->fork, 0)) != cudaSuccess) return e;
-    bwd_dkdv_kernel<D><<<gk, Cfg::THREADS, Cfg::SMEM, side->s>>>(mq, mk, mv, mdo, p);
+    // a causal mask, longest first) goes on the caller's second stream, which
+    // the caller gives a higher priority, so that its CTAs are placed first;
+    // the many short dQ CTAs fill the SMs it leaves idle. The caller's events
+    // fork the second stream from `stream` and join it back.
+    if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess) return e;
+    bwd_dkdv_kernel<D><<<gk, Cfg::THREADS, Cfg::SMEM, side.stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_dq_kernel<D><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(side->join, side->s)) != cudaSuccess) return e;
-    return cudaStreamWaitEvent(stream, side->join, 0);
+    if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(stream, side.join, 0);
+  }
+  if (nblocks > 0) {   // one stream: dK/dV, then dQ
+    bwd_dkdv_kernel<D><<<gk, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (mblocks > 0) {
     bwd_dq_kernel<D><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
-    return cudaGetLastError();
-  }
-  if (nblocks > 0) {
-    bwd_dkdv_kernel<D><<<gk, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -728,9 +699,9 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtens
 bool bwd_supported(int dk, int dv) { return (dk == 64 && dv == 64) || (dk == 128 && dv == 128); }
 
 cudaError_t launch_bwd(const BwdParams& p, int d, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream) {
-  if (d == 64) return launch_bwd_t<64>(p, mq, mk, mv, mdo, stream);
-  if (d == 128) return launch_bwd_t<128>(p, mq, mk, mv, mdo, stream);
+                       const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream, const BwdSide& side) {
+  if (d == 64) return launch_bwd_t<64>(p, mq, mk, mv, mdo, stream, side);
+  if (d == 128) return launch_bwd_t<128>(p, mq, mk, mv, mdo, stream, side);
   return cudaErrorInvalidValue;
 }
 

@@ -655,9 +655,11 @@ cudaError_t launch_decode_t(const FwdParams& p, const CUtensorMap& mk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   // packed rows (query rows x heads per KV head) in chunks of kRows over grid.y
-  const int rows = p.max_seqlen_q * p.r;
-  const int chunks = (rows + kRows - 1) / kRows;
-  dim3 grid(p.num_splits, p.hkv * chunks, p.batch);
+  const long long rows = static_cast<long long>(p.max_seqlen_q) * p.r;
+  const long long chunks = (rows + kRows - 1) / kRows;
+  // grid.y and grid.z are limited to 65535 (long fp8 prefills can exceed it)
+  if (p.hkv * chunks > 65535 || p.batch > 65535) return cudaErrorInvalidConfiguration;
+  dim3 grid(p.num_splits, static_cast<unsigned>(p.hkv * chunks), p.batch);
   kern<<<grid, kDecThreads, C::SMEM, stream>>>(mk, mv, p);
   return cudaGetLastError();
 }

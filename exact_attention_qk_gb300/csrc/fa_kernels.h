@@ -91,8 +91,15 @@ struct BwdParams {
 __host__ __device__ inline int64_t bwd_ws_row0(const int* cu_seqlens_q, int b) {
   return ((int64_t(cu_seqlens_q[b]) + 132 * int64_t(b) + 3) / 4) * 4;
 }
+// Optional second stream of the caller for the dK/dV kernel, with the two
+// events that fork it from and join it back into the main stream (all three
+// owned by the caller). stream == nullptr: every kernel on the main stream.
+struct BwdSide {
+  cudaStream_t stream;
+  cudaEvent_t fork, join;
+};
 cudaError_t launch_bwd(const BwdParams& p, int d, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream);
+                       const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream, const BwdSide& side);
 bool bwd_supported(int dk, int dv);
 
 struct CombineParams {

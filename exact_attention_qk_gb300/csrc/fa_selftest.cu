@@ -187,11 +187,13 @@ __global__ void __launch_bounds__(64, 1) never_kernel(int* status, int* report, 
   __shared__ uint64_t bar_a, bar_b;
   __shared__ uint32_t slot;
   __shared__ volatile int abort_flag;
+  __shared__ int own_status;   // warp 1's status word (it must stay untouched)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&bar_a, 1);
     mbar_init(&bar_b, 1);
     abort_flag = 0;
+    own_status = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -207,10 +209,9 @@ __global__ void __launch_bounds__(64, 1) never_kernel(int* status, int* report, 
       report[0] = mbar_wait(&bar_a, 0, g) ? 0 : 1;
     } else {
       // a much longer limit: only the abort raised by warp 0 can end this wait early
-      int dummy = 0;
-      const WaitGuard g{&abort_flag, &dummy, timeout_ns * 1000ull};
+      const WaitGuard g{&abort_flag, &own_status, timeout_ns * 1000ull};
       const bool r = mbar_wait(&bar_b, 0, g);
-      report[1] = (!r && dummy == 0) ? 1 : 0;
+      report[1] = (!r && own_status == 0) ? 1 : 0;
     }
   }
   tc_fence_before();

@@ -104,6 +104,8 @@ _lib.fa_fwd_decode_noalloc.argtypes = [_P, _vp]
 _lib.fa_fwd_decode_noalloc.restype = ctypes.c_int
 _lib.fa_bwd.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
 _lib.fa_bwd.restype = ctypes.c_int
+_lib.fa_bwd_two_streams.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]
+_lib.fa_bwd_two_streams.restype = ctypes.c_int
 _lib.fa_bwd_workspace_size.argtypes = [_P]
 _lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
 _lib.fa_abi_version.argtypes = []
@@ -270,13 +272,35 @@ def fa_bwd_workspace_size(args: FwdArgs) -> int:
     return int(_lib.fa_bwd_workspace_size(ctypes.byref(args)))
 
 
-def fa_bwd(q, k, v, out, lse, dout, dq=None, dk=None, dv=None, *, workspace=None, stream=None, **kw):
+_SIDE = {}
+
+
+def side_stream_objects(device) -> tuple:
+    """A high-priority torch stream and two events per device, made once and
+    reused by fa_bwd(concurrent=True): PyTorch owns them, not the library."""
+    idx = torch.device(device).index
+    if idx is None:
+        idx = torch.cuda.current_device()
+    if idx not in _SIDE:
+        with torch.cuda.device(idx):
+            side = torch.cuda.Stream(priority=-1)
+            fork, join = torch.cuda.Event(), torch.cuda.Event()
+            fork.record(side)       # torch creates the CUDA event at its first record
+            join.record(side)
+            _SIDE[idx] = (side, fork, join)
+    return _SIDE[idx]
+
+
+def fa_bwd(q, k, v, out, lse, dout, dq=None, dk=None, dv=None, *, workspace=None, stream=None,
+           concurrent=True, **kw):
     """dQ, dK, dV of the forward (q, k, v) -> (out, lse), given dO.
 
     Batched or packed varlen layout (pass the forward's cu_seqlens_q/k and
     max_seqlen_q/k). out and lse are the forward's results; dout has out's
     shape and strides; dq / dk / dv (allocated when None) take q's / k's / v's.
     kw: the forward's mask, scale and varlen keywords (see make_args).
+    concurrent: run dK/dV on a second (torch-owned, high-priority) stream
+    alongside dQ (fa_bwd_two_streams); otherwise every kernel on `stream`.
     Deterministic: the same inputs give the same bits.
     """
     if dq is None:
@@ -294,8 +318,14 @@ def fa_bwd(q, k, v, out, lse, dout, dq=None, dk=None, dv=None, *, workspace=None
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = _ptr(workspace) if need > 0 else None
     ws_bytes = workspace.numel() * workspace.element_size() if need > 0 else 0
-    _check(_lib.fa_bwd(ctypes.byref(args), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), ws_ptr, ws_bytes,
-                       _vp(_stream_handle(stream))), "fa_bwd")
+    if concurrent:
+        side, fork, join = side_stream_objects(q.device)
+        _check(_lib.fa_bwd_two_streams(ctypes.byref(args), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), ws_ptr,
+                                       ws_bytes, _vp(_stream_handle(stream)), _vp(side.cuda_stream),
+                                       _vp(fork.cuda_event), _vp(join.cuda_event)), "fa_bwd_two_streams")
+    else:
+        _check(_lib.fa_bwd(ctypes.byref(args), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), ws_ptr, ws_bytes,
+                           _vp(_stream_handle(stream))), "fa_bwd")
     return dq, dk, dv
 
 

@@ -15,6 +15,7 @@ prefill, a large head dim, varlen packing with a sliding window and the
 
   tiny     B=1  Hq=Hkv=2  Sq=Sk=128  D=64, dense
   causal   B=2  Hq=32 Hkv=4  Sq=Sk=4096  D=128, causal
+  dense    the causal shape (and the same draws) without a mask
   large    B=1  Hq=16 Hkv=2  Sq=Sk=8192  D=256, dense and causal, scale 1/16
   varlen   16 sequences, lengths uniform in [256, 8192], Hq=Hkv=16,
            Dqk=192, Dv=128, causal, window_left=1024
@@ -284,8 +285,9 @@ def decode_seqused() -> np.ndarray:
 def workload(name: str) -> Workload:
     if name == "tiny":
         return batched("tiny", 1, 1, 128, 128, 2, 2, 64, 64)
-    if name == "causal":
-        return batched("causal", 2, 2, 4096, 4096, 32, 4, 128, 128, causal=True)
+    if name in ("causal", "dense"):
+        # the causal GQA prefill and its unmasked twin (the same q, k, v draws)
+        return batched(name, 2, 2, 4096, 4096, 32, 4, 128, 128, causal=(name == "causal"))
     if name in ("large_dense", "large_causal"):
         return batched(name, 3, 1, 8192, 8192, 16, 2, 256, 256, scale=1.0 / 16,
                        causal=(name == "large_causal"))
@@ -324,6 +326,6 @@ def workload(name: str) -> Workload:
     raise KeyError(name)
 
 
-WORKLOADS = ("tiny", "causal", "large_dense", "large_causal", "varlen", "decode", "decode_small",
+WORKLOADS = ("tiny", "causal", "dense", "large_dense", "large_causal", "varlen", "decode", "decode_small",
              "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
              "decode_fp8_small", "decode_paged_small", "causal_bwd", "dense_bwd", "chunk_single")

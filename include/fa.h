@@ -197,19 +197,24 @@ int fa_combine(const float* out_partial, const float* lse_partial, int num_split
  * fa_fwd_decode_noalloc - split-KV decode plus combine, like fa_fwd on a
  * decode-shaped problem, but with no workspace argument: the fp32 split
  * partials live in a fixed array inside the library (FA_NOALLOC_SCRATCH_BYTES
- * per GPU, reserved when the library is loaded and held until the process
- * exits). The pages have no counterpart of this entry point; it exists for
- * callers that cannot allocate device memory at the point of the call, for
- * example code running while its stream is captured into a CUDA graph (where
- * cudaMalloc is not allowed), engines whose device memory is owned by another
- * allocator they cannot reach, and latency-critical paths that must not take
- * the driver's allocation locks or its implicit synchronisation.
- * The caller still passes q/k/v/out/lse in args; args->num_splits is resolved as
- * in fa_fwd. Problems whose partials (num_splits * rows * Hq * (head_dim_v + 1)
+ * per GPU). The pages have no counterpart of this entry point. It exists for
+ * callers that cannot allocate device memory at the point of the call:
+ * engines whose device memory belongs to another allocator that they cannot
+ * reach from the call site, and latency-critical paths that must not take the
+ * driver's allocation locks or its implicit synchronisation.
+ * The array is reserved on each device when the library's module is loaded
+ * there, which under CUDA's default lazy module loading is the first call of
+ * any entry point of this library on that device (with
+ * CUDA_MODULE_LOADING=EAGER, when the library is loaded); it is held until the
+ * process exits. The first call of this entry point on each device also looks
+ * up the array's device address there (the device must be current); make
+ * that first call before any stream capture.
+ * The caller still passes q/k/v/out/lse in args. Only decode-shaped problems
+ * (seqlen_q * Hq/Hkv <= 16) and fp8 caches are served, on the decode kernel;
+ * other shapes return FA_ERR_UNSUPPORTED. args->num_splits is resolved as in
+ * fa_fwd. Problems whose partials (num_splits * rows * Hq * (head_dim_v + 1)
  * floats) exceed the array return FA_ERR_WORKSPACE before anything is launched.
  * No call allocates: it calls no cudaMalloc/cudaFree or allocating library routine.
- * The first call on each device looks up the array's device address there (the
- * device must be current); make that first call before any stream capture.
  * Every call on a device shares the one array: calls whose work overlaps on the
  * GPU (different streams without ordering between them) race and give wrong
  * results. Nothing in the array needs clearing: each call writes every partial
@@ -236,14 +241,30 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
  * workspace: at least fa_bwd_workspace_size(args) bytes, 256-byte aligned
  *   (fp32 LSE * log2(e) and D for every padded query row). The call is
  *   deterministic: no atomics, the same inputs give the same bits.
- * The dK/dV kernel runs on a second stream of the library's (one per device,
- * created by the device's first fa_bwd call, highest priority), forked from
- * and joined back into `stream` with events: to the caller the work is
- * ordered on `stream` alone, and a captured `stream` captures both. Make a
- * device's first fa_bwd call outside stream capture.
+ * Every kernel runs on `stream`, one after the other (preprocess, dK/dV, dQ).
  */
 int fa_bwd(const fa_fwd_args* args, const void* dout, void* dq, void* dk, void* dv, void* workspace,
            size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd_two_streams - fa_bwd with the dK/dV kernel on a second stream of the
+ * caller's, concurrent with the dQ kernel on `stream` (the two only share
+ * read-only inputs). side_stream is a cudaStream_t and fork_event /
+ * join_event are cudaEvent_t (created by the caller, e.g. with
+ * cudaEventDisableTiming), all passed as void*. The call records fork_event
+ * on `stream` after the preprocess, makes side_stream wait for it, launches
+ * dK/dV there, records join_event on side_stream and makes `stream` wait for
+ * it: to the caller the whole backward is ordered on `stream`. Give
+ * side_stream a higher priority than `stream`, so that the long dK/dV CTAs
+ * are placed first and the short dQ CTAs fill the SMs they leave idle.
+ * The library creates no stream or event. Both events are re-recorded by
+ * every call: calls that share them must be issued from one host thread.
+ * Returns FA_ERR_INVALID_ARG when side_stream or an event is NULL or
+ * side_stream == stream; otherwise as fa_bwd.
+ */
+int fa_bwd_two_streams(const fa_fwd_args* args, const void* dout, void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes, void* stream, void* side_stream,
+                       void* fork_event, void* join_event);
 
 /* Bytes of workspace fa_bwd needs for args (0 when fa_bwd would reject args). */
 size_t fa_bwd_workspace_size(const fa_fwd_args* args);
@@ -252,19 +273,42 @@ size_t fa_bwd_workspace_size(const fa_fwd_args* args);
 size_t fa_workspace_size(const fa_fwd_args* args);
 
 /*
- * Split count fa_fwd uses when args->num_splits == 0. Decode-shaped problems
- * (seqlen_q * Hq/Hkv <= 16) are split into chunks of about 2048 keys so that
- * sequences of very different length spread over the SMs. Prefill shapes with
- * a bf16 cache are split only when their grid of 256-row (128 for head dim
- * 256) query tiles would fill at most half of the SMs: then into
- * min(num_sms / tiles, key blocks / 4, 32) splits of whole 128-key blocks,
- * run by the prefill kernel and merged by the combine. Others are not split.
+ * Split count fa_fwd uses when args->num_splits == 0.
+ * The pages' policies, and where this one departs from them:
+ *   "mslk/attention/flash_attn/interface.py", `num_splits_heuristic`: no split
+ *     when a sequence has at most 4 key blocks, else
+ *     min(num_SMs / total_mblocks, max_splits, key blocks), that is, split
+ *     only a grid that leaves SMs idle. The prefill rule below is this one
+ *     (at least 4 key blocks per split, at most 32 splits, counted in the
+ *     256-row tiles of this library's prefill kernel) with one change: a grid
+ *     that fills more than half of the SMs is not split, because the fp32
+ *     partials and the combine cost more than the idle SMs.
+ *   "mslk/attention/fmha/triton_splitk.py", `get_split_k` / `split_size`:
+ *     for decode, the splits follow the key length (about Mk / 128-key
+ *     chunks, halved until they fit) and each split covers
+ *     ceil(Mk / split_k) keys. The decode rule below also splits by key
+ *     length, with a longer chunk: about 2048 keys per split, doubled while
+ *     (sequences x KV heads x row chunks x splits) < 2 x num_sms, at most 128.
+ *     `num_splits_heuristic` would return 1 on a decode batch whose KV heads
+ *     alone fill the SMs; with seqused_k spread 16x between sequences that
+ *     leaves a long tail of the longest sequences, so the fixed key length
+ *     wins there.
+ * Decode-shaped problems are those with seqlen_q * Hq/Hkv <= 16. Prefill
+ * shapes with a bf16 cache split into whole 128-key blocks and run on the
+ * prefill kernel, merged by the combine. fp8 caches follow the decode rule.
  * num_sms <= 0 queries the current device.
  */
 int fa_num_splits(const fa_fwd_args* args, int num_sms);
 
-/* Keys per split, L = 64 * ceil(ceil(Kmax / num_splits) / 64), Kmax = seqlen_k
- * (batched) or max_seqlen_k (varlen). */
+/*
+ * Keys per split of the decode kernel and of fa_fwd_splitkv:
+ * L = 64 * ceil(ceil(Kmax / num_splits) / 64), Kmax = seqlen_k (batched),
+ * max_seqlen_k (varlen) or max_pages_per_seq * page_size (paged); split s
+ * covers key positions [s*L, (s+1)*L). This is the split-K page's
+ * `split_size` = ceil(Mk / split_k) ("mslk/attention/fmha/triton_splitk.py"),
+ * rounded up to the decode kernel's 64-key tile so that no tile straddles two
+ * splits. Returns 0 when args are invalid.
+ */
 int fa_split_len(const fa_fwd_args* args, int num_splits);
 
 /*
@@ -281,7 +325,8 @@ void fa_set_wait_timeout_ns(uint64_t ns);
 const char* fa_status_string(int status);
 
 /* ABI version (major*100 + minor): 200 since fa_fwd_args gained the KV-cache
- * fields, 201 since fa_bwd. */
+ * fields, 201 since fa_bwd, 202 since fa_bwd_two_streams (fa_bwd itself runs
+ * on the caller's stream alone). */
 int fa_abi_version(void);
 
 #ifdef __cplusplus

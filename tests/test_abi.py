@@ -59,7 +59,7 @@ def test_struct_layout_matches_header(fa, tmp_path):
     assert int(got["sizeof"]) == ctypes.sizeof(fa.FwdArgs)
     for n in fields:
         assert int(got[n]) == getattr(fa.FwdArgs, n).offset, n
-    assert fa.fa_abi_version() == 201
+    assert fa.fa_abi_version() == 202
 
 
 def _args(fa, **over):
@@ -208,3 +208,14 @@ def test_backward_varlen_workspace(fa):
     assert fa.fa_bwd_workspace_size(a) == 2 * per
     # accepted: the next check is the missing workspace
     assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 4
+
+
+def test_bwd_two_streams_needs_the_callers_stream_and_events(fa):
+    a = _args(fa, lse=0x70000)
+    call = fa.lib().fa_bwd_two_streams
+    # a missing second stream or event, or the second stream equal to the first: refused before any launch
+    assert call(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None, None, 0x1, 0x2) == 1
+    assert call(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None, 0x5, None, 0x2) == 1
+    assert call(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, 0x5, 0x5, 0x1, 0x2) == 1
+    # otherwise the same checks as fa_bwd (workspace missing)
+    assert call(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None, 0x5, 0x1, 0x2) == 4

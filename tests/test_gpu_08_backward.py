@@ -30,7 +30,7 @@ TOL_MEAN_REL = 4e-3
 TOL_CANCELLED_ZERO = 1e-4
 
 
-def run_bwd(w, do_bits):
+def run_bwd(w, do_bits, concurrent=True):
     from exact_attention_qk_gb300 import fa
     q, k, v, do = gu.to_dev(w.q), gu.to_dev(w.k), gu.to_dev(w.v), gu.to_dev(do_bits)
     kw = dict(gu.kw_of(w))
@@ -38,7 +38,7 @@ def run_bwd(w, do_bits):
         kw.update(cu_seqlens_q=gu.i32(w.cu_seqlens_q), cu_seqlens_k=gu.i32(w.cu_seqlens_k),
                   max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k)
     o, lse = fa.fa_fwd(q, k, v, **kw)
-    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, **kw)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, concurrent=concurrent, **kw)
     assert fa.fa_get_status() == fa.FA_OK
     return dq, dk, dv
 
@@ -165,6 +165,18 @@ def test_deterministic():
     b = run_bwd(w, do)
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_one_stream_equals_two_streams():
+    """fa_bwd (every kernel on the caller's stream) and fa_bwd_two_streams (dK/dV
+    on the caller's second stream) run the same kernels: the same bits."""
+    w = inputs.batched("bwd1s", 436, 2, 700, 650, 8, 2, 128, 128, causal=True, window_left=200)
+    do = inputs.grad_out(w)
+    a = run_bwd(w, do, concurrent=False)
+    b = run_bwd(w, do, concurrent=True)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+    print(check_bwd(w))
 
 
 @pytest.mark.parametrize("d", [64, 128])

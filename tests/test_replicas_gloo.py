@@ -54,3 +54,22 @@ def test_single_rank_is_identity():
     assert bench.max_over_ranks(1.5, 1) == 1.5
     assert bench.job_rate(1e12, 1.0, 1, "causal") == pytest.approx(1000.0)
     assert bench.job_rate(2e9, 1.0, 1, "decode") == pytest.approx(2000.0)
+
+
+def test_gpus_flag_launches_that_many_ranks():
+    """`bench.py --gpus 2` started outside torchrun re-launches itself with two
+    ranks (torch.distributed.run); --dry-run keeps it on the CPU (gloo)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--dry-run",
+                        "--steps", "4", "--warmup", "3"], capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2
+    assert d["max_over_ranks"] == 2.0       # ranks report 1 and 2; the max wins
