@@ -59,8 +59,7 @@ struct PrefillCfg {
   static constexpr int OFF_OST = OFF_V + VST * V_BYTES;
   static constexpr int OST_BYTES = OSTAGE ? 2 * kChunkBytes : 0;
   static constexpr int OFF_BAR = OFF_OST + OST_BYTES;
-  static constexpr int REL = (KST > VST) ? KST : VST;
-  static constexpr int NBAR = 2 * 2 + 2 * KST + 3 * VST + 2 + 2 + 2 + 2 + REL + 1;
+  static constexpr int NBAR = 2 * 2 + 2 * KST + 3 * VST + 2 + 2 + 2 + 2 + 2 + 2;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // at least half the SM's shared memory, so one CTA (the one that owns all
   // 512 TMEM columns) is resident per SM
@@ -70,6 +69,7 @@ struct PrefillCfg {
   static constexpr int MMA_WARP = 4 * NSM;
   static constexpr int TMA_QK_WARP = MMA_WARP + 1;
   static constexpr int TMA_V_WARP = MMA_WARP + 2;
+  static constexpr int PV_WARP = MMA_WARP + 3;   // NQ == 2: issues the P.V GEMMs
   static constexpr int THREADS = 32 * 4 * (NSM + 1);
   // register split (NQ == 2): 256 x 200 + 128 x 104 (or 256 x 192 + 128 x 120) = 384 x 168 at launch
   static constexpr int REG_SOFTMAX = (DK == 192) ? 192 : 200;
@@ -221,8 +221,8 @@ struct Bars {
   uint64_t* p_full;    // [2] per S slot
   uint64_t* o_bar;     // [2] per O: one phase per P.V
   uint64_t* o_empty;   // [2] per O: epilogue done reading
-  uint64_t* kv_rel;    // [REL] NQ == 2: K and V of a block released together
-  uint64_t* drain;
+  uint64_t* pv_done;   // [2] per S slot (NQ == 2): the P.V reading its P has completed
+  uint64_t* drain;     // [2] per issuing thread
 };
 
 template <class Cfg>
@@ -240,8 +240,8 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   B.p_full = b; b += 2;
   B.o_bar = b; b += 2;
   B.o_empty = b; b += 2;
-  B.kv_rel = b; b += Cfg::REL;
-  B.drain = b; b += 1;
+  B.pv_done = b; b += 2;
+  B.drain = b; b += 2;
   return B;
 }
 
@@ -299,6 +299,8 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       mbar_init(&B.p_full[i], 4);      // one arrival per softmax warp
       mbar_init(&B.o_bar[i], 1);
       mbar_init(&B.o_empty[i], 4);
+      mbar_init(&B.pv_done[i], 1);
+      mbar_init(&B.drain[i], 1);
     }
     for (int i = 0; i < Cfg::KST; ++i) {
       mbar_init(&B.k_full[i], 1);
@@ -309,8 +311,6 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       mbar_init(&B.v_empty[i], 1);
       mbar_init(&B.v_fixed[i], 1);
     }
-    for (int i = 0; i < Cfg::REL; ++i) mbar_init(&B.kv_rel[i], 1);
-    mbar_init(B.drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -341,15 +341,11 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       }
       uint32_t kc = 0, qc[2] = {0, 0};
       bool ok = true;
-      // Block j's K and V tiles may be overwritten once block j is released:
-      // NQ == 2 releases K(j) and V(j) together (one commit, barrier ring of
-      // REL slots); NQ == 1 releases K and V separately on their own rings.
-      auto wait_release = [&](uint32_t j, uint64_t* own_ring, int own_depth) -> bool {
-        if constexpr (NQ == 2) {
-          return mbar_wait(&B.kv_rel[j % Cfg::REL], (j / Cfg::REL) & 1, guard);
-        } else {
-          return mbar_wait(&own_ring[j % own_depth], (j / own_depth) & 1, guard);
-        }
+      // K(j) and V(j) are released separately, each by one commit after the
+      // last MMA that reads it (K(j) after S(j, *), V(j) after P.V(j, *)), so
+      // the next tile of a ring loads as early as possible.
+      auto wait_release = [&](uint32_t j, uint64_t* ring, int depth) -> bool {
+        return mbar_wait(&ring[j % depth], (j / depth) & 1, guard);
       };
       for (int k = 0; ok; ++k) {
         Tile T;
@@ -450,9 +446,18 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           drain_wait(&B.v_full[u % nst], (u / nst) & 1, p.timeout_ns);
       }
     }
-  } else if (warp == Cfg::MMA_WARP) {
-    // ================= MMA issuer (one thread) =================
+  } else if (warp == Cfg::MMA_WARP || (NQ == 2 && warp == Cfg::PV_WARP)) {
+    // ================= MMA issuers =================
+    // A tcgen05.mma takes about 50 cycles to issue and the tensor queue holds
+    // only a few instructions, while an M=128 N=128 K=16 MMA runs 64 cycles:
+    // one thread issuing every GEMM of the two-tile kernels (plus its waits
+    // and commits) cannot keep the pipe busy. So with NQ == 2 lane 0 of the
+    // MMA warp issues S = Q K^T and lane 0 of the P.V warp (another SM
+    // sub-partition) issues O += P V. S(n-1, t) overwrites the TMEM columns
+    // P(n, t) occupies, so it waits until the P.V reading them has completed
+    // (pv_done[t]). The head-dim-256 kernel keeps one issuing thread.
     if (lane == 0) {
+      const bool s_role = warp == Cfg::MMA_WARP;
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(kBM, DV, false, true);
       const uint32_t q_base = smem_u32(smem + Cfg::OFF_Q);
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       };
 
       uint32_t kc = 0, vc = 0, qw[2] = {0, 0}, pw[2] = {0, 0}, ou[2] = {0, 0};
-      uint32_t rel = 0;   // NQ == 2: blocks released so far
+      uint32_t sc[2] = {0, 0};   // NQ == 2: S GEMMs issued per slot (one pv_done phase each)
       uint32_t jc = 0;   // NQ == 1: jobs so far (S slot = job parity)
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -531,88 +536,61 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         };
 
         if constexpr (NQ == 2) {
-          // Q tile s takes part in key block n when lo[s] <= n < hi[s]. The
-          // issuing thread runs straight-line code per block: every branch,
-          // wait and commit between two MMA groups leaves the tensor pipe idle.
-          const int lo0 = has_work(R[0]) ? R[0].nlo : INT32_MAX, hi0 = has_work(R[0]) ? R[0].nhi : INT32_MIN;
-          const int lo1 = has_work(R[1]) ? R[1].nlo : INT32_MAX, hi1 = has_work(R[1]) ? R[1].nhi : INT32_MIN;
-          if (hi0 > lo0) {
-            if (!mbar_wait(&B.q_full[0], qw[0] & 1, guard)) { ok = false; break; }
-            ++qw[0];
-          }
-          if (hi1 > lo1) {
-            if (!mbar_wait(&B.q_full[1], qw[1] & 1, guard)) { ok = false; break; }
-            ++qw[1];
-          }
-          // prologue: S for the first block of each participating Q tile
-          {
-            const int n0 = nhi - 1, st = kc % Cfg::KST;
-            if (!mbar_wait(&B.k_full[st], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
-            if (n0 >= lo0 && n0 < hi0) {
-              issue_s(0, 0, st);
-              mma_commit(&B.s_full[0]);
-              if (n0 == lo0) mma_commit(&B.q_empty[0]);
+          // Q tile t takes part in key block n when lo[t] <= n < hi[t]
+          const int lo[2] = {has_work(R[0]) ? R[0].nlo : INT32_MAX, has_work(R[1]) ? R[1].nlo : INT32_MAX};
+          const int hi[2] = {has_work(R[0]) ? R[0].nhi : INT32_MIN, has_work(R[1]) ? R[1].nhi : INT32_MIN};
+          if (s_role) {
+            // ---- S = Q K^T for every block, both Q tiles; K(n) released after S(n, *)
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (hi[t] > lo[t]) {
+                if (!mbar_wait(&B.q_full[t], qw[t] & 1, guard)) { ok = false; break; }
+                ++qw[t];
+              }
             }
-            if (n0 >= lo1 && n0 < hi1) {
-              issue_s(1, 1, st);
-              mma_commit(&B.s_full[1]);
-              if (n0 == lo1) mma_commit(&B.q_empty[1]);
-            }
-            ++kc;
-          }
-          // the O accumulators are free once the previous tile's epilogue read them
-          if (hi0 > lo0) {
-            if (ou[0] > 0 && !mbar_wait(&B.o_empty[0], (ou[0] - 1) & 1, guard)) { ok = false; break; }
-            ++ou[0];
-          }
-          if (hi1 > lo1) {
-            if (ou[1] > 0 && !mbar_wait(&B.o_empty[1], (ou[1] - 1) & 1, guard)) { ok = false; break; }
-            ++ou[1];
-          }
-          for (int n = nhi - 1; n >= nlo; --n) {
-            const int vst = vc % Cfg::VST, kst = kc % Cfg::KST;
-            const bool has_next = n - 1 >= nlo;
-            if (!mbar_wait(&B.v_full[vst], (vc / Cfg::VST) & 1, guard)) { ok = false; break; }
-            if (!wait_fix(n, vst, T)) { ok = false; break; }
-            const int steps = pv_steps<TAIL>(T, n);
-            bool k_ready = false;   // K(n-1) is waited for just before its first use
-            // Q tile 0: P.V of block n, then S of block n-1 into the same slot
-            if (n >= lo0 && n < hi0) {
-              if (!mbar_wait(&B.p_full[0], pw[0] & 1, guard)) { ok = false; break; }
-              ++pw[0];
-              tc_fence_after();
-              issue_pv(0, 0, vst, n != hi0 - 1, steps);
-              if (n == lo0) mma_commit(&B.o_bar[0]);   // O[0] complete for this tile
-            }
-            if (has_next && n - 1 >= lo0 && n - 1 < hi0) {
-              if (!mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
-              k_ready = true;
-              issue_s(0, 0, kst);
-              mma_commit(&B.s_full[0]);
-              if (n - 1 == lo0) mma_commit(&B.q_empty[0]);
-            }
-            // Q tile 1
-            if (n >= lo1 && n < hi1) {
-              if (!mbar_wait(&B.p_full[1], pw[1] & 1, guard)) { ok = false; break; }
-              ++pw[1];
-              tc_fence_after();
-              issue_pv(1, 1, vst, n != hi1 - 1, steps);
-              if (n == lo1) mma_commit(&B.o_bar[1]);
-            }
-            if (has_next && n - 1 >= lo1 && n - 1 < hi1) {
-              if (!k_ready && !mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
-              k_ready = true;
-              issue_s(1, 1, kst);
-              mma_commit(&B.s_full[1]);
-              if (n - 1 == lo1) mma_commit(&B.q_empty[1]);
-            }
-            // every MMA reading K(n) and V(n) is issued: release block n
-            mma_commit(&B.kv_rel[rel % Cfg::REL]);
-            ++rel;
-            ++vc;
-            if (has_next) {
-              if (!k_ready && !mbar_wait(&B.k_full[kst], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
+            if (!ok) break;
+            for (int n = nhi - 1; n >= nlo; --n) {
+              const int st = kc % Cfg::KST;
+              if (!mbar_wait(&B.k_full[st], (kc / Cfg::KST) & 1, guard)) { ok = false; break; }
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (n < lo[t] || n >= hi[t]) continue;
+                // the previous P of this slot has been read by its P.V
+                if (sc[t] > 0 && !mbar_wait(&B.pv_done[t], (sc[t] - 1) & 1, guard)) { ok = false; break; }
+                tc_fence_after();
+                issue_s(t, t, st);
+                mma_commit(&B.s_full[t]);
+                if (n == lo[t]) mma_commit(&B.q_empty[t]);
+                ++sc[t];
+              }
+              if (!ok) break;
+              mma_commit(&B.k_empty[st]);
               ++kc;
+            }
+          } else {
+            // ---- O += P V for every block, both Q tiles; V(n) released after P.V(n, *)
+            for (int n = nhi - 1; n >= nlo; --n) {
+              const int vst = vc % Cfg::VST;
+              if (!mbar_wait(&B.v_full[vst], (vc / Cfg::VST) & 1, guard)) { ok = false; break; }
+              if (!wait_fix(n, vst, T)) { ok = false; break; }
+              const int steps = pv_steps<TAIL>(T, n);
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (n < lo[t] || n >= hi[t]) continue;
+                if (n == hi[t] - 1) {   // O[t] free once the previous tile's epilogue read it
+                  if (ou[t] > 0 && !mbar_wait(&B.o_empty[t], (ou[t] - 1) & 1, guard)) { ok = false; break; }
+                  ++ou[t];
+                }
+                if (!mbar_wait(&B.p_full[t], pw[t] & 1, guard)) { ok = false; break; }
+                ++pw[t];
+                tc_fence_after();
+                issue_pv(t, t, vst, n != hi[t] - 1, steps);
+                mma_commit(&B.pv_done[t]);
+                if (n == lo[t]) mma_commit(&B.o_bar[t]);   // O[t] complete for this tile
+              }
+              if (!ok) break;
+              mma_commit(&B.v_empty[vst]);
+              ++vc;
             }
           }
         } else {
@@ -652,8 +630,9 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         }
       }
       // wait for every MMA this thread issued before TMEM is released
-      mma_commit(B.drain);
-      drain_wait(B.drain, 0, p.timeout_ns);
+      uint64_t* drain = &B.drain[s_role ? 0 : 1];
+      mma_commit(drain);
+      drain_wait(drain, 0, p.timeout_ns);
     }
     __syncwarp();
   }
