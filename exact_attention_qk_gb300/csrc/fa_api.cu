@@ -465,7 +465,7 @@ BwdWs bwd_ws(const fa_fwd_args* a) {
 int check_bwd_args(const fa_fwd_args* a, Resolved* r) {
   const int rc = check_args(a, r);
   if (rc != FA_OK) return rc;
-  if (a->seqused_k != nullptr || a->page_table != nullptr || a->kv_format != FA_KV_BF16) return FA_ERR_UNSUPPORTED;
+  if (a->page_table != nullptr || a->kv_format != FA_KV_BF16) return FA_ERR_UNSUPPORTED;
   if (!bwd_supported(a->head_dim_qk, a->head_dim_v)) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -685,6 +685,7 @@ static int bwd_impl(const fa_fwd_args* a, const void* dout, void* dq, void* dk, 
   p.sq_pad = w.sq_pad;
   p.cu_seqlens_q = a->cu_seqlens_q;
   p.cu_seqlens_k = a->cu_seqlens_k;
+  p.seqused_k = a->seqused_k;
   p.total_q = r.varlen ? a->total_q : 0;
   p.ws_rows = w.ws_rows;
   if (r.varlen) {   // batch strides are ignored in the packed layout

@@ -79,6 +79,7 @@ struct BBars {
   uint64_t* ds_full;    // [2] per column half: dS written by its warpgroup (4 arrivals)
   uint64_t* acc_full;   // accumulators final
   uint64_t* drain;
+  uint64_t* k_fixed;    // dQ kernel, seqused_k: K rows past the used keys cleared
 };
 
 template <class Cfg>
@@ -94,6 +95,7 @@ __device__ __forceinline__ BBars carve(uint8_t* smem) {
   B.ds_full = b; b += 2;
   B.acc_full = b; b += 1;
   B.drain = b; b += 1;
+  B.k_fixed = b; b += 1;
   return B;
 }
 
@@ -112,6 +114,7 @@ __device__ __forceinline__ void init_bars(const BBars& B) {
   }
   mbar_init(B.acc_full, 1);
   mbar_init(B.drain, 1);
+  mbar_init(B.k_fixed, 1);
   fence_barrier_init();
 }
 
@@ -147,6 +150,16 @@ __device__ __forceinline__ void issue_ts_half(uint32_t d_tmem, uint32_t a_tmem, 
   }
 }
 
+// The same for the first `steps` (0..4) 16-deep slices of half h only.
+__device__ __forceinline__ void issue_ts_half_steps(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, int h,
+                                                    uint32_t idesc, bool acc, int steps) {
+  const uint64_t bd = sdesc_sw128(b_base, kChunk, 1024);
+  for (int k4 = 0; k4 < steps; ++k4) {
+    const int kk = h * 4 + k4;
+    mma_bf16_ts(d_tmem, a_tmem + h * 64 + k4 * 8, bd + ((kk * 16 * 128) >> 4), idesc, (acc || k4 > 0) ? 1u : 0u);
+  }
+}
+
 // 32 fp32 accumulator columns of one row, times f, to 64 bytes of bf16
 __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&o)[32], float f) {
   uint32_t w[16];
@@ -166,8 +179,11 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* dst, int d) {
 // One sequence of the call: its lengths, its first rows in q's and k's row
 // axes (0 when batched), the batch coordinate of the tensor maps and the
 // first workspace row of q head h.
+// sk: the keys that exist (seqused_k[b] when given); ska: the key rows the
+// sequence owns in k's row axis (its capacity), whose rows at or past sk the
+// dK/dV kernel sets to 0.
 struct BSeq {
-  int sq, sk, q_row0, k_row0, bc;
+  int sq, sk, ska, q_row0, k_row0, bc;
 };
 
 __device__ __forceinline__ BSeq bwd_seq(const BwdParams& p, int b) {
@@ -176,14 +192,15 @@ __device__ __forceinline__ BSeq bwd_seq(const BwdParams& p, int b) {
     S.q_row0 = p.cu_seqlens_q[b];
     S.sq = p.cu_seqlens_q[b + 1] - S.q_row0;
     S.k_row0 = p.cu_seqlens_k[b];
-    S.sk = p.cu_seqlens_k[b + 1] - S.k_row0;
+    S.ska = p.cu_seqlens_k[b + 1] - S.k_row0;
     S.bc = 0;
   } else {
     S.q_row0 = S.k_row0 = 0;
     S.sq = p.seqlen_q;
-    S.sk = p.seqlen_k;
+    S.ska = p.seqlen_k;
     S.bc = b;
   }
+  S.sk = p.seqused_k != nullptr ? min(p.seqused_k[b], S.ska) : S.ska;
   return S;
 }
 
@@ -233,7 +250,7 @@ __global__ void __launch_bounds__(1024) bwd_preprocess_kernel(const BwdParams p,
 }
 
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool TAIL>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                   const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
@@ -273,34 +290,65 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const WaitGuard guard{abort_flag, p.status, p.timeout_ns};
 
   if (warp == Cfg::TMA_WARP) {
-    if (lane == 0 && has) {
-      tma_prefetch_desc(&mapQ);
-      tma_prefetch_desc(&mapK);
-      tma_prefetch_desc(&mapV);
-      tma_prefetch_desc(&mapDO);
-      uint8_t* res = smem + Cfg::OFF_RES;
-      mbar_arrive_expect_tx(B.res_full, 2 * Cfg::T_BYTES);
-#pragma unroll
-      for (int c = 0; c < Cfg::CH; ++c) {
-        tma_load_4d(res + c * kChunk, &mapQ, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
-        tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapDO, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
-      }
-      uint32_t u = 0;
-      for (int n = nhi - 1; n >= nlo; --n, ++u) {
-        const int st = u % Cfg::ST;
-        if (u >= Cfg::ST && !mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard)) break;
-        uint8_t* dst = smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES;
-        mbar_arrive_expect_tx(&B.str_full[st], 2 * Cfg::T_BYTES);
+    // Lane 0 issues the copies. With seqused_k (TAIL), the whole warp clears
+    // the rows of the last, partly used key block from the used length up to
+    // the next 16-key step in shared memory: cache rows past seqused_k may
+    // hold anything (NaN), and dQ += dS K contracts over them up to that step
+    // (dS is 0 there, but 0 * NaN is not).
+    if (has) {
+      if (lane == 0) {
+        tma_prefetch_desc(&mapQ);
+        tma_prefetch_desc(&mapK);
+        tma_prefetch_desc(&mapV);
+        tma_prefetch_desc(&mapDO);
+        uint8_t* res = smem + Cfg::OFF_RES;
+        mbar_arrive_expect_tx(B.res_full, 2 * Cfg::T_BYTES);
 #pragma unroll
         for (int c = 0; c < Cfg::CH; ++c) {
-          tma_load_4d(dst + c * kChunk, &mapK, &B.str_full[st], c * 64, S.k_row0 + n * kB, g, S.bc);
-          tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapV, &B.str_full[st], c * 64, S.k_row0 + n * kB, g, S.bc);
+          tma_load_4d(res + c * kChunk, &mapQ, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
+          tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapDO, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
+        }
+      }
+      constexpr unsigned wmask = TAIL ? 0xffffffffu : 1u;
+      uint32_t u = 0;
+      if (lane == 0 || TAIL) {
+        for (int n = nhi - 1; n >= nlo; --n, ++u) {
+          const int st = u % Cfg::ST;
+          uint8_t* dst = smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES;
+          bool w = true;
+          if (lane == 0) {
+            w = u < Cfg::ST || mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard);
+            if (w) {
+              mbar_arrive_expect_tx(&B.str_full[st], 2 * Cfg::T_BYTES);
+#pragma unroll
+              for (int c = 0; c < Cfg::CH; ++c) {
+                tma_load_4d(dst + c * kChunk, &mapK, &B.str_full[st], c * 64, S.k_row0 + n * kB, g, S.bc);
+                tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapV, &B.str_full[st], c * 64, S.k_row0 + n * kB, g,
+                            S.bc);
+              }
+            }
+          }
+          if (!__shfl_sync(wmask, w ? 1 : 0, 0)) break;
+          const int valid = S.sk - n * kB;
+          if (TAIL && valid < kB) {
+            if (!__all_sync(wmask, mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard))) break;
+            const int pieces = (min(kB, (valid + 15) & ~15) - valid) * Cfg::CH * 8;   // 16-byte pieces
+            for (int idx = lane; idx < pieces; idx += 32) {
+              const int row = valid + idx / (Cfg::CH * 8), rem = idx % (Cfg::CH * 8);
+              *reinterpret_cast<uint4*>(dst + (rem >> 3) * kChunk + row * 128 + (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp(wmask);
+            if (lane == 0) mbar_arrive(B.k_fixed);
+          }
         }
       }
       // drain the copies still in flight (only after an abort can any be)
-      for (uint32_t x = (u > (uint32_t)Cfg::ST ? u - Cfg::ST : 0); x < u; ++x)
-        drain_phase(&B.str_full[x % Cfg::ST], (x / Cfg::ST) & 1, p.timeout_ns);
-      drain_phase(B.res_full, 0, p.timeout_ns);
+      if (lane == 0) {
+        for (uint32_t x = (u > (uint32_t)Cfg::ST ? u - Cfg::ST : 0); x < u; ++x)
+          drain_phase(&B.str_full[x % Cfg::ST], (x / Cfg::ST) & 1, p.timeout_ns);
+        drain_phase(B.res_full, 0, p.timeout_ns);
+      }
     }
   } else if (warp == Cfg::MMA_WARP) {
     if (lane == 0 && has) {
@@ -329,10 +377,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           issue_ss(tmem, q_base, kv(u + 1), D, IDESC_S);
           mma_commit(B.s_full);
         }
+        // the last, partly used key block (seqused_k): K cleared up to the next
+        // 16-key step, and the contraction stops there
+        const int valid = S.sk - (nhi - 1 - static_cast<int>(u)) * kB;
+        const bool tail = TAIL && valid < kB;
+        if (tail && !mbar_wait(B.k_fixed, 0, guard)) { ok = false; break; }
+        const int steps = tail ? (valid + 15) / 16 : 8;
         for (int c = 0; c < 2; ++c) {
           if (!mbar_wait(&B.ds_full[c], u & 1, guard)) { ok = false; break; }
           tc_fence_after();
-          issue_ts_half(tmem + 256, tmem + 128, kv(u), c, IDESC_DQ, u > 0 || c > 0);   // dQ += dS_c K_c
+          if (!tail)
+            issue_ts_half(tmem + 256, tmem + 128, kv(u), c, IDESC_DQ, u > 0 || c > 0);   // dQ += dS_c K_c
+          else
+            issue_ts_half_steps(tmem + 256, tmem + 128, kv(u), c, IDESC_DQ, u > 0 || (c > 0 && steps > 0),
+                                min(4, max(0, steps - 4 * c)));
         }
         if (!ok) break;
         mma_commit(&B.str_empty[u % Cfg::ST]);
@@ -393,9 +451,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           uint32_t dp[64], w[32];
           tmem_ld64(tmem + lane_off + 128 + 64 * c, dp);
 #pragma unroll
-          for (int e = 0; e < 64; e += 2)
-            w[e >> 1] = pack_bf16x2(pf[e] * (__uint_as_float(dp[e]) - dsum),
-                                    pf[e + 1] * (__uint_as_float(dp[e + 1]) - dsum));
+          for (int e = 0; e < 64; e += 2) {
+            float d0 = pf[e] * (__uint_as_float(dp[e]) - dsum), d1 = pf[e + 1] * (__uint_as_float(dp[e + 1]) - dsum);
+            if (TAIL) {   // dP of keys past seqused_k may be NaN (their V rows are not data)
+              d0 = pf[e] != 0.f ? d0 : 0.f;
+              d1 = pf[e + 1] != 0.f ? d1 : 0.f;
+            }
+            w[e >> 1] = pack_bf16x2(d0, d1);
+          }
           tmem_st32(tmem + lane_off + 128 + 64 * c, w);
         }
         tmem_st_wait();
@@ -427,7 +490,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool TAIL>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                     const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
@@ -443,7 +506,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const int b = blockIdx.x / p.hkv, g = blockIdx.x % p.hkv;
   const int n = blockIdx.y;   // low key blocks first: under a causal mask they see the most query tiles
   const BSeq S = bwd_seq(p, b);
-  if (n * kB >= S.sk) return;   // a block past this sequence's keys (whole CTA, before any barrier)
+  if (n * kB >= S.sk) {   // a block past this sequence's keys (whole CTA, before any barrier)
+    if (TAIL) {   // cache rows past seqused_k: dK = dV = 0
+      for (int idx = threadIdx.x; idx < 2 * kB; idx += blockDim.x) {
+        const int j = n * kB + (idx >> 1);
+        if (j >= S.ska) continue;
+        __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(idx & 1 ? p.dk : p.dv) +
+                             int64_t(S.bc) * (idx & 1 ? p.k_bs : p.v_bs) +
+                             int64_t(S.k_row0 + j) * (idx & 1 ? p.k_rs : p.v_rs) + int64_t(g) * (idx & 1 ? p.k_hs : p.v_hs);
+        zero_row(row, D);
+      }
+    }
+    return;
+  }
   const int off = S.sk - S.sq;
   const int j0 = n * kB, jlast = min(j0 + kB - 1, S.sk - 1);
   // query rows that see some key of the block
@@ -637,9 +712,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tmem_ld32(tmem + lane_off + 256 + c * D + k * 32, o);
           if (j < S.sk) store_row32(dst + k * 32, o, f);
         }
+        if (TAIL && j >= S.sk && j < S.ska) zero_row(dst, D);   // cache rows past seqused_k
       }
-    } else if (j < S.sk) {
-      zero_row(c == 0 ? dv : dk, D);   // no query sees these keys
+    } else if (j < (TAIL ? S.ska : S.sk)) {
+      zero_row(c == 0 ? dv : dk, D);   // no query sees these keys (or they are past seqused_k)
     }
   }
 
@@ -651,7 +727,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool TAIL>
 cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, cudaStream_t stream, const BwdSide& side) {
   using Cfg = BwdCfg<D>;
@@ -663,9 +739,9 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtens
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   const dim3 gq(p.batch * p.hq, mblocks), gk(p.batch * p.hkv, nblocks);
   if (mblocks > 0 && nblocks > 0 && side.stream != nullptr) {
@@ -676,19 +752,19 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtens
     // fork the second stream from `stream` and join it back.
     if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess) return e;
-    bwd_dkdv_kernel<D><<<gk, Cfg::THREADS, Cfg::SMEM, side.stream>>>(mq, mk, mv, mdo, p);
+    bwd_dkdv_kernel<D, TAIL><<<gk, Cfg::THREADS, Cfg::SMEM, side.stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_dq_kernel<D><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+    bwd_dq_kernel<D, TAIL><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
     return cudaStreamWaitEvent(stream, side.join, 0);
   }
   if (nblocks > 0) {   // one stream: dK/dV, then dQ
-    bwd_dkdv_kernel<D><<<gk, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+    bwd_dkdv_kernel<D, TAIL><<<gk, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (mblocks > 0) {
-    bwd_dq_kernel<D><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+    bwd_dq_kernel<D, TAIL><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -700,8 +776,12 @@ bool bwd_supported(int dk, int dv) { return (dk == 64 && dv == 64) || (dk == 128
 
 cudaError_t launch_bwd(const BwdParams& p, int d, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream, const BwdSide& side) {
-  if (d == 64) return launch_bwd_t<64>(p, mq, mk, mv, mdo, stream, side);
-  if (d == 128) return launch_bwd_t<128>(p, mq, mk, mv, mdo, stream, side);
+  // the TAIL instances handle key caches with unused rows (seqused_k)
+  const bool tail = p.seqused_k != nullptr;
+  if (d == 64) return tail ? launch_bwd_t<64, true>(p, mq, mk, mv, mdo, stream, side)
+                           : launch_bwd_t<64, false>(p, mq, mk, mv, mdo, stream, side);
+  if (d == 128) return tail ? launch_bwd_t<128, true>(p, mq, mk, mv, mdo, stream, side)
+                            : launch_bwd_t<128, false>(p, mq, mk, mv, mdo, stream, side);
   return cudaErrorInvalidValue;
 }
 

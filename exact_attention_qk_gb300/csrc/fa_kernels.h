@@ -81,6 +81,7 @@ struct BwdParams {
   int wl, wr;                    // -1 = unbounded; wr is 0 when causal
   const int* cu_seqlens_q;       // varlen: int32 [batch+1], else NULL
   const int* cu_seqlens_k;
+  const int* seqused_k;          // int32 [batch] or NULL: keys [0, seqused_k[b]) exist
   int total_q;                   // varlen: rows of q (LSE row stride)
   int64_t ws_rows;               // varlen: workspace rows per head
   int* status;

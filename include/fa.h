@@ -237,7 +237,11 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
  *   that no query sees get dK = dV = 0; rows that see no key get dQ = 0.
  * Supported: (head_dim_qk, head_dim_v) (64,64) or (128,128); causal, sliding
  *   window, GQA/MQA and varlen (cu_seqlens_q / cu_seqlens_k) as in the
- *   forward. seqused_k, a page table or an fp8 cache give FA_ERR_UNSUPPORTED.
+ *   forward; seqused_k as in the forward ("interface.py", `_flash_attn_bwd`
+ *   takes seqused_q / seqused_k): only keys [0, seqused_k[b]) exist, cache
+ *   rows past them may hold anything (NaN included), and their dK and dV are
+ *   written as 0 (up to seqlen_k, or the sequence's cu_seqlens_k length).
+ *   A page table or an fp8 cache gives FA_ERR_UNSUPPORTED.
  * workspace: at least fa_bwd_workspace_size(args) bytes, 256-byte aligned
  *   (fp32 LSE * log2(e) and D for every padded query row). The call is
  *   deterministic: no atomics, the same inputs give the same bits.

@@ -173,7 +173,6 @@ def test_status_strings(fa):
 
 
 @pytest.mark.parametrize("over,code", [
-    (dict(seqused_k=0x50000), 2),
     (dict(page_table=0x50000, max_pages_per_seq=3, page_size=128, num_pages=6), 2),
     (dict(kv_format=1), 2),                               # fp8 cache
     (dict(head_dim_qk=192, head_dim_v=128), 2),           # forward-only head dims
@@ -187,6 +186,12 @@ def test_backward_rejections_before_launch(fa, over, code):
     if "lse" not in over:
         a.lse = 0x70000
     assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == code
+
+
+def test_backward_accepts_seqused_k(fa):
+    # seqused_k is served (the TAIL kernels); the call gets as far as the workspace check
+    a = _args(fa, lse=0x70000, seqused_k=0x50000)
+    assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 4
 
 
 def test_backward_workspace(fa):

@@ -37,6 +37,8 @@ def run_bwd(w, do_bits, concurrent=True):
     if w.varlen:
         kw.update(cu_seqlens_q=gu.i32(w.cu_seqlens_q), cu_seqlens_k=gu.i32(w.cu_seqlens_k),
                   max_seqlen_q=w.max_seqlen_q, max_seqlen_k=w.max_seqlen_k)
+    if w.seqused_k is not None:
+        kw["seqused_k"] = gu.i32(w.seqused_k)
     o, lse = fa.fa_fwd(q, k, v, **kw)
     dq, dk, dv = fa.fa_bwd(q, k, v, o, lse, do, concurrent=concurrent, **kw)
     assert fa.fa_get_status() == fa.FA_OK
@@ -46,7 +48,7 @@ def run_bwd(w, do_bits, concurrent=True):
 def oracle_bwd(w, do_bits):
     kw = dict(scale=w.softmax_scale, causal=w.causal, window_left=w.window_left, window_right=w.window_right)
     if not w.varlen:
-        return oracle.attention_backward(w.q, w.k, w.v, do_bits, **kw)
+        return oracle.attention_backward(w.q, w.k, w.v, do_bits, seqused_k=w.seqused_k, **kw)
     # packed varlen: each sequence is its own batched problem of batch 1
     dq = np.zeros(w.q.shape, np.float64)
     dk = np.zeros(w.k.shape, np.float64)
@@ -56,8 +58,9 @@ def oracle_bwd(w, do_bits):
         q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
         if q1 == q0 or k1 == k0:
             continue   # no query row or no key: every gradient of the sequence is 0
+        used = None if w.seqused_k is None else w.seqused_k[b:b + 1]
         rq, rk, rv = oracle.attention_backward(w.q[None, q0:q1], w.k[None, k0:k1], w.v[None, k0:k1],
-                                               do_bits[None, q0:q1], **kw)
+                                               do_bits[None, q0:q1], seqused_k=used, **kw)
         dq[q0:q1], dk[k0:k1], dv[k0:k1] = rq[0], rk[0], rv[0]
     return dq, dk, dv
 
@@ -218,3 +221,31 @@ def test_full_size_causal_one_kv_group():
                                            do[b:b + 1, :, hs], scale=w.softmax_scale, causal=True)
     print(compare(dq[b:b + 1, :, hs], rq, "dQ"), compare(dk[b:b + 1, :, g:g + 1], rk, "dK"),
           compare(dv[b:b + 1, :, g:g + 1], rv, "dV"))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_seqused_k_with_nan_cache_slots(d):
+    """seqused_k: keys [0, seqused_k[b]) exist; the cache slots past them hold
+    NaN, which must not reach any gradient, and their dK and dV are written 0."""
+    used = np.array([700, 1, 129, 300], np.int32)   # a tail inside a block, one key, 128+1, ...
+    w = inputs.batched("bwdsu", 450 + d, 4, 200, 768, 8, 2, d, d, causal=True, seqused_k=used)
+    print(check_bwd(w))
+    w2 = inputs.batched("bwdsu2", 460 + d, 3, 257, 512, 4, 4, d, d, window_left=100, window_right=30,
+                        seqused_k=np.array([512, 95, 260], np.int32))
+    print(check_bwd(w2))
+
+
+def test_seqused_k_varlen():
+    """seqused_k with packed varlen: each sequence's keys [0, seqused_k[b]) of
+    its cu_seqlens_k rows exist; the rest of its rows get dK = dV = 0 and the
+    next sequence's rows are not touched."""
+    lens_q = [130, 64, 1, 300]
+    lens_k = [400, 64, 260, 300]
+    w = inputs.packed("bwdsuvl", 470, lens_q, lens_k, 8, 2, 128, 128, causal=True)
+    used = np.array([257, 64, 3, 150], np.int32)
+    w.seqused_k = used
+    for b in range(len(used)):   # NaN in every slot past the used keys
+        k0, k1 = int(w.cu_seqlens_k[b]), int(w.cu_seqlens_k[b + 1])
+        w.k[k0 + used[b]:k1] = inputs.BF16_NAN_BITS
+        w.v[k0 + used[b]:k1] = inputs.BF16_NAN_BITS
+    print(check_bwd(w))

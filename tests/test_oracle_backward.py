@@ -148,3 +148,40 @@ def test_hand_worked_golden_example():
     np.testing.assert_allclose(dq[0, 0, 0], eval(vals["dQ"], env), rtol=0, atol=1e-14)
     np.testing.assert_allclose(dk[0, :, 0], eval(vals["dK"], env), rtol=0, atol=1e-14)
     np.testing.assert_allclose(dv[0, :, 0], eval(vals["dV"], env), rtol=0, atol=1e-14)
+
+
+def test_seqused_k_finite_differences_and_unused_slots():
+    """seqused_k: central finite differences of the forward oracle (with the
+    same seqused_k) for every element, including cache slots past the used
+    length, whose gradients must be exactly 0; NaN in those slots must not
+    reach any gradient."""
+    rng = np.random.default_rng(9)
+    B, Sq, Sk, hq, hkv, D = 2, 4, 7, 2, 1, 3
+    used = np.array([5, 2], np.int32)
+    q = rng.standard_normal((B, Sq, hq, D))
+    k = rng.standard_normal((B, Sk, hkv, D))
+    v = rng.standard_normal((B, Sk, hkv, D))
+    w = rng.standard_normal((B, Sq, hq, D))
+    kw = dict(scale=0.6, causal=True, window_left=2, seqused_k=used)
+    dq, dk, dv = oracle.attention_backward(q, k, v, w, **kw)
+    eps = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [xp if a is x else a for a in (q, k, v)]
+            args_m = [xm if a is x else a for a in (q, k, v)]
+            num[idx] = (_loss(*args_p, w, **kw) - _loss(*args_m, w, **kw)) / (2 * eps)
+        np.testing.assert_allclose(g, num, rtol=0, atol=1e-7)
+    for b in range(B):
+        assert (dk[b, used[b]:] == 0).all() and (dv[b, used[b]:] == 0).all()
+    kn, vn = k.copy(), v.copy()
+    for b in range(B):
+        kn[b, used[b]:] = np.nan
+        vn[b, used[b]:] = np.nan
+    gq, gk, gv = oracle.attention_backward(q, kn, vn, w, **kw)
+    np.testing.assert_array_equal(gq, dq)
+    np.testing.assert_array_equal(gk, dk)
+    np.testing.assert_array_equal(gv, dv)
