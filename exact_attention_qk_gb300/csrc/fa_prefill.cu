@@ -59,7 +59,7 @@ struct PrefillCfg {
   static constexpr int OFF_OST = OFF_V + VST * V_BYTES;
   static constexpr int OST_BYTES = OSTAGE ? 2 * kChunkBytes : 0;
   static constexpr int OFF_BAR = OFF_OST + OST_BYTES;
-  static constexpr int NBAR = 2 * 2 + 2 * KST + 3 * VST + 2 + 2 + 2 + 2 + 2 + 2;
+  static constexpr int NBAR = 2 * 2 + 2 * KST + 3 * VST + 2 + 2 + 2 + 2 + 2 + 2 + 2;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // at least half the SM's shared memory, so one CTA (the one that owns all
   // 512 TMEM columns) is resident per SM
@@ -219,6 +219,7 @@ struct Bars {
   uint64_t* v_fixed;   // [VST] tail rows of the V tile cleared (seqused_k)
   uint64_t* s_full;    // [2] per S slot
   uint64_t* p_full;    // [2] per S slot
+  uint64_t* p_half;    // [2] per S slot (NQ == 2): P of keys [0, 64) stored
   uint64_t* o_bar;     // [2] per O: one phase per P.V
   uint64_t* o_empty;   // [2] per O: epilogue done reading
   uint64_t* pv_done;   // [2] per S slot (NQ == 2): the P.V reading its P has completed
@@ -238,6 +239,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   B.v_fixed = b; b += Cfg::VST;
   B.s_full = b; b += 2;
   B.p_full = b; b += 2;
+  B.p_half = b; b += 2;
   B.o_bar = b; b += 2;
   B.o_empty = b; b += 2;
   B.pv_done = b; b += 2;
@@ -297,6 +299,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       mbar_init(&B.q_empty[i], 1);
       mbar_init(&B.s_full[i], 1);
       mbar_init(&B.p_full[i], 4);      // one arrival per softmax warp
+      mbar_init(&B.p_half[i], 4);
       mbar_init(&B.o_bar[i], 1);
       mbar_init(&B.o_empty[i], 4);
       mbar_init(&B.pv_done[i], 1);
@@ -491,6 +494,24 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
             mma_bf16_ts(d, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
         }
       };
+      // the 16-key steps [k0, k1) of the same product (P of keys 16 k0 .. 16 k1 - 1)
+      auto issue_pv_steps = [&](int o, int slot, int vst, bool acc, int k0, int k1) {
+        const uint32_t d = tmem + Cfg::O_COL + o * DV;
+        const uint64_t vd = sdesc_sw128(v_base + vst * Cfg::V_BYTES, kChunkBytes, 1024);
+        const uint32_t pa = tmem + slot * 128;
+        if (k0 == 0 && k1 == 4) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts(d, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
+        } else if (k0 == 4 && k1 == 8) {
+#pragma unroll
+          for (int kk = 4; kk < 8; ++kk)
+            mma_bf16_ts(d, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, 1u);
+        } else {
+          for (int kk = k0; kk < k1; ++kk)
+            mma_bf16_ts(d, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (kk > 0 || acc) ? 1u : 0u);
+        }
+      };
       uint32_t vfix = 0;   // parity bit per V stage of its v_fixed barrier
       auto wait_fix = [&](int n, int vst, const Tile& T) -> bool {
         if (!tail_fix<TAIL>(T, n)) return true;
@@ -581,10 +602,14 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
                   if (ou[t] > 0 && !mbar_wait(&B.o_empty[t], (ou[t] - 1) & 1, guard)) { ok = false; break; }
                   ++ou[t];
                 }
+                // keys [0, 64) as soon as their P is stored, then the rest
+                if (!mbar_wait(&B.p_half[t], pw[t] & 1, guard)) { ok = false; break; }
+                tc_fence_after();
+                issue_pv_steps(t, t, vst, n != hi[t] - 1, 0, min(4, steps));
                 if (!mbar_wait(&B.p_full[t], pw[t] & 1, guard)) { ok = false; break; }
                 ++pw[t];
                 tc_fence_after();
-                issue_pv(t, t, vst, n != hi[t] - 1, steps);
+                issue_pv_steps(t, t, vst, n != hi[t] - 1, 4, steps);
                 mma_commit(&B.pv_done[t]);
                 if (n == lo[t]) mma_commit(&B.o_bar[t]);   // O[t] complete for this tile
               }
@@ -733,7 +758,8 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         // that is consumed exactly once: before O is rescaled, or else just
         // before this block's P is published (so the next P.V cannot run ahead).
         // NQ == 1 only: with NQ == 2, S(n) completing implies every earlier
-        // P.V of this O completed (same issuing thread, issued before it).
+        // P.V of this O completed (the S thread issued S(n) only after the
+        // P.V of the block before had completed, pv_done).
         bool pending = (NQ == 1) && (n != R.nhi - 1);
         if (n == R.nhi - 1) {
           m = m_new;
@@ -767,20 +793,50 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         const float2 nm2 = make_float2(-mu, -mu);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
+        if constexpr (NQ == 2) {
+          // P in two halves: keys [0, 64) are stored and published first, so
+          // that the P.V thread starts on them while the rest is computed
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
-          s[c] = ex2_approx(x.x);
-          s[c + 1] = ex2_approx(x.y);
-          acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+          for (int c = 0; c < 64; c += 2) {
+            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+            s[c] = ex2_approx(x.x);
+            s[c + 1] = ex2_approx(x.y);
+            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+          }
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+          tmem_st32(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[32]>(r[0]));
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.p_half[slot]);
+#pragma unroll
+          for (int c = 64; c < 128; c += 2) {
+            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+            s[c] = ex2_approx(x.x);
+            s[c + 1] = ex2_approx(x.y);
+            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+          }
+#pragma unroll
+          for (int c = 32; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+          tmem_st32(tmem + lane_off + slot * 128 + 32, reinterpret_cast<uint32_t(&)[32]>(r[32]));
+          tmem_st_wait();
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; c += 2) {
+            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+            s[c] = ex2_approx(x.x);
+            s[c + 1] = ex2_approx(x.y);
+            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+          }
+#pragma unroll
+          for (int c = 0; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+          tmem_st64(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[64]>(r));
+          tmem_st_wait();
         }
         const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
         const float2 a = __fadd2_rn(a01, a23);
         l += a.x + a.y;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
-        tmem_st64(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[64]>(r));
-        tmem_st_wait();
         if (pending) {
           if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) { ok = false; break; }
           ++ow;
