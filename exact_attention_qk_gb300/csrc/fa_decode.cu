@@ -114,6 +114,18 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t w) {
   return h;
 }
 
+// The same for the high 16 bits of w.
+template <int KVT>
+__device__ __forceinline__ uint32_t fp8x2_hi_to_f16x2(uint32_t w) {
+  uint32_t h;
+  if constexpr (KVT == 1) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, b;\n\t}" : "=r"(h) : "r"(w));
+  } else {
+    h = __byte_perm(w, 0u, 0x3424);
+  }
+  return h;
+}
+
 template <int DK, int DV, int KVT>
 __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
     decode_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -121,7 +133,9 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
   using C = DecodeCfg<DK, DV, KVT>;
   constexpr int NR = kRows;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, offset from the array itself so that every access
+  // through it stays a shared-memory access with 32-bit addressing
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint16_t* p_s = reinterpret_cast<uint16_t*>(smem + C::OFF_P);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::NSTAGE;
@@ -366,6 +380,23 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
   uint16_t* pw = p_s + warp * (NR * WK);          // this warp's P[row][WK keys]
   const int key_end = min(sk, s_hi);              // keys at or past this are never used
 
+  // Byte offsets (from stage 0) of this thread's first K and V fragment words.
+  // The 128-byte swizzle stores 16-byte granule j of tile row r at granule
+  // j ^ (r & 7). The rows one thread reads in a fragment agree in their low
+  // three bits with a per-thread value, so a fragment word of k step kk (K) or
+  // of column block j and key i (V) sits at (offset ^ (c << 4)) + d, with c
+  // and d compile-time constants.
+  uint32_t kofs, vofs;
+  if constexpr (KVT == 0) {
+    kofs = (warp * WK + g8) * 128 + ((((t4 >> 1) ^ g8)) << 4) + 8 * (t4 & 1);
+    vofs = C::KCH * C::BOX + (warp * WK + 4 * t4) * 128 + ((((g8 >> 1) ^ (4 * (t4 & 1)))) << 4) + 8 * (g8 & 1);
+  } else {
+    kofs = (warp * WK + g8) * 128 + (g8 << 4) + 4 * t4;
+    vofs = C::KCH * C::BOX + (warp * WK + 4 * t4) * 128 + ((((g8 >> 2) ^ (4 * (t4 & 1)))) << 4) + 4 * (g8 & 3);
+  }
+  auto lds32 = [&](uint32_t o) { return *reinterpret_cast<const uint32_t*>(smem + o); };
+  auto lds64 = [&](uint32_t o) { return *reinterpret_cast<const uint2*>(smem + o); };
+
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
     const int st = t % C::NSTAGE;
@@ -373,8 +404,27 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
       ok = false;
       break;
     }
-    const uint8_t* stage = smem + st * C::STAGE_BYTES;
+    uint8_t* stage = smem + st * C::STAGE_BYTES;
     const int tkey0 = key_base + t * TK;
+    const uint32_t kst = st * C::STAGE_BYTES + kofs, vst = st * C::STAGE_BYTES + vofs;
+
+    // V rows at or past key_end may hold anything (NaN included). The warp
+    // whose rows reach them zeroes them in shared memory before its P.V, so
+    // that no 0 * NaN reaches O; the fence orders these writes before the
+    // next TMA write into the stage.
+    const int vlim = key_end - tkey0;
+    const bool vtail = vlim < warp * WK + WK;
+    if (vtail) {
+      const int r0 = max(vlim, warp * WK);
+      const int nchunk = (warp * WK + WK - r0) * C::VCH * 8;
+      for (int idx = lane; idx < nchunk; idx += 32) {
+        const int rr = r0 + idx / (C::VCH * 8), rem = idx % (C::VCH * 8);
+        *reinterpret_cast<uint4*>(stage + (C::KCH + rem / 8) * C::BOX + rr * 128 + (rem % 8) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
 
     // ---- S^T = K q^T over this warp's WK keys, in 16-key groups ----
     float sv[G][4];
@@ -385,19 +435,16 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         if constexpr (KVT == 0) {
-          // dims 16kk + 4t4 .. +3: 8 bytes in box kk/4, granule 2(kk%4) + t4/2
-          const int gran = 2 * (kk & 3) + (t4 >> 1), byt = 8 * (t4 & 1);
-          const uint8_t* kbox = stage + (kk >> 2) * C::BOX;
-          const uint2 x = *reinterpret_cast<const uint2*>(kbox + ka * 128 + ((gran ^ (ka & 7)) << 4) + byt);
-          const uint2 y = *reinterpret_cast<const uint2*>(kbox + kb * 128 + ((gran ^ (kb & 7)) << 4) + byt);
+          // dims 16kk + 4t4 .. +3: 8 bytes in box kk/4, granule 2(kk%4) + t4/2; row kb = ka + 8
+          const uint32_t o = (kst ^ ((2 * (kk & 3)) << 4)) + (kk >> 2) * C::BOX + grp * 2048;
+          const uint2 x = lds64(o), y = lds64(o + 1024);
           mma_16816_bf16(sacc, x.x, y.x, x.y, y.y, qf[kk][0], qf[kk][1]);
         } else {
           // dims 16kk + 4t4 .. +3: 4 bytes in box kk/8, granule kk%8
-          const uint8_t* kbox = stage + (kk >> 3) * C::BOX;
-          const uint32_t x = *reinterpret_cast<const uint32_t*>(kbox + ka * 128 + (((kk & 7) ^ (ka & 7)) << 4) + 4 * t4);
-          const uint32_t y = *reinterpret_cast<const uint32_t*>(kbox + kb * 128 + (((kk & 7) ^ (kb & 7)) << 4) + 4 * t4);
-          mma_16816_f16(sacc, fp8x2_to_f16x2<KVT>(x), fp8x2_to_f16x2<KVT>(y), fp8x2_to_f16x2<KVT>(x >> 16),
-                        fp8x2_to_f16x2<KVT>(y >> 16), qf[kk][0], qf[kk][1]);
+          const uint32_t o = (kst ^ ((kk & 7) << 4)) + (kk >> 3) * C::BOX + grp * 2048;
+          const uint32_t x = lds32(o), y = lds32(o + 1024);
+          mma_16816_f16(sacc, fp8x2_to_f16x2<KVT>(x), fp8x2_to_f16x2<KVT>(y), fp8x2_hi_to_f16x2<KVT>(x),
+                        fp8x2_hi_to_f16x2<KVT>(y), qf[kk][0], qf[kk][1]);
         }
       }
       // sacc: (key ka, row 2t4), (ka, 2t4+1), (kb, 2t4), (kb, 2t4+1); base-2 scores
@@ -480,43 +527,33 @@ __global__ void __launch_bounds__(kDecThreads, (DV <= 128) ? 3 : 2)
     for (int grp = 0; grp < G; ++grp) {
       // P^T as the B operand: row g8, keys 16 grp + 4t4 .. +3
       const uint2 pf = *reinterpret_cast<const uint2*>(pw + g8 * WK + grp * 16 + 4 * t4);
-      const int kv0 = warp * WK + grp * 16 + 4 * t4;   // this thread's V rows (tile keys)
-      // keys at or past key_end may hold anything (NaN included): zero them
-      const bool vtail = tkey0 + warp * WK + grp * 16 + 16 > key_end;
+      // this thread's V rows (tile keys) are warp * WK + grp * 16 + 4 t4 + i, i < 4
 #pragma unroll
       for (int j = 0; j < DV / 32; ++j) {
         // columns 32j + 4g8 .. +3: m tile 2j holds (4g8, 4g8+1), m tile 2j+1 (4g8+2, 4g8+3)
         if constexpr (KVT == 0) {
-          const int gran = 4 * (j & 1) + (g8 >> 1), byt = 8 * (g8 & 1);
-          const uint8_t* vbox = stage + (C::KCH + (j >> 1)) * C::BOX;
+          // granule 4(j%2) + g8/2 of box j/2
           uint2 r[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int kr = kv0 + i;
-            r[i] = *reinterpret_cast<const uint2*>(vbox + kr * 128 + ((gran ^ (kr & 7)) << 4) + byt);
-            if (vtail && tkey0 + kr >= key_end) r[i] = make_uint2(0u, 0u);
-          }
+          for (int i = 0; i < 4; ++i)
+            r[i] = lds64((vst ^ ((i ^ (4 * (j & 1))) << 4)) + (j >> 1) * C::BOX + grp * 2048 + i * 128);
           mma_16816_bf16(o[2 * j], __byte_perm(r[0].x, r[1].x, 0x5410), __byte_perm(r[0].x, r[1].x, 0x7632),
                          __byte_perm(r[2].x, r[3].x, 0x5410), __byte_perm(r[2].x, r[3].x, 0x7632), pf.x, pf.y);
           mma_16816_bf16(o[2 * j + 1], __byte_perm(r[0].y, r[1].y, 0x5410), __byte_perm(r[0].y, r[1].y, 0x7632),
                          __byte_perm(r[2].y, r[3].y, 0x5410), __byte_perm(r[2].y, r[3].y, 0x7632), pf.x, pf.y);
         } else {
-          const int gran = 2 * (j & 3) + (g8 >> 2), byt = 4 * (g8 & 3);
-          const uint8_t* vbox = stage + (C::KCH + (j >> 2)) * C::BOX;
+          // granule 2(j%4) + g8/4 of box j/4
           uint32_t r[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int kr = kv0 + i;
-            r[i] = *reinterpret_cast<const uint32_t*>(vbox + kr * 128 + ((gran ^ (kr & 7)) << 4) + byt);
-            if (vtail && tkey0 + kr >= key_end) r[i] = 0u;
-          }
+          for (int i = 0; i < 4; ++i)
+            r[i] = lds32((vst ^ ((i ^ (2 * (j & 3))) << 4)) + (j >> 2) * C::BOX + grp * 2048 + i * 128);
           // byte pairs (key 4t4 + 2c, key 4t4 + 2c + 1) of one column
           const uint32_t c01a = __byte_perm(r[0], r[1], 0x5140), c23a = __byte_perm(r[0], r[1], 0x7362);
           const uint32_t c01b = __byte_perm(r[2], r[3], 0x5140), c23b = __byte_perm(r[2], r[3], 0x7362);
-          mma_16816_f16(o[2 * j], fp8x2_to_f16x2<KVT>(c01a), fp8x2_to_f16x2<KVT>(c01a >> 16),
-                        fp8x2_to_f16x2<KVT>(c01b), fp8x2_to_f16x2<KVT>(c01b >> 16), pf.x, pf.y);
-          mma_16816_f16(o[2 * j + 1], fp8x2_to_f16x2<KVT>(c23a), fp8x2_to_f16x2<KVT>(c23a >> 16),
-                        fp8x2_to_f16x2<KVT>(c23b), fp8x2_to_f16x2<KVT>(c23b >> 16), pf.x, pf.y);
+          mma_16816_f16(o[2 * j], fp8x2_to_f16x2<KVT>(c01a), fp8x2_hi_to_f16x2<KVT>(c01a),
+                        fp8x2_to_f16x2<KVT>(c01b), fp8x2_hi_to_f16x2<KVT>(c01b), pf.x, pf.y);
+          mma_16816_f16(o[2 * j + 1], fp8x2_to_f16x2<KVT>(c23a), fp8x2_hi_to_f16x2<KVT>(c23a),
+                        fp8x2_to_f16x2<KVT>(c23b), fp8x2_hi_to_f16x2<KVT>(c23b), pf.x, pf.y);
         }
       }
     }
