@@ -285,7 +285,9 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
   using Cfg = PrefillCfg<DK, DV>;
   constexpr int NQ = Cfg::NQ;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, offset from the array itself so that accesses
+  // through it stay shared-memory accesses with 32-bit addressing
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars B = carve_bars<Cfg>(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_BAR + Cfg::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
