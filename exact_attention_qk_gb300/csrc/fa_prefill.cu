@@ -918,11 +918,17 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-            uint4* dst = reinterpret_cast<uint4*>(out + orow + c * 32);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+            __nv_bfloat16* dst = out + orow + c * 32;
+            if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {   // whole 32-byte sectors
+              st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+              st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              d4[2] = make_uint4(w[8], w[9], w[10], w[11]);
+              d4[3] = make_uint4(w[12], w[13], w[14], w[15]);
+            }
           }
         }
       }
