@@ -165,6 +165,11 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
   uint32_t w[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * f, __uint_as_float(o[2 * e + 1]) * f);
+  if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {   // whole 32-byte sectors
+    st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+    st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+    return;
+  }
   uint4* d4 = reinterpret_cast<uint4*>(dst);
   d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
   d4[1] = make_uint4(w[4], w[5], w[6], w[7]);

@@ -871,11 +871,25 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           uint32_t o[32];
           tmem_ld32(o_addr + c * 32, o);
           if (valid) {
-            float4* dst = reinterpret_cast<float4*>(opart + c * 32);
+            float* dst = opart + c * 32;
+            if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {   // whole 32-byte sectors
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
-                                   __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
+              for (int e = 0; e < 4; ++e)
+                st_global_v8(dst + 8 * e, __float_as_uint(__uint_as_float(o[8 * e]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[8 * e + 1]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[8 * e + 2]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[8 * e + 3]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[8 * e + 4]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[8 * e + 5]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[8 * e + 6]) * inv_l),
+                             __float_as_uint(__uint_as_float(o[8 * e + 7]) * inv_l));
+            } else {
+              float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                d4[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
+                                    __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
+            }
           }
         }
         if (valid) *lpart = empty_row ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
