@@ -28,6 +28,8 @@
 // device status word, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
 
@@ -720,22 +722,30 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
       }
       const int off = T.sk - T.sq;
       float m = -INFINITY, l = 0.f;
-      for (int n = R.nhi - 1; n >= R.nlo; --n) {
+      // One instance of the block body for blocks with masked keys and one for
+      // blocks without: sharing the code after the mask made every block
+      // slower, and the masked instance's per-column test is one unsigned
+      // range compare (measured: causal +2 to 3 %, varlen +1 to 3 %)
+      auto block = [&](auto masked, int n) -> bool {
         const int slot = (NQ == 2) ? wg : (jc & 1);
-        if (!mbar_wait(&B.s_full[slot], (slot ? sw1 : sw0) & 1, guard)) { ok = false; break; }
+        if (!mbar_wait(&B.s_full[slot], (slot ? sw1 : sw0) & 1, guard)) return false;
         if (slot) ++sw1; else ++sw0;
         tc_fence_after();
         uint32_t r[128];
         float* s = reinterpret_cast<float*>(r);
         float bmax;
-        if (needs_mask(p, T, R, n)) {   // (warp-uniform)
+        if constexpr (decltype(masked)::value) {
           tmem_ld128(tmem + lane_off + slot * 128, r);
           const int jb = n * kBN;
           const int c_lo = (p.wl >= 0) ? i + off - p.wl - jb : INT32_MIN / 2;
           int c_hi = T.sk - 1 - jb;
           if (p.wr >= 0) c_hi = min(c_hi, i + off + p.wr - jb);
+          // column c is visible when (unsigned)(c - c_lo) <= (unsigned)(c_hi - c_lo); an
+          // empty range gets a lower end past every column
+          const int lo_e = (c_hi < c_lo) ? 256 : c_lo;
+          const uint32_t width = (c_hi < c_lo) ? 0u : static_cast<uint32_t>(c_hi - c_lo);
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (c < c_lo || c > c_hi) ? -INFINITY : s[c];
+          for (int c = 0; c < 128; ++c) s[c] = (static_cast<uint32_t>(c - lo_e) <= width) ? s[c] : -INFINITY;
           // row max: eight independent chains of 3-input max
           float mx[8];
 #pragma unroll
@@ -769,7 +779,7 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
           const bool need = m_new > m + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
             if (NQ == 1) {
-              if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) { ok = false; break; }
+              if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) return false;
               ++ow;
               pending = false;
             }
@@ -840,13 +850,18 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         const float2 a = __fadd2_rn(a01, a23);
         l += a.x + a.y;
         if (pending) {
-          if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) { ok = false; break; }
+          if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) return false;
           ++ow;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.p_full[slot]);
         ++jc;
+        return true;
+      };
+      for (int n = R.nhi - 1; n >= R.nlo; --n) {
+        const bool go = needs_mask(p, T, R, n) ? block(std::true_type{}, n) : block(std::false_type{}, n);
+        if (!go) { ok = false; break; }
       }
       if (!ok) break;
       // ---- epilogue: O / l -> bf16, LSE (natural log) ----
