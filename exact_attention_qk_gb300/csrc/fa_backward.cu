@@ -39,6 +39,8 @@
 // tensor memory and returns.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 
 #include "fa_kernels.h"
 #include "fa_ptx.cuh"
@@ -439,15 +441,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!mbar_wait(B.s_full, u & 1, guard)) { ok = false; break; }
         tc_fence_after();
         float pf[64];
-        {
+        // one instance for blocks every key of which this tile sees, one with the
+        // mask (column e visible when (unsigned)(e - c_lo) <= (unsigned)(c_hi - c_lo))
+        auto p_phase = [&](auto masked) {
           uint32_t sv[64];
           tmem_ld64(tmem + lane_off + 64 * c, sv);
+          const int lo_e = (c_hi < c_lo) ? 256 : c_lo;
+          const uint32_t width = (c_hi < c_lo) ? 0u : static_cast<uint32_t>(c_hi - c_lo);
 #pragma unroll
           for (int e = 0; e < 64; ++e) {
             const float x = ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, nl2));
-            pf[e] = (full || (e >= c_lo && e <= c_hi)) ? x : 0.f;
+            if constexpr (decltype(masked)::value)
+              pf[e] = (static_cast<uint32_t>(e - lo_e) <= width) ? x : 0.f;
+            else
+              pf[e] = x;
           }
-        }
+        };
+        if (full)
+          p_phase(std::false_type{});
+        else
+          p_phase(std::true_type{});
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.p_done[c]);
@@ -669,9 +682,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!mbar_wait(B.s_full, u & 1, guard)) { ok = false; break; }
         tc_fence_after();
         float pf[64];
-        {
+        // one instance for jobs every (key, query) pair of which is visible, one
+        // with the mask (column e visible when (unsigned)(e - c_lo) <= (unsigned)(c_hi - c_lo))
+        auto p_phase = [&](auto masked) {
           uint32_t sv[64], pw[32];
           tmem_ld64(tmem + lane_off + 64 * c, sv);
+          const int lo_e = (c_hi < c_lo) ? 256 : c_lo;
+          const uint32_t width = (c_hi < c_lo) ? 0u : static_cast<uint32_t>(c_hi - c_lo);
 #pragma unroll
           for (int e = 0; e < 64; e += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(vl + e);
@@ -679,13 +696,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const float x = ex2_approx(fmaf(__uint_as_float(sv[e + q]), p.scale_log2, -lv[q]));
-              pf[e + q] = (full || (e + q >= c_lo && e + q <= c_hi)) ? x : 0.f;
+              if constexpr (decltype(masked)::value)
+                pf[e + q] = (static_cast<uint32_t>(e + q - lo_e) <= width) ? x : 0.f;
+              else
+                pf[e + q] = x;
             }
             pw[e >> 1] = pack_bf16x2(pf[e], pf[e + 1]);
             pw[(e >> 1) + 1] = pack_bf16x2(pf[e + 2], pf[e + 3]);
           }
           tmem_st32(tmem + lane_off + 64 * c, pw);
-        }
+        };
+        if (full)
+          p_phase(std::false_type{});
+        else
+          p_phase(std::true_type{});
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
