@@ -733,51 +733,127 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
         tc_fence_after();
         uint32_t r[128];
         float* s = reinterpret_cast<float*>(r);
-        float bmax;
+        float bmax = -INFINITY;
         if constexpr (decltype(masked)::value) {
-          tmem_ld128(tmem + lane_off + slot * 128, r);
+          // ---- a block with masked keys ----
           const int jb = n * kBN;
           const int c_lo = (p.wl >= 0) ? i + off - p.wl - jb : INT32_MIN / 2;
           int c_hi = T.sk - 1 - jb;
           if (p.wr >= 0) c_hi = min(c_hi, i + off + p.wr - jb);
+          const bool row_vis = c_hi >= c_lo && c_hi >= 0 && c_lo <= 127;   // the row sees a key here
           // column c is visible when (unsigned)(c - c_lo) <= (unsigned)(c_hi - c_lo); an
           // empty range gets a lower end past every column
           const int lo_e = (c_hi < c_lo) ? 256 : c_lo;
           const uint32_t width = (c_hi < c_lo) ? 0u : static_cast<uint32_t>(c_hi - c_lo);
+          auto apply_mask = [&]() {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (static_cast<uint32_t>(c - lo_e) <= width) ? s[c] : -INFINITY;
-          // row max: eight independent chains of 3-input max
-          float mx[8];
+            for (int c = 0; c < 128; ++c) s[c] = (static_cast<uint32_t>(c - lo_e) <= width) ? s[c] : -INFINITY;
+          };
+          const bool first = n == R.nhi - 1;
+          float m_new = m, lsum = 0.f;
+          bool need = false;
+          // The load's own row max covers the masked columns too, so it is only an
+          // upper bound mc of the visible max (a max over the masked row costs far
+          // more here). P is first formed against mc, masked columns exactly 0; the
+          // largest P then gives the visible block max, mc + log2(p_max), and P is
+          // scaled to the reference the online softmax would have used, so the
+          // row's largest P is 1 as with the exact max. A row whose visible keys
+          // all sit more than 100 (base 2) under mc is redone below with the
+          // visible max (S is still in tensor memory).
+          float hw;
+          tmem_ld128_max(tmem + lane_off + slot * 128, r, hw);
+          apply_mask();
+          const float mc = fmaxf(m, row_vis ? hw * p.scale_log2 : -INFINITY);
+          const float muc = (mc == -INFINITY) ? 0.f : mc;
+          {
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+            const float2 nm2 = make_float2(-muc, -muc);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) mx[j] = s[j];
+            for (int c = 0; c < 128; c += 2) {
+              const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+              s[c] = ex2_approx(x.x);
+              s[c + 1] = ex2_approx(x.y);
+            }
+          }
+          float pm[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) pm[j] = s[j];
 #pragma unroll
           for (int c = 8; c + 16 <= 128; c += 16) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) mx[j] = fmax3(mx[j], s[c + j], s[c + 8 + j]);
+            for (int j = 0; j < 8; ++j) pm[j] = fmax3(pm[j], s[c + j], s[c + 8 + j]);
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], s[120 + j]);
-          bmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
-                 p.scale_log2;
-        } else {
-          // every column is visible: the load returns the row max with the row
-          float hw;
-          tmem_ld128_max(tmem + lane_off + slot * 128, r, hw);
-          bmax = hw * p.scale_log2;
-        }
-        const float m_new = fmaxf(m, bmax);
-        // The previous P.V of this O (if any in this tile) has a phase on o_bar
-        // that is consumed exactly once: before O is rescaled, or else just
-        // before this block's P is published (so the next P.V cannot run ahead).
-        // NQ == 1 only: with NQ == 2, S(n) completing implies every earlier
-        // P.V of this O completed (the S thread issued S(n) only after the
-        // P.V of the block before had completed, pv_done).
-        bool pending = (NQ == 1) && (n != R.nhi - 1);
-        if (n == R.nhi - 1) {
-          m = m_new;
-        } else {
-          const bool need = m_new > m + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
+          for (int j = 0; j < 8; ++j) pm[j] = fmaxf(pm[j], s[120 + j]);
+          const float p_max = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+          if (!__any_sync(0xffffffffu, row_vis && !(p_max >= 0x1p-100f))) {
+            const float mb = (p_max > 0.f) ? muc + __log2f(p_max) : -INFINITY;   // visible block max
+            m_new = fmaxf(m, mb);
+            need = first || m_new > m + kRescaleThreshold;
+            const float mref = need ? m_new : m;
+            const float mu = (mref == -INFINITY) ? 0.f : mref;
+            const float g = (p_max > 0.f) ? ex2_approx(muc - mu) : 0.f;
+            const float2 g2 = make_float2(g, g);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float2 pv = __fmul2_rn(make_float2(s[2 * c], s[2 * c + 1]), g2);
+              acc[c & 3] = __fadd2_rn(acc[c & 3], pv);
+              r[c] = pack_bf16x2(pv.x, pv.y);
+            }
+            const float2 a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+            lsum = a2.x + a2.y;
+            // P into tensor memory over S's first 64 columns (published below)
+            if constexpr (NQ == 2) {
+              tmem_st32(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[32]>(r[0]));
+              tmem_st32(tmem + lane_off + slot * 128 + 32, reinterpret_cast<uint32_t(&)[32]>(r[32]));
+            } else {
+              tmem_st64(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[64]>(r));
+            }
+          } else {
+            // (rare) the same with the visible max, S read again 32 columns at a
+            // time and each chunk's P stored over S columns already read
+            float bx = -INFINITY;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+              uint32_t t[32];
+              tmem_ld32(tmem + lane_off + slot * 128 + 32 * ch, t);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (static_cast<uint32_t>(32 * ch + e - lo_e) <= width) bx = fmaxf(bx, __uint_as_float(t[e]));
+            }
+            m_new = fmaxf(m, bx * p.scale_log2);
+            need = first || m_new > m + kRescaleThreshold;
+            const float mref = need ? m_new : m;
+            const float mu = (mref == -INFINITY) ? 0.f : mref;
+            float sum = 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+              uint32_t t[32], w[16];
+              tmem_ld32(tmem + lane_off + slot * 128 + 32 * ch, t);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                float pv[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int e = 2 * k + u;
+                  const bool vis = static_cast<uint32_t>(32 * ch + e - lo_e) <= width;
+                  pv[u] = vis ? ex2_approx(fmaf(__uint_as_float(t[e]), p.scale_log2, -mu)) : 0.f;
+                  sum += pv[u];
+                }
+                w[k] = pack_bf16x2(pv[0], pv[1]);
+              }
+              tmem_st16(tmem + lane_off + slot * 128 + 16 * ch, w);
+            }
+            lsum = sum;
+          }
+          tmem_st_wait();
+          // the O rescale (not on a tile's first block), as for unmasked blocks
+          bool pending = (NQ == 1) && !first;
+          if (first) {
+            m = m_new;
+          } else if (__any_sync(0xffffffffu, need)) {
             if (NQ == 1) {
               if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) return false;
               ++ow;
@@ -799,64 +875,119 @@ __global__ void __launch_bounds__(PrefillCfg<DK, DV>::THREADS, 1)
               m = m_new;
             }
           }
-        }
-        const float mu = (m == -INFINITY) ? 0.f : m;
-        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-        const float2 nm2 = make_float2(-mu, -mu);
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                         make_float2(0.f, 0.f)};
-        if constexpr (NQ == 2) {
-          // P in two halves: keys [0, 64) are stored and published first, so
-          // that the P.V thread starts on them while the rest is computed
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
-            s[c] = ex2_approx(x.x);
-            s[c + 1] = ex2_approx(x.y);
-            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+          l += lsum;
+          if (pending) {
+            if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) return false;
+            ++ow;
           }
-#pragma unroll
-          for (int c = 0; c < 32; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
-          tmem_st32(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[32]>(r[0]));
-          tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&B.p_half[slot]);
-#pragma unroll
-          for (int c = 64; c < 128; c += 2) {
-            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
-            s[c] = ex2_approx(x.x);
-            s[c + 1] = ex2_approx(x.y);
-            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+          if (lane == 0) {
+            if (NQ == 2) mbar_arrive(&B.p_half[slot]);
+            mbar_arrive(&B.p_full[slot]);
           }
-#pragma unroll
-          for (int c = 32; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
-          tmem_st32(tmem + lane_off + slot * 128 + 32, reinterpret_cast<uint32_t(&)[32]>(r[32]));
-          tmem_st_wait();
+          ++jc;
+          return true;
         } else {
+          // every column is visible: the load returns the row max with the row
+          float hw;
+          tmem_ld128_max(tmem + lane_off + slot * 128, r, hw);
+          bmax = hw * p.scale_log2;
+        }
+        if constexpr (!decltype(masked)::value) {
+          const float m_new = fmaxf(m, bmax);
+          // The previous P.V of this O (if any in this tile) has a phase on o_bar
+          // that is consumed exactly once: before O is rescaled, or else just
+          // before this block's P is published (so the next P.V cannot run ahead).
+          // NQ == 1 only: with NQ == 2, S(n) completing implies every earlier
+          // P.V of this O completed (the S thread issued S(n) only after the
+          // P.V of the block before had completed, pv_done).
+          bool pending = (NQ == 1) && (n != R.nhi - 1);
+          if (n == R.nhi - 1) {
+            m = m_new;
+          } else {
+            const bool need = m_new > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need)) {
+              if (NQ == 1) {
+                if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) return false;
+                ++ow;
+                pending = false;
+              }
+              tc_fence_after();
+              const float f = need ? ex2_approx(m - m_new) : 1.f;
+#pragma unroll 1
+              for (int c = 0; c < DV / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + c * 32, o);
 #pragma unroll
-          for (int c = 0; c < 128; c += 2) {
-            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
-            s[c] = ex2_approx(x.x);
-            s[c + 1] = ex2_approx(x.y);
-            acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                tmem_st32(o_addr + c * 32, o);
+              }
+              tmem_st_wait();
+              if (need) {
+                l *= f;
+                m = m_new;
+              }
+            }
           }
+          const float mu = (m == -INFINITY) ? 0.f : m;
+          const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+          const float2 nm2 = make_float2(-mu, -mu);
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+          if constexpr (NQ == 2) {
+            // P in two halves: keys [0, 64) are stored and published first, so
+            // that the P.V thread starts on them while the rest is computed
 #pragma unroll
-          for (int c = 0; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
-          tmem_st64(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[64]>(r));
-          tmem_st_wait();
+            for (int c = 0; c < 64; c += 2) {
+              const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+              s[c] = ex2_approx(x.x);
+              s[c + 1] = ex2_approx(x.y);
+              acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+            }
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+            tmem_st32(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[32]>(r[0]));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.p_half[slot]);
+#pragma unroll
+            for (int c = 64; c < 128; c += 2) {
+              const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+              s[c] = ex2_approx(x.x);
+              s[c + 1] = ex2_approx(x.y);
+              acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+            }
+#pragma unroll
+            for (int c = 32; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+            tmem_st32(tmem + lane_off + slot * 128 + 32, reinterpret_cast<uint32_t(&)[32]>(r[32]));
+            tmem_st_wait();
+          } else {
+#pragma unroll
+            for (int c = 0; c < 128; c += 2) {
+              const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
+              s[c] = ex2_approx(x.x);
+              s[c + 1] = ex2_approx(x.y);
+              acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+            }
+#pragma unroll
+            for (int c = 0; c < 64; ++c) r[c] = pack_bf16x2(s[2 * c], s[2 * c + 1]);
+            tmem_st64(tmem + lane_off + slot * 128, reinterpret_cast<uint32_t(&)[64]>(r));
+            tmem_st_wait();
+          }
+          const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+          const float2 a = __fadd2_rn(a01, a23);
+          l += a.x + a.y;
+          if (pending) {
+            if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) return false;
+            ++ow;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.p_full[slot]);
+          ++jc;
         }
-        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
-        const float2 a = __fadd2_rn(a01, a23);
-        l += a.x + a.y;
-        if (pending) {
-          if (!mbar_wait(&B.o_bar[o_idx], ow & 1, guard)) return false;
-          ++ow;
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&B.p_full[slot]);
-        ++jc;
         return true;
       };
       for (int n = R.nhi - 1; n >= R.nlo; --n) {

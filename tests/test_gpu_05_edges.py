@@ -2,6 +2,8 @@
 chunking, every decode head-dim variant with explicit splits, varlen with
 seqused_k, sequences with no keys, odd head counts, split-KV on prefill
 shapes, shifted diagonals and non-default scales."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -87,3 +89,25 @@ def test_decode_repeat_is_bitwise_stable():
     o1, l1 = gu.run_gpu(w)
     o2, l2 = gu.run_gpu(w)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def _bf16_bits(x: float) -> np.uint16:
+    return np.uint16(np.array([x], np.float32).view(np.uint32)[0] >> 16)
+
+
+@pytest.mark.parametrize("d,dv,wl", [(128, 128, -1), (64, 64, -1), (192, 128, -1), (256, 256, -1),
+                                     (128, 128, 100)])
+def test_masked_keys_with_scores_far_above_the_visible_ones(d, dv, wl):
+    """Keys a row must not see score about 150-290 (base 2, scaled) above every
+    key it sees, inside the same key block. A block max taken over all of a
+    masked block's columns would put every visible P of such a row below the
+    float range; the kernel must notice and use the visible max."""
+    w = inputs.batched("maskfar", 61, 1, 256, 256, 2, 1, d, dv, causal=True, window_left=wl)
+    q, k = w.q.copy(), w.k.copy()
+    q[..., 0] = _bf16_bits(8.0)
+    if wl < 0:
+        k[:, 64:128, :, 0] = _bf16_bits(200.0)    # rows 0-63 see none of these keys
+    else:
+        k[:, 0:100, :, 0] = _bf16_bits(200.0)     # rows 200+ see none of these keys
+    w = dataclasses.replace(w, q=q, k=k)
+    print(gu.check_workload(w))
