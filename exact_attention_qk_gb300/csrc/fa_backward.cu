@@ -448,13 +448,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tmem_ld64(tmem + lane_off + 64 * c, sv);
           const int lo_e = (c_hi < c_lo) ? 256 : c_lo;
           const uint32_t width = (c_hi < c_lo) ? 0u : static_cast<uint32_t>(c_hi - c_lo);
+          const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nl22 = make_float2(nl2, nl2);
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const float x = ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, nl2));
-            if constexpr (decltype(masked)::value)
-              pf[e] = (static_cast<uint32_t>(e - lo_e) <= width) ? x : 0.f;
-            else
-              pf[e] = x;
+          for (int e = 0; e < 64; e += 2) {
+            const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nl22);
+            const float x0 = ex2_approx(x2.x), x1 = ex2_approx(x2.y);
+            if constexpr (decltype(masked)::value) {
+              pf[e] = (static_cast<uint32_t>(e - lo_e) <= width) ? x0 : 0.f;
+              pf[e + 1] = (static_cast<uint32_t>(e + 1 - lo_e) <= width) ? x1 : 0.f;
+            } else {
+              pf[e] = x0;
+              pf[e + 1] = x1;
+            }
           }
         };
         if (full)
@@ -471,8 +476,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           uint32_t dp[64], w[32];
           tmem_ld64(tmem + lane_off + 128 + 64 * c, dp);
 #pragma unroll
+          const float2 nd2 = make_float2(-dsum, -dsum);
           for (int e = 0; e < 64; e += 2) {
-            float d0 = pf[e] * (__uint_as_float(dp[e]) - dsum), d1 = pf[e + 1] * (__uint_as_float(dp[e + 1]) - dsum);
+            const float2 d2 = __fmul2_rn(make_float2(pf[e], pf[e + 1]),
+                                         __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2));
+            float d0 = d2.x, d1 = d2.y;
             if (TAIL) {   // dP of keys past seqused_k may be NaN (their V rows are not data)
               d0 = pf[e] != 0.f ? d0 : 0.f;
               d1 = pf[e + 1] != 0.f ? d1 : 0.f;
@@ -694,12 +702,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             const float4 l4 = *reinterpret_cast<const float4*>(vl + e);
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float x = ex2_approx(fmaf(__uint_as_float(sv[e + q]), p.scale_log2, -lv[q]));
-              if constexpr (decltype(masked)::value)
-                pf[e + q] = (static_cast<uint32_t>(e + q - lo_e) <= width) ? x : 0.f;
-              else
-                pf[e + q] = x;
+            for (int q = 0; q < 4; q += 2) {
+              const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(sv[e + q]), __uint_as_float(sv[e + q + 1])),
+                                           make_float2(p.scale_log2, p.scale_log2), make_float2(-lv[q], -lv[q + 1]));
+              const float x0 = ex2_approx(x2.x), x1 = ex2_approx(x2.y);
+              if constexpr (decltype(masked)::value) {
+                pf[e + q] = (static_cast<uint32_t>(e + q - lo_e) <= width) ? x0 : 0.f;
+                pf[e + q + 1] = (static_cast<uint32_t>(e + q + 1 - lo_e) <= width) ? x1 : 0.f;
+              } else {
+                pf[e + q] = x0;
+                pf[e + q + 1] = x1;
+              }
             }
             pw[e >> 1] = pack_bf16x2(pf[e], pf[e + 1]);
             pw[(e >> 1) + 1] = pack_bf16x2(pf[e + 2], pf[e + 3]);
@@ -723,9 +736,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 64; e += 4) {
             const float4 d4 = *reinterpret_cast<const float4*>(vd + e);
-            dw[e >> 1] = pack_bf16x2(pf[e] * (__uint_as_float(dp[e]) - d4.x), pf[e + 1] * (__uint_as_float(dp[e + 1]) - d4.y));
-            dw[(e >> 1) + 1] = pack_bf16x2(pf[e + 2] * (__uint_as_float(dp[e + 2]) - d4.z),
-                                           pf[e + 3] * (__uint_as_float(dp[e + 3]) - d4.w));
+            const float2 a2 = __fmul2_rn(make_float2(pf[e], pf[e + 1]),
+                                         __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                                    make_float2(-d4.x, -d4.y)));
+            const float2 b2 = __fmul2_rn(make_float2(pf[e + 2], pf[e + 3]),
+                                         __fadd2_rn(make_float2(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])),
+                                                    make_float2(-d4.z, -d4.w)));
+            dw[e >> 1] = pack_bf16x2(a2.x, a2.y);
+            dw[(e >> 1) + 1] = pack_bf16x2(b2.x, b2.y);
           }
           tmem_st32(tmem + lane_off + 128 + 64 * c, dw);
         }
