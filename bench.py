@@ -384,10 +384,8 @@ def time_e2e(r: Runner, steps: int, warmup: int):
     ho = torch.empty(r.out.shape, dtype=torch.int16).pin_memory()
     hl = torch.empty(r.lse.shape, dtype=torch.float32).pin_memory()
     dq, dk, dv = bits(r.q), bits(r.k), bits(r.v)
-    # the small per-call inputs of a KV-cache form travel too
-    small = [(torch.from_numpy(np.ascontiguousarray(x)).pin_memory(), r.extra[name])
-             for name, x in (("k_descale", w.k_descale), ("v_descale", w.v_descale), ("page_table", w.page_table))
-             if name in r.extra]
+    # the small per-call inputs (sequence offsets and lengths, a KV-cache form's descales and page table) travel too
+    small = small_inputs(r)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv)) + \
         sum(h.numel() * h.element_size() for h, _ in small)
     d2h = ho.numel() * 2 + hl.numel() * 4
@@ -414,18 +412,33 @@ def time_e2e(r: Runner, steps: int, warmup: int):
     return a.elapsed_time(b) / steps, h2d, d2h
 
 
+def small_inputs(r: Runner):
+    """(pinned host copy, device tensor) of each small per-call input the step
+    reads: varlen offsets, seqused_k, fp8 descales, a page table."""
+    import numpy as np
+    w = r.w
+    src = (("cu_seqlens_q", w.cu_seqlens_q), ("cu_seqlens_k", w.cu_seqlens_k), ("seqused_k", w.seqused_k),
+           ("k_descale", w.k_descale), ("v_descale", w.v_descale), ("page_table", w.page_table))
+    return [(r.torch.from_numpy(np.ascontiguousarray(x)).pin_memory(), r.extra[name])
+            for name, x in src if name in r.extra]
+
+
 def time_e2e_bwd(r: Runner, steps: int, warmup: int):
     torch, fa = r.torch, r.fa
     dev_in = [r.q, r.k, r.v, r.out, r.lse, r.do]
     host_in = [(t.view(torch.int16) if t.dtype == torch.bfloat16 else t).cpu().pin_memory() for t in dev_in]
     host_out = [torch.empty(t.shape, dtype=torch.int16).pin_memory() for t in (r.dq, r.dk, r.dv)]
-    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    small = small_inputs(r)
+    h2d = sum(h.numel() * h.element_size() for h in host_in) + sum(h.numel() * h.element_size() for h, _ in small)
     d2h = sum(h.numel() * 2 for h in host_out)
 
     def one():
         for h, d in zip(host_in, dev_in):
             (d.view(torch.int16) if d.dtype == torch.bfloat16 else d).copy_(h, non_blocking=True)
-        fa.fa_bwd(r.q, r.k, r.v, r.out, r.lse, r.do, dq=r.dq, dk=r.dk, dv=r.dv, workspace=r.bws, **r.kw)
+        for h, d in small:
+            d.copy_(h, non_blocking=True)
+        fa.fa_bwd(r.q, r.k, r.v, r.out, r.lse, r.do, dq=r.dq, dk=r.dk, dv=r.dv, workspace=r.bws, **r.kw,
+                  **r.extra)
         for h, d in zip(host_out, (r.dq, r.dk, r.dv)):
             h.copy_(d.view(torch.int16), non_blocking=True)
 
@@ -486,7 +499,9 @@ def oracle_sample(w, budget_s: float, max_pairs=None):
             v = vv[bb:bb + 1, :s.sk, h // r:h // r + 1]
         t0 = time.perf_counter()
         if is_backward(w.name):
-            do = inputs.grad_out(dataclasses.replace(w, q=q, batch=1, num_heads_q=1))
+            # dO of this (sequence, head) pair alone, in the batched layout of q here
+            do = inputs.grad_out(dataclasses.replace(w, q=q, batch=1, num_heads_q=1, seqlen_q=q.shape[1],
+                                                     cu_seqlens_q=None, cu_seqlens_k=None))
             t0 = time.perf_counter()
             oracle.attention_backward(q, k, v, do, scale=w.softmax_scale, causal=w.causal,
                                       window_left=w.window_left, window_right=w.window_right)
@@ -666,7 +681,7 @@ def main():
 
 
 SECONDARY = ("dense", "tiny", "large_dense", "large_causal", "varlen", "decode", "decode_fp8", "decode_paged",
-             "causal_paged", "chunk_gqa", "chunk_single", "causal_bwd", "dense_bwd")
+             "causal_paged", "chunk_gqa", "chunk_single", "causal_bwd", "dense_bwd", "varlen_bwd")
 DATA = "synthetic (seeded N(0,1) bf16, numpy PCG64)"
 
 

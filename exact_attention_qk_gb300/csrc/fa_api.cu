@@ -709,18 +709,18 @@ static int bwd_impl(const fa_fwd_args* a, const void* dout, void* dq, void* dk, 
   const int64_t obs = r.varlen ? a->o_row_stride * sq : a->o_batch_stride;
   const int64_t kbs = r.varlen ? a->k_row_stride * sk : a->k_batch_stride;
   const int64_t vbs = r.varlen ? a->v_row_stride * sk : a->v_batch_stride;
-  const int d = a->head_dim_qk;
+  const int d = a->head_dim_qk, d_v = a->head_dim_v;
   // the maps of an empty side are stand-ins (copies of the other side's), never read
   CUtensorMap mq, mk, mv, mdo;
   if (has_q && (!make_map(&mq, a->q, d, sq, a->num_heads_q, nb, a->q_row_stride, a->q_head_stride, qbs, 128) ||
-                !make_map(&mdo, dout, d, sq, a->num_heads_q, nb, a->o_row_stride, a->o_head_stride, obs, 128)))
+                !make_map(&mdo, dout, d_v, sq, a->num_heads_q, nb, a->o_row_stride, a->o_head_stride, obs, 128)))
     return FA_ERR_CUDA;
   if (has_k && (!make_map(&mk, a->k, d, sk, a->num_heads_kv, nb, a->k_row_stride, a->k_head_stride, kbs, 128) ||
-                !make_map(&mv, a->v, d, sk, a->num_heads_kv, nb, a->v_row_stride, a->v_head_stride, vbs, 128)))
+                !make_map(&mv, a->v, d_v, sk, a->num_heads_kv, nb, a->v_row_stride, a->v_head_stride, vbs, 128)))
     return FA_ERR_CUDA;
   if (!has_q) mq = mdo = mk;
   if (!has_k) mk = mv = mq;
-  cudaError_t e = launch_bwd(p, d, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream), side);
+  cudaError_t e = launch_bwd(p, d, d_v, mq, mk, mv, mdo, static_cast<cudaStream_t>(stream), side);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -21,7 +21,12 @@
 //     memory, dV += P^T dO and dK += dS^T Q.
 //
 // Tensor memory (512 columns, one CTA per SM): S [0,128), dP [128,256),
-// accumulators from 256 (dQ; or dV then dK). Two warpgroups share each
+// accumulators from 256 (dQ; or dV then dK). With the (192, 128) head dims
+// dV and dK together (128 + 192 columns) do not fit beside S and dP, so the
+// dK/dV kernel runs as two launches: a dV-only pass (S^T, P^T, dV += P^T dO)
+// and a dK-only pass (S^T, dP^T, dS^T, dK += dS^T Q). Where shared memory holds
+// a single stage of the streamed pair, the MMA thread issues the next job's
+// GEMMs only after the current job has released the stage. Two warpgroups share each
 // 128 x 128 score block, warpgroup c taking columns [64c, 64c+64) for all 128
 // rows, in two phases: P from S (the dK/dV kernel writes P^T back in bf16),
 // then dS from dP and the P kept in registers, back in bf16. A bf16 result of
@@ -51,14 +56,24 @@ namespace {
 constexpr int kB = 128;                 // rows of a query tile and of a key block
 constexpr int kChunk = 128 * 128;       // bytes of 128 rows x 64 bf16 columns (one 128B-swizzle chunk)
 
-template <int D>
+// Passes of the dK/dV kernel: both accumulators (head dims 64 and 128), or
+// the dV-only and dK-only passes of the (192, 128) head dims.
+enum : int { kBoth = 0, kDvOnly = 1, kDkOnly = 2 };
+
+template <int DK_, int DV_, int MODE_ = kBoth>
 struct BwdCfg {
-  static constexpr int CH = D / 64;                    // 64-column chunks of a row
-  static constexpr int T_BYTES = CH * kChunk;          // one 128-row tile
-  static constexpr int ST = 2;                         // stages of the streamed tile pair
-  static constexpr int OFF_RES = 0;                    // resident pair: Q, dO (dQ) or K, V (dK/dV)
-  static constexpr int OFF_STR = 2 * T_BYTES;          // streamed pairs: K, V (dQ) or Q, dO (dK/dV)
-  static constexpr int OFF_VEC = OFF_STR + ST * 2 * T_BYTES;   // dK/dV: lse2[128], D[128] per stage
+  static constexpr int DK = DK_, DV = DV_, MODE = MODE_;
+  static constexpr int CQ = DK / 64, CV = DV / 64;     // 64-column chunks of a Q or K row, of a dO or V row
+  static constexpr int TQ = CQ * kChunk;               // one 128-row tile of Q or K
+  static constexpr int TV = CV * kChunk;               // one 128-row tile of dO or V
+  static constexpr int PAIR = TQ + TV;
+  // resident: Q, dO (dQ) or K, V (dK/dV; K alone in the dV-only pass)
+  static constexpr int RES = (MODE == kDvOnly) ? TQ : PAIR;
+  // stages of the streamed pair (K, V for dQ; Q, dO and lse2 / D for dK/dV): two where they fit
+  static constexpr int ST = (RES + 2 * (PAIR + 1024) + 2048 <= 227 * 1024) ? 2 : 1;
+  static constexpr int OFF_RES = 0;
+  static constexpr int OFF_STR = RES;
+  static constexpr int OFF_VEC = OFF_STR + ST * PAIR;  // dK/dV: lse2[128], D[128] per stage
   static constexpr int OFF_BAR = OFF_VEC + ST * 1024;
   static constexpr int NBAR = 16;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
@@ -68,7 +83,7 @@ struct BwdCfg {
   static constexpr int THREADS = 320;
   static constexpr int TMA_WARP = 8, MMA_WARP = 9;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(256 + 2 * D <= 512, "tensor memory budget");
+  static_assert(OFF_STR % 1024 == 0 && PAIR % 1024 == 0, "128B-swizzled tiles start 1024-byte aligned");
 };
 
 struct BBars {
@@ -257,12 +272,13 @@ __global__ void __launch_bounds__(1024) bwd_preprocess_kernel(const BwdParams p,
 }
 
 // ---------------------------------------------------------------------------
-template <int D, bool TAIL>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+template <int DK, int DV, bool TAIL>
+__global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                   const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
                   const BwdParams p) {
-  using Cfg = BwdCfg<D>;
+  using Cfg = BwdCfg<DK, DV>;
+  static_assert(256 + DK <= 512, "tensor memory budget");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, offset from the array itself so that accesses
   // through it stay shared-memory accesses with 32-bit addressing
@@ -311,11 +327,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tma_prefetch_desc(&mapV);
         tma_prefetch_desc(&mapDO);
         uint8_t* res = smem + Cfg::OFF_RES;
-        mbar_arrive_expect_tx(B.res_full, 2 * Cfg::T_BYTES);
+        mbar_arrive_expect_tx(B.res_full, Cfg::PAIR);
 #pragma unroll
-        for (int c = 0; c < Cfg::CH; ++c) {
-          tma_load_4d(res + c * kChunk, &mapQ, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
-          tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapDO, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
+        for (int c = 0; c < (Cfg::CQ > Cfg::CV ? Cfg::CQ : Cfg::CV); ++c) {
+          if (c < Cfg::CQ) tma_load_4d(res + c * kChunk, &mapQ, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
+          if (c < Cfg::CV)
+            tma_load_4d(res + Cfg::TQ + c * kChunk, &mapDO, B.res_full, c * 64, S.q_row0 + i0, h, S.bc);
         }
       }
       constexpr unsigned wmask = TAIL ? 0xffffffffu : 1u;
@@ -323,17 +340,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (lane == 0 || TAIL) {
         for (int n = nhi - 1; n >= nlo; --n, ++u) {
           const int st = u % Cfg::ST;
-          uint8_t* dst = smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES;
+          uint8_t* dst = smem + Cfg::OFF_STR + st * Cfg::PAIR;
           bool w = true;
           if (lane == 0) {
             w = u < Cfg::ST || mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard);
             if (w) {
-              mbar_arrive_expect_tx(&B.str_full[st], 2 * Cfg::T_BYTES);
+              mbar_arrive_expect_tx(&B.str_full[st], Cfg::PAIR);
 #pragma unroll
-              for (int c = 0; c < Cfg::CH; ++c) {
-                tma_load_4d(dst + c * kChunk, &mapK, &B.str_full[st], c * 64, S.k_row0 + n * kB, g, S.bc);
-                tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapV, &B.str_full[st], c * 64, S.k_row0 + n * kB, g,
-                            S.bc);
+              for (int c = 0; c < (Cfg::CQ > Cfg::CV ? Cfg::CQ : Cfg::CV); ++c) {
+                if (c < Cfg::CQ)
+                  tma_load_4d(dst + c * kChunk, &mapK, &B.str_full[st], c * 64, S.k_row0 + n * kB, g, S.bc);
+                if (c < Cfg::CV)
+                  tma_load_4d(dst + Cfg::TQ + c * kChunk, &mapV, &B.str_full[st], c * 64, S.k_row0 + n * kB, g,
+                              S.bc);
               }
             }
           }
@@ -341,9 +360,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           const int valid = S.sk - n * kB;
           if (TAIL && valid < kB) {
             if (!__all_sync(wmask, mbar_wait(&B.str_full[st], (u / Cfg::ST) & 1, guard))) break;
-            const int pieces = (min(kB, (valid + 15) & ~15) - valid) * Cfg::CH * 8;   // 16-byte pieces
+            const int pieces = (min(kB, (valid + 15) & ~15) - valid) * Cfg::CQ * 8;   // 16-byte pieces of K
             for (int idx = lane; idx < pieces; idx += 32) {
-              const int row = valid + idx / (Cfg::CH * 8), rem = idx % (Cfg::CH * 8);
+              const int row = valid + idx / (Cfg::CQ * 8), rem = idx % (Cfg::CQ * 8);
               *reinterpret_cast<uint4*>(dst + (rem >> 3) * kChunk + row * 128 + (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
@@ -365,25 +384,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // so that dP(u) runs while the warps form P(u), S(u+1) while they form
       // dS(u), and dQ(u) and dP(u+1) while they form P(u+1). dS(u) lives in
       // dP's columns, which dP(u+1) only overwrites after dQ(u) has read them
-      // (the tensor pipe runs one thread's MMAs in order).
+      // (the tensor pipe runs one thread's MMAs in order). With one stage,
+      // S(u+1) needs K(u+1), which loads only once dQ(u) has released the
+      // stage: ... [dS(u)] dQ(u) | S(u+1) dP(u+1).
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
-      constexpr uint32_t IDESC_DQ = idesc_bf16_f32(kB, D, false, true);
-      const uint32_t q_base = smem_u32(smem + Cfg::OFF_RES), do_base = q_base + Cfg::T_BYTES;
+      constexpr uint32_t IDESC_DQ = idesc_bf16_f32(kB, DK, false, true);
+      const uint32_t q_base = smem_u32(smem + Cfg::OFF_RES), do_base = q_base + Cfg::TQ;
       const uint32_t nb = static_cast<uint32_t>(nhi - nlo);
-      auto kv = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * 2 * Cfg::T_BYTES); };
+      auto kv = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * Cfg::PAIR); };
       bool ok = mbar_wait(B.res_full, 0, guard) && mbar_wait(&B.str_full[0], 0, guard);
       if (ok) {
-        issue_ss(tmem, q_base, kv(0), D, IDESC_S);                          // S  = Q K^T
+        issue_ss(tmem, q_base, kv(0), DK, IDESC_S);                         // S  = Q K^T
         mma_commit(B.s_full);
-        issue_ss(tmem + 128, do_base, kv(0) + Cfg::T_BYTES, D, IDESC_S);    // dP = dO V^T
+        issue_ss(tmem + 128, do_base, kv(0) + Cfg::TQ, DV, IDESC_S);        // dP = dO V^T
         mma_commit(B.dp_full);
       }
       for (uint32_t u = 0; ok && u < nb; ++u) {
         if (!mbar_wait(&B.p_done[0], u & 1, guard) || !mbar_wait(&B.p_done[1], u & 1, guard)) { ok = false; break; }
-        if (u + 1 < nb) {
+        if (Cfg::ST > 1 && u + 1 < nb) {
           if (!mbar_wait(&B.str_full[(u + 1) % Cfg::ST], ((u + 1) / Cfg::ST) & 1, guard)) { ok = false; break; }
           tc_fence_after();
-          issue_ss(tmem, q_base, kv(u + 1), D, IDESC_S);
+          issue_ss(tmem, q_base, kv(u + 1), DK, IDESC_S);
           mma_commit(B.s_full);
         }
         // the last, partly used key block (seqused_k): K cleared up to the next
@@ -404,7 +425,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (!ok) break;
         mma_commit(&B.str_empty[u % Cfg::ST]);
         if (u + 1 < nb) {
-          issue_ss(tmem + 128, do_base, kv(u + 1) + Cfg::T_BYTES, D, IDESC_S);
+          if (Cfg::ST == 1) {
+            if (!mbar_wait(&B.str_full[0], (u + 1) & 1, guard)) { ok = false; break; }
+            tc_fence_after();
+            issue_ss(tmem, q_base, kv(u + 1), DK, IDESC_S);
+            mma_commit(B.s_full);
+          }
+          issue_ss(tmem + 128, do_base, kv(u + 1) + Cfg::TQ, DV, IDESC_S);
           mma_commit(B.dp_full);
         }
       }
@@ -422,7 +449,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const int i = i0 + t;
     const int64_t vrow = ws_row0(p, b, h) + i;   // inside the sequence's 128-row padded region
     __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(p.dq) + int64_t(S.bc) * p.q_bs +
-                        int64_t(S.q_row0 + i) * p.q_rs + int64_t(h) * p.q_hs + c * (D / 2);
+                        int64_t(S.q_row0 + i) * p.q_rs + int64_t(h) * p.q_hs + c * (DK / 2);
     if (has) {
       const float nl2 = -p.lse2[vrow], dsum = p.dsum[vrow];
       bool ok = true;
@@ -496,16 +523,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       if (ok && mbar_wait(B.acc_full, 0, guard)) {
         tc_fence_after();
-        // warpgroup c writes dQ columns [c D/2, (c+1) D/2)
+        // warpgroup c writes dQ columns [c DK/2, (c+1) DK/2)
 #pragma unroll 1
-        for (int k = 0; k < D / 64; ++k) {
+        for (int k = 0; k < DK / 64; ++k) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + 256 + c * (D / 2) + k * 32, o);
+          tmem_ld32(tmem + lane_off + 256 + c * (DK / 2) + k * 32, o);
           if (i < S.sq) store_row32(dq + k * 32, o, p.scale);
         }
       }
     } else if (i < S.sq) {
-      zero_row(dq, D / 2);   // no visible key: dQ = 0
+      zero_row(dq, DK / 2);   // no visible key: dQ = 0
     }
   }
 
@@ -518,12 +545,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int D, bool TAIL>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+template <int DK, int DV, bool TAIL, int MODE>
+__global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                     const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
                     const BwdParams p) {
-  using Cfg = BwdCfg<D>;
+  using Cfg = BwdCfg<DK, DV, MODE>;
+  static_assert(256 + (MODE == kBoth ? DK + DV : MODE == kDvOnly ? DV : DK) <= 512, "tensor memory budget");
+  constexpr bool kDv = MODE != kDkOnly, kDk = MODE != kDvOnly;   // accumulators of this pass
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, offset from the array itself so that accesses
   // through it stay shared-memory accesses with 32-bit addressing
@@ -537,14 +566,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const int n = blockIdx.y;   // low key blocks first: under a causal mask they see the most query tiles
   const BSeq S = bwd_seq(p, b);
   if (n * kB >= S.sk) {   // a block past this sequence's keys (whole CTA, before any barrier)
-    if (TAIL) {   // cache rows past seqused_k: dK = dV = 0
+    if (TAIL) {   // cache rows past seqused_k: dK = dV = 0 (this pass's accumulators)
       for (int idx = threadIdx.x; idx < 2 * kB; idx += blockDim.x) {
         const int j = n * kB + (idx >> 1);
-        if (j >= S.ska) continue;
-        __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(idx & 1 ? p.dk : p.dv) +
-                             int64_t(S.bc) * (idx & 1 ? p.k_bs : p.v_bs) +
-                             int64_t(S.k_row0 + j) * (idx & 1 ? p.k_rs : p.v_rs) + int64_t(g) * (idx & 1 ? p.k_hs : p.v_hs);
-        zero_row(row, D);
+        const bool is_k = idx & 1;
+        if (j >= S.ska || (is_k ? !kDk : !kDv)) continue;
+        __nv_bfloat16* row = reinterpret_cast<__nv_bfloat16*>(is_k ? p.dk : p.dv) +
+                             int64_t(S.bc) * (is_k ? p.k_bs : p.v_bs) +
+                             int64_t(S.k_row0 + j) * (is_k ? p.k_rs : p.v_rs) + int64_t(g) * (is_k ? p.k_hs : p.v_hs);
+        zero_row(row, is_k ? DK : DV);
       }
     }
     return;
@@ -579,25 +609,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&mapV);
       tma_prefetch_desc(&mapDO);
       uint8_t* res = smem + Cfg::OFF_RES;
-      mbar_arrive_expect_tx(B.res_full, 2 * Cfg::T_BYTES);
+      mbar_arrive_expect_tx(B.res_full, Cfg::RES);
 #pragma unroll
-      for (int c = 0; c < Cfg::CH; ++c) {
-        tma_load_4d(res + c * kChunk, &mapK, B.res_full, c * 64, S.k_row0 + j0, g, S.bc);
-        tma_load_4d(res + Cfg::T_BYTES + c * kChunk, &mapV, B.res_full, c * 64, S.k_row0 + j0, g, S.bc);
+      for (int c = 0; c < (Cfg::CQ > Cfg::CV ? Cfg::CQ : Cfg::CV); ++c) {
+        if (c < Cfg::CQ) tma_load_4d(res + c * kChunk, &mapK, B.res_full, c * 64, S.k_row0 + j0, g, S.bc);
+        if (kDk && c < Cfg::CV)   // V feeds dP^T only
+          tma_load_4d(res + Cfg::TQ + c * kChunk, &mapV, B.res_full, c * 64, S.k_row0 + j0, g, S.bc);
       }
       uint32_t u = 0;
       for (; u < static_cast<uint32_t>(jobs); ++u) {
         const int st = u % Cfg::ST;
         const int hh = g * p.r + static_cast<int>(u) / nm, m = mlo + static_cast<int>(u) % nm;
         if (u >= Cfg::ST && !mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard)) break;
-        uint8_t* dst = smem + Cfg::OFF_STR + st * 2 * Cfg::T_BYTES;
+        uint8_t* dst = smem + Cfg::OFF_STR + st * Cfg::PAIR;
         float* vec = reinterpret_cast<float*>(smem + Cfg::OFF_VEC + st * 1024);
         const int64_t vrow = ws_row0(p, b, hh) + m * kB;
-        mbar_arrive_expect_tx(&B.str_full[st], 2 * Cfg::T_BYTES + 1024);
+        mbar_arrive_expect_tx(&B.str_full[st], Cfg::PAIR + 1024);
 #pragma unroll
-        for (int c = 0; c < Cfg::CH; ++c) {
-          tma_load_4d(dst + c * kChunk, &mapQ, &B.str_full[st], c * 64, S.q_row0 + m * kB, hh, S.bc);
-          tma_load_4d(dst + Cfg::T_BYTES + c * kChunk, &mapDO, &B.str_full[st], c * 64, S.q_row0 + m * kB, hh, S.bc);
+        for (int c = 0; c < (Cfg::CQ > Cfg::CV ? Cfg::CQ : Cfg::CV); ++c) {
+          if (c < Cfg::CQ)
+            tma_load_4d(dst + c * kChunk, &mapQ, &B.str_full[st], c * 64, S.q_row0 + m * kB, hh, S.bc);
+          if (c < Cfg::CV)
+            tma_load_4d(dst + Cfg::TQ + c * kChunk, &mapDO, &B.str_full[st], c * 64, S.q_row0 + m * kB, hh, S.bc);
         }
         bulk_load(vec, p.lse2 + vrow, 512, &B.str_full[st]);
         bulk_load(vec + 128, p.dsum + vrow, 512, &B.str_full[st]);
@@ -613,43 +646,62 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // they form dS(u), and dK(u) and dP(u+1) while they form P(u+1). P^T(u)
       // and dS^T(u) live in S's and dP's columns, which S(u+1) and dP(u+1) only
       // overwrite after dV(u) and dK(u) have read them (one thread's MMAs run
-      // in order).
+      // in order). The dV-only pass drops dP and dK, the dK-only pass dV (its
+      // S(u+1) then waits only for the warps to have read S(u)). With one stage,
+      // S(u+1) needs Q(u+1), which loads only once the job's last GEMM has
+      // released the stage: ... dK(u) | S(u+1) dP(u+1).
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
-      constexpr uint32_t IDESC_ACC = idesc_bf16_f32(kB, D, false, true);
-      const uint32_t k_base = smem_u32(smem + Cfg::OFF_RES), v_base = k_base + Cfg::T_BYTES;
+      constexpr uint32_t IDESC_DV = idesc_bf16_f32(kB, DV, false, true);
+      constexpr uint32_t IDESC_DK = idesc_bf16_f32(kB, DK, false, true);
+      constexpr uint32_t DV_COL = 256, DK_COL = (MODE == kBoth) ? 256 + DV : 256;
+      const uint32_t k_base = smem_u32(smem + Cfg::OFF_RES), v_base = k_base + Cfg::TQ;
       const uint32_t nj = static_cast<uint32_t>(jobs);
-      auto qs = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * 2 * Cfg::T_BYTES); };
+      auto qs = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * Cfg::PAIR); };
       bool ok = mbar_wait(B.res_full, 0, guard) && mbar_wait(&B.str_full[0], 0, guard);
       if (ok) {
-        issue_ss(tmem, k_base, qs(0), D, IDESC_S);                         // S^T  = K Q^T
+        issue_ss(tmem, k_base, qs(0), DK, IDESC_S);                          // S^T  = K Q^T
         mma_commit(B.s_full);
-        issue_ss(tmem + 128, v_base, qs(0) + Cfg::T_BYTES, D, IDESC_S);    // dP^T = V dO^T
-        mma_commit(B.dp_full);
+        if constexpr (kDk) {
+          issue_ss(tmem + 128, v_base, qs(0) + Cfg::TQ, DV, IDESC_S);        // dP^T = V dO^T
+          mma_commit(B.dp_full);
+        }
       }
       for (uint32_t u = 0; ok && u < nj; ++u) {
-        const uint32_t qb = qs(u), dob = qb + Cfg::T_BYTES;
+        const uint32_t qb = qs(u), dob = qb + Cfg::TQ;
         const bool acc = u > 0;
         for (int c = 0; c < 2; ++c) {
           if (!mbar_wait(&B.p_done[c], u & 1, guard)) { ok = false; break; }
-          tc_fence_after();
-          issue_ts_half(tmem + 256, tmem, dob, c, IDESC_ACC, acc || c > 0);   // dV += P^T_c dO_c
+          if constexpr (kDv) {
+            tc_fence_after();
+            issue_ts_half(tmem + DV_COL, tmem, dob, c, IDESC_DV, acc || c > 0);   // dV += P^T_c dO_c
+          }
         }
         if (!ok) break;
-        if (u + 1 < nj) {
+        if (Cfg::ST > 1 && u + 1 < nj) {
           if (!mbar_wait(&B.str_full[(u + 1) % Cfg::ST], ((u + 1) / Cfg::ST) & 1, guard)) { ok = false; break; }
-          issue_ss(tmem, k_base, qs(u + 1), D, IDESC_S);
+          issue_ss(tmem, k_base, qs(u + 1), DK, IDESC_S);
           mma_commit(B.s_full);
         }
-        for (int c = 0; c < 2; ++c) {
-          if (!mbar_wait(&B.ds_full[c], u & 1, guard)) { ok = false; break; }
-          tc_fence_after();
-          issue_ts_half(tmem + 256 + D, tmem + 128, qb, c, IDESC_ACC, acc || c > 0);   // dK += dS^T_c Q_c
+        if constexpr (kDk) {
+          for (int c = 0; c < 2; ++c) {
+            if (!mbar_wait(&B.ds_full[c], u & 1, guard)) { ok = false; break; }
+            tc_fence_after();
+            issue_ts_half(tmem + DK_COL, tmem + 128, qb, c, IDESC_DK, acc || c > 0);   // dK += dS^T_c Q_c
+          }
+          if (!ok) break;
         }
-        if (!ok) break;
         mma_commit(&B.str_empty[u % Cfg::ST]);
         if (u + 1 < nj) {
-          issue_ss(tmem + 128, v_base, qs(u + 1) + Cfg::T_BYTES, D, IDESC_S);
-          mma_commit(B.dp_full);
+          if (Cfg::ST == 1) {
+            if (!mbar_wait(&B.str_full[0], (u + 1) & 1, guard)) { ok = false; break; }
+            tc_fence_after();
+            issue_ss(tmem, k_base, qs(u + 1), DK, IDESC_S);
+            mma_commit(B.s_full);
+          }
+          if constexpr (kDk) {
+            issue_ss(tmem + 128, v_base, qs(u + 1) + Cfg::TQ, DV, IDESC_S);
+            mma_commit(B.dp_full);
+          }
         }
       }
       if (ok) mma_commit(B.acc_full);
@@ -668,6 +720,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                         int64_t(S.k_row0 + j) * p.k_rs + int64_t(g) * p.k_hs;
     __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(p.dv) + int64_t(S.bc) * p.v_bs +
                         int64_t(S.k_row0 + j) * p.v_rs + int64_t(g) * p.v_hs;
+    // the accumulator columns this warpgroup writes: with both, warpgroup 0 all
+    // of dV and warpgroup 1 all of dK (times the softmax scale); in a one-
+    // accumulator pass, warpgroup c its half [c n/2, (c+1) n/2)
+    constexpr int kOut = (MODE == kDkOnly) ? DK : DV;
+    auto out_cols = [&]() { return (MODE == kBoth) ? (c == 0 ? DV : DK) : kOut / 2; };
+    auto out_row = [&]() {
+      const bool wdk = (MODE == kBoth) ? c == 1 : MODE == kDkOnly;
+      return (wdk ? dk : dv) + ((MODE == kBoth) ? 0 : c * (kOut / 2));
+    };
     if (jobs > 0) {
       bool ok = true;
       for (uint32_t u = 0; u < static_cast<uint32_t>(jobs); ++u) {
@@ -717,16 +778,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             pw[e >> 1] = pack_bf16x2(pf[e], pf[e + 1]);
             pw[(e >> 1) + 1] = pack_bf16x2(pf[e + 2], pf[e + 3]);
           }
-          tmem_st32(tmem + lane_off + 64 * c, pw);
+          if constexpr (kDv) tmem_st32(tmem + lane_off + 64 * c, pw);   // P^T feeds dV only
         };
         if (full)
           p_phase(std::false_type{});
         else
           p_phase(std::true_type{});
-        tmem_st_wait();
+        if constexpr (kDv) tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.p_done[c]);
+        if constexpr (!kDk) continue;
         // dS^T = P^T (dP^T - D), bf16 into the first 32 columns of this half of dP^T
         if (!mbar_wait(B.dp_full, u & 1, guard)) { ok = false; break; }
         tc_fence_after();
@@ -754,19 +816,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       if (ok && mbar_wait(B.acc_full, 0, guard)) {
         tc_fence_after();
-        // warpgroup 0 writes dV, warpgroup 1 dK (times the softmax scale)
-        __nv_bfloat16* dst = c == 0 ? dv : dk;
-        const float f = c == 0 ? 1.f : p.scale;
+        const bool wdk = (MODE == kBoth) ? c == 1 : MODE == kDkOnly;
+        const int ocols = out_cols();
+        const uint32_t ocol = (MODE == kBoth) ? 256 + c * DV : 256 + c * (kOut / 2);
+        __nv_bfloat16* dst = out_row();
+        const float f = wdk ? p.scale : 1.f;
 #pragma unroll 1
-        for (int k = 0; k < D / 32; ++k) {
+        for (int k = 0; k < ocols / 32; ++k) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + 256 + c * D + k * 32, o);
+          tmem_ld32(tmem + lane_off + ocol + k * 32, o);
           if (j < S.sk) store_row32(dst + k * 32, o, f);
         }
-        if (TAIL && j >= S.sk && j < S.ska) zero_row(dst, D);   // cache rows past seqused_k
+        if (TAIL && j >= S.sk && j < S.ska) zero_row(dst, ocols);   // cache rows past seqused_k
       }
     } else if (j < (TAIL ? S.ska : S.sk)) {
-      zero_row(c == 0 ? dv : dk, D);   // no query sees these keys (or they are past seqused_k)
+      zero_row(out_row(), out_cols());   // no query sees these keys (or they are past seqused_k)
     }
   }
 
@@ -778,22 +842,61 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool TAIL>
+template <int DK, int DV, bool TAIL, int MODE>
+cudaError_t launch_dkdv(const BwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const CUtensorMap& mdo, dim3 grid, cudaStream_t stream) {
+  using Cfg = BwdCfg<DK, DV, MODE>;
+  bwd_dkdv_kernel<DK, DV, TAIL, MODE><<<grid, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError();
+}
+
+// dK and dV: one launch with both accumulators, or the dV-only and dK-only passes
+template <int DK, int DV, bool TAIL>
+constexpr bool kOnePass = 256 + DK + DV <= 512;
+
+template <int DK, int DV, bool TAIL>
+cudaError_t set_dkdv_smem() {   // (host calls kept ahead of the launches: they delay them otherwise)
+  if constexpr (kOnePass<DK, DV, TAIL>) {
+    return cudaFuncSetAttribute(bwd_dkdv_kernel<DK, DV, TAIL, kBoth>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                BwdCfg<DK, DV, kBoth>::SMEM);
+  } else {
+    const cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<DK, DV, TAIL, kDvOnly>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               BwdCfg<DK, DV, kDvOnly>::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(bwd_dkdv_kernel<DK, DV, TAIL, kDkOnly>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                BwdCfg<DK, DV, kDkOnly>::SMEM);
+  }
+}
+
+template <int DK, int DV, bool TAIL>
+cudaError_t launch_dkdv_all(const BwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const CUtensorMap& mdo, dim3 grid, cudaStream_t stream) {
+  if constexpr (kOnePass<DK, DV, TAIL>) {
+    return launch_dkdv<DK, DV, TAIL, kBoth>(p, mq, mk, mv, mdo, grid, stream);
+  } else {
+    const cudaError_t e = launch_dkdv<DK, DV, TAIL, kDvOnly>(p, mq, mk, mv, mdo, grid, stream);
+    if (e != cudaSuccess) return e;
+    return launch_dkdv<DK, DV, TAIL, kDkOnly>(p, mq, mk, mv, mdo, grid, stream);
+  }
+}
+
+template <int DK, int DV, bool TAIL>
 cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, cudaStream_t stream, const BwdSide& side) {
-  using Cfg = BwdCfg<D>;
+  using Cfg = BwdCfg<DK, DV>;
   // batched: every sequence's lengths; varlen: the longest (CTAs past a
   // shorter sequence's end return at once)
   const int mblocks = (p.seqlen_q + kB - 1) / kB, nblocks = (p.seqlen_k + kB - 1) / kB;
   if (mblocks > 0 && p.batch > 0) {
-    bwd_preprocess_kernel<<<dim3(p.batch * mblocks, p.hq), 1024, 0, stream>>>(p, D, mblocks);
+    bwd_preprocess_kernel<<<dim3(p.batch * mblocks, p.hq), 1024, 0, stream>>>(p, DV, mblocks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<DK, DV, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-  if (e != cudaSuccess) return e;
+  if ((e = set_dkdv_smem<DK, DV, TAIL>()) != cudaSuccess) return e;
   const dim3 gq(p.batch * p.hq, mblocks), gk(p.batch * p.hkv, nblocks);
   if (mblocks > 0 && nblocks > 0 && side.stream != nullptr) {
     // The two kernels only share read-only inputs. dK/dV (few long CTAs under
@@ -803,19 +906,17 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtens
     // fork the second stream from `stream` and join it back.
     if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess) return e;
-    bwd_dkdv_kernel<D, TAIL><<<gk, Cfg::THREADS, Cfg::SMEM, side.stream>>>(mq, mk, mv, mdo, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_dq_kernel<D, TAIL><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+    if ((e = launch_dkdv_all<DK, DV, TAIL>(p, mq, mk, mv, mdo, gk, side.stream)) != cudaSuccess) return e;
+    bwd_dq_kernel<DK, DV, TAIL><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
     return cudaStreamWaitEvent(stream, side.join, 0);
   }
   if (nblocks > 0) {   // one stream: dK/dV, then dQ
-    bwd_dkdv_kernel<D, TAIL><<<gk, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dkdv_all<DK, DV, TAIL>(p, mq, mk, mv, mdo, gk, stream)) != cudaSuccess) return e;
   }
   if (mblocks > 0) {
-    bwd_dq_kernel<D, TAIL><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
+    bwd_dq_kernel<DK, DV, TAIL><<<gq, Cfg::THREADS, Cfg::SMEM, stream>>>(mq, mk, mv, mdo, p);
     return cudaGetLastError();
   }
   return cudaSuccess;
@@ -823,16 +924,23 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtens
 
 }  // namespace
 
-bool bwd_supported(int dk, int dv) { return (dk == 64 && dv == 64) || (dk == 128 && dv == 128); }
+bool bwd_supported(int dk, int dv) {
+  return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128);
+}
 
-cudaError_t launch_bwd(const BwdParams& p, int d, const CUtensorMap& mq, const CUtensorMap& mk,
+cudaError_t launch_bwd(const BwdParams& p, int dk, int dv, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream, const BwdSide& side) {
   // the TAIL instances handle key caches with unused rows (seqused_k)
   const bool tail = p.seqused_k != nullptr;
-  if (d == 64) return tail ? launch_bwd_t<64, true>(p, mq, mk, mv, mdo, stream, side)
-                           : launch_bwd_t<64, false>(p, mq, mk, mv, mdo, stream, side);
-  if (d == 128) return tail ? launch_bwd_t<128, true>(p, mq, mk, mv, mdo, stream, side)
-                            : launch_bwd_t<128, false>(p, mq, mk, mv, mdo, stream, side);
+  if (dk == 64 && dv == 64)
+    return tail ? launch_bwd_t<64, 64, true>(p, mq, mk, mv, mdo, stream, side)
+                : launch_bwd_t<64, 64, false>(p, mq, mk, mv, mdo, stream, side);
+  if (dk == 128 && dv == 128)
+    return tail ? launch_bwd_t<128, 128, true>(p, mq, mk, mv, mdo, stream, side)
+                : launch_bwd_t<128, 128, false>(p, mq, mk, mv, mdo, stream, side);
+  if (dk == 192 && dv == 128)
+    return tail ? launch_bwd_t<192, 128, true>(p, mq, mk, mv, mdo, stream, side)
+                : launch_bwd_t<192, 128, false>(p, mq, mk, mv, mdo, stream, side);
   return cudaErrorInvalidValue;
 }
 

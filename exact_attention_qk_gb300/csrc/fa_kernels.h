@@ -99,7 +99,7 @@ struct BwdSide {
   cudaStream_t stream;
   cudaEvent_t fork, join;
 };
-cudaError_t launch_bwd(const BwdParams& p, int d, const CUtensorMap& mq, const CUtensorMap& mk,
+cudaError_t launch_bwd(const BwdParams& p, int dk, int dv, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t stream, const BwdSide& side);
 bool bwd_supported(int dk, int dv);
 

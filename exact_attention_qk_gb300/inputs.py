@@ -40,6 +40,8 @@ Backward workloads (dQ, dK, dV given dO; dO is N(0,1) bf16 from its own stream):
 
   causal_bwd    the causal prefill shape (B=2 Hq=32 Hkv=4 S=4096 D=128)
   dense_bwd     the same shape without a mask
+  varlen_bwd    the varlen sliding-window workload (Dqk=192 Dv=128; the same
+                q, k, v draws)
 """
 from __future__ import annotations
 
@@ -291,9 +293,9 @@ def workload(name: str) -> Workload:
     if name in ("large_dense", "large_causal"):
         return batched(name, 3, 1, 8192, 8192, 16, 2, 256, 256, scale=1.0 / 16,
                        causal=(name == "large_causal"))
-    if name == "varlen":
+    if name in ("varlen", "varlen_bwd"):
         lens = varlen_lengths()
-        return packed("varlen", 4, lens, lens, 16, 16, 192, 128, causal=True,
+        return packed(name, 4, lens, lens, 16, 16, 192, 128, causal=True,
                       window_left=1024, window_right=0)
     if name == "decode":
         return batched("decode", 5, 64, 1, 16384, 32, 8, 128, 128, seqused_k=decode_seqused())
@@ -328,4 +330,5 @@ def workload(name: str) -> Workload:
 
 WORKLOADS = ("tiny", "causal", "dense", "large_dense", "large_causal", "varlen", "decode", "decode_small",
              "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
-             "decode_fp8_small", "decode_paged_small", "causal_bwd", "dense_bwd", "chunk_single")
+             "decode_fp8_small", "decode_paged_small", "causal_bwd", "dense_bwd", "chunk_single",
+             "varlen_bwd")

@@ -1,5 +1,6 @@
 """Attention backward through the C ABI vs the fp64 oracle: dQ, dK, dV for
-head dims 64 and 128, causal and sliding-window masks with Sq != Sk, GQA and
+head dims 64, 128 and (192, 128) (the last with its dK/dV kernel in two
+passes and single-stage rings), causal and sliding-window masks with Sq != Sk, GQA and
 MQA, ragged tails, empty axes, determinism, and the full-size causal workload
 checked on one KV head group.
 
@@ -90,6 +91,35 @@ def check_bwd(w):
 def test_head_dims_gqa(d, causal):
     # 300 rows: two full 128-row tiles and a 44-row tail; GQA 4/2
     w = inputs.batched("bwd", 400 + d, 2, 300, 300, 4, 2, d, d, causal=causal)
+    print(check_bwd(w))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dims_192_128(causal):
+    # Dqk = 192, Dv = 128: 300 rows (two tiles and a tail), GQA 4/2
+    w = inputs.batched("bwd192", 480 + causal, 2, 300, 300, 4, 2, 192, 128, causal=causal)
+    print(check_bwd(w))
+
+
+def test_head_dims_192_128_many_jobs_and_windows():
+    # several query tiles per key block and q heads per KV head, so each single-stage
+    # ring turns over many times; Sq != Sk with a two-sided window
+    w = inputs.batched("bwd192j", 482, 1, 700, 600, 8, 2, 192, 128, causal=True)
+    print(check_bwd(w))
+    w2 = inputs.batched("bwd192w", 483, 2, 390, 450, 4, 1, 192, 128, window_left=150, window_right=60)
+    print(check_bwd(w2))
+
+
+def test_head_dims_192_128_varlen_window():
+    # the varlen shape of the forward's sliding-window workload, small: causal, window 200
+    lens = [300, 1, 129, 513, 64]
+    w = inputs.packed("bwd192vl", 484, lens, lens, 4, 4, 192, 128, causal=True, window_left=200)
+    print(check_bwd(w))
+
+
+def test_head_dims_192_128_seqused_k():
+    used = np.array([700, 1, 129], np.int32)
+    w = inputs.batched("bwd192su", 485, 3, 200, 768, 4, 2, 192, 128, causal=True, seqused_k=used)
     print(check_bwd(w))
 
 
