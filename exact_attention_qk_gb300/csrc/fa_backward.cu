@@ -24,9 +24,10 @@
 // accumulators from 256 (dQ; or dV then dK). With the (192, 128) head dims
 // dV and dK together (128 + 192 columns) do not fit beside S and dP, so the
 // dK/dV kernel runs as two launches: a dV-only pass (S^T, P^T, dV += P^T dO)
-// and a dK-only pass (S^T, dP^T, dS^T, dK += dS^T Q). Where shared memory holds
-// a single stage of the streamed pair, the MMA thread issues the next job's
-// GEMMs only after the current job has released the stage. Two warpgroups share each
+// and a dK-only pass (S^T, dP^T, dS^T, dK += dS^T Q). Where two stages of the
+// streamed tile pair do not fit in shared memory, its two tiles get rings of
+// their own: the 192-column tile (K; Q) two stages, the 128-column one (V; dO)
+// one stage, which only the job's first GEMM reads. Two warpgroups share each
 // 128 x 128 score block, warpgroup c taking columns [64c, 64c+64) for all 128
 // rows, in two phases: P from S (the dK/dV kernel writes P^T back in bf16),
 // then dS from dP and the P kept in registers, back in bf16. A bf16 result of
@@ -69,13 +70,19 @@ struct BwdCfg {
   static constexpr int PAIR = TQ + TV;
   // resident: Q, dO (dQ) or K, V (dK/dV; K alone in the dV-only pass)
   static constexpr int RES = (MODE == kDvOnly) ? TQ : PAIR;
-  // stages of the streamed pair (K, V for dQ; Q, dO and lse2 / D for dK/dV): two where they fit
-  static constexpr int ST = (RES + 2 * (PAIR + 1024) + 2048 <= 227 * 1024) ? 2 : 1;
+  // The streamed pair (K, V for dQ; Q, dO and lse2 / D for dK/dV) runs through
+  // two stages where two fit. Otherwise (SPLIT) its tiles get rings of their
+  // own: the A tile (K; Q with lse2 / D) two stages, the B tile (V; dO) one,
+  // which suffices since only the job's first GEMMs read it (dP = dO V^T).
+  static constexpr bool SPLIT = RES + 2 * (PAIR + 1024) + 2048 > 227 * 1024;
+  static constexpr int ST = 2;                         // stages of the pair, or of the A tile
+  static constexpr int A_BYTES = SPLIT ? TQ : PAIR;    // one stage of that ring
   static constexpr int OFF_RES = 0;
   static constexpr int OFF_STR = RES;
-  static constexpr int OFF_VEC = OFF_STR + ST * PAIR;  // dK/dV: lse2[128], D[128] per stage
+  static constexpr int OFF_B = OFF_STR + ST * A_BYTES; // SPLIT: the B tile's stage
+  static constexpr int OFF_VEC = OFF_B + (SPLIT ? TV : 0);   // dK/dV: lse2[128], D[128] per stage
   static constexpr int OFF_BAR = OFF_VEC + ST * 1024;
-  static constexpr int NBAR = 16;
+  static constexpr int NBAR = 18;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
   // at least half the SM's shared memory: one CTA (owning all 512 tensor-memory
   // columns) per SM
@@ -97,6 +104,8 @@ struct BBars {
   uint64_t* acc_full;   // accumulators final
   uint64_t* drain;
   uint64_t* k_fixed;    // dQ kernel, seqused_k: K rows past the used keys cleared
+  uint64_t* b_full;     // SPLIT: the B tile's stage landed
+  uint64_t* b_empty;    // SPLIT: the B tile's stage read
 };
 
 template <class Cfg>
@@ -113,6 +122,8 @@ __device__ __forceinline__ BBars carve(uint8_t* smem) {
   B.acc_full = b; b += 1;
   B.drain = b; b += 1;
   B.k_fixed = b; b += 1;
+  B.b_full = b; b += 1;
+  B.b_empty = b; b += 1;
   return B;
 }
 
@@ -132,6 +143,8 @@ __device__ __forceinline__ void init_bars(const BBars& B) {
   mbar_init(B.acc_full, 1);
   mbar_init(B.drain, 1);
   mbar_init(B.k_fixed, 1);
+  mbar_init(B.b_full, 1);
+  mbar_init(B.b_empty, 1);
   fence_barrier_init();
 }
 
@@ -336,23 +349,35 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
         }
       }
       constexpr unsigned wmask = TAIL ? 0xffffffffu : 1u;
-      uint32_t u = 0;
+      uint32_t u = 0, nka = 0, nbl = 0;   // blocks walked, K (ring) and V (SPLIT) copies issued by lane 0
       if (lane == 0 || TAIL) {
         for (int n = nhi - 1; n >= nlo; --n, ++u) {
           const int st = u % Cfg::ST;
-          uint8_t* dst = smem + Cfg::OFF_STR + st * Cfg::PAIR;
+          uint8_t* dst = smem + Cfg::OFF_STR + st * Cfg::A_BYTES;
           bool w = true;
           if (lane == 0) {
             w = u < Cfg::ST || mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard);
             if (w) {
-              mbar_arrive_expect_tx(&B.str_full[st], Cfg::PAIR);
+              mbar_arrive_expect_tx(&B.str_full[st], Cfg::A_BYTES);
 #pragma unroll
               for (int c = 0; c < (Cfg::CQ > Cfg::CV ? Cfg::CQ : Cfg::CV); ++c) {
                 if (c < Cfg::CQ)
                   tma_load_4d(dst + c * kChunk, &mapK, &B.str_full[st], c * 64, S.k_row0 + n * kB, g, S.bc);
-                if (c < Cfg::CV)
+                if (!Cfg::SPLIT && c < Cfg::CV)
                   tma_load_4d(dst + Cfg::TQ + c * kChunk, &mapV, &B.str_full[st], c * 64, S.k_row0 + n * kB, g,
                               S.bc);
+              }
+            }
+            if (w) ++nka;
+            if (Cfg::SPLIT && w) {   // V(u) into its own stage once dP(u-1) has read it
+              w = u == 0 || mbar_wait(B.b_empty, (u - 1) & 1, guard);
+              if (w) {
+                uint8_t* vdst = smem + Cfg::OFF_B;
+                mbar_arrive_expect_tx(B.b_full, Cfg::TV);
+#pragma unroll
+                for (int c = 0; c < Cfg::CV; ++c)
+                  tma_load_4d(vdst + c * kChunk, &mapV, B.b_full, c * 64, S.k_row0 + n * kB, g, S.bc);
+                ++nbl;
               }
             }
           }
@@ -371,10 +396,12 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
           }
         }
       }
-      // drain the copies still in flight (only after an abort can any be)
+      // drain the copies still in flight (only after an abort can any be):
+      // nka stages of the ring and nbl B-tile copies were issued
       if (lane == 0) {
-        for (uint32_t x = (u > (uint32_t)Cfg::ST ? u - Cfg::ST : 0); x < u; ++x)
+        for (uint32_t x = (nka > (uint32_t)Cfg::ST ? nka - Cfg::ST : 0); x < nka; ++x)
           drain_phase(&B.str_full[x % Cfg::ST], (x / Cfg::ST) & 1, p.timeout_ns);
+        if (Cfg::SPLIT && nbl > 0) drain_phase(B.b_full, (nbl - 1) & 1, p.timeout_ns);
         drain_phase(B.res_full, 0, p.timeout_ns);
       }
     }
@@ -384,24 +411,34 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
       // so that dP(u) runs while the warps form P(u), S(u+1) while they form
       // dS(u), and dQ(u) and dP(u+1) while they form P(u+1). dS(u) lives in
       // dP's columns, which dP(u+1) only overwrites after dQ(u) has read them
-      // (the tensor pipe runs one thread's MMAs in order). With one stage,
-      // S(u+1) needs K(u+1), which loads only once dQ(u) has released the
-      // stage: ... [dS(u)] dQ(u) | S(u+1) dP(u+1).
+      // (the tensor pipe runs one thread's MMAs in order). With SPLIT rings,
+      // V(u+1) loads once dP(u) has completed, well before dP(u+1) is issued.
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
       constexpr uint32_t IDESC_DQ = idesc_bf16_f32(kB, DK, false, true);
       const uint32_t q_base = smem_u32(smem + Cfg::OFF_RES), do_base = q_base + Cfg::TQ;
       const uint32_t nb = static_cast<uint32_t>(nhi - nlo);
-      auto kv = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * Cfg::PAIR); };
+      auto kv = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * Cfg::A_BYTES); };
+      auto vt = [&](uint32_t u) { return Cfg::SPLIT ? smem_u32(smem + Cfg::OFF_B) : kv(u) + Cfg::TQ; };
+      // dP(u) = dO V(u)^T, after the B stage has landed (SPLIT), released by a commit after it
+      auto issue_dp = [&](uint32_t u) -> bool {
+        if (Cfg::SPLIT) {
+          if (!mbar_wait(B.b_full, u & 1, guard)) return false;
+          tc_fence_after();
+        }
+        issue_ss(tmem + 128, do_base, vt(u), DV, IDESC_S);
+        mma_commit(B.dp_full);
+        if (Cfg::SPLIT) mma_commit(B.b_empty);
+        return true;
+      };
       bool ok = mbar_wait(B.res_full, 0, guard) && mbar_wait(&B.str_full[0], 0, guard);
       if (ok) {
         issue_ss(tmem, q_base, kv(0), DK, IDESC_S);                         // S  = Q K^T
         mma_commit(B.s_full);
-        issue_ss(tmem + 128, do_base, kv(0) + Cfg::TQ, DV, IDESC_S);        // dP = dO V^T
-        mma_commit(B.dp_full);
+        ok = issue_dp(0);                                                   // dP = dO V^T
       }
       for (uint32_t u = 0; ok && u < nb; ++u) {
         if (!mbar_wait(&B.p_done[0], u & 1, guard) || !mbar_wait(&B.p_done[1], u & 1, guard)) { ok = false; break; }
-        if (Cfg::ST > 1 && u + 1 < nb) {
+        if (u + 1 < nb) {
           if (!mbar_wait(&B.str_full[(u + 1) % Cfg::ST], ((u + 1) / Cfg::ST) & 1, guard)) { ok = false; break; }
           tc_fence_after();
           issue_ss(tmem, q_base, kv(u + 1), DK, IDESC_S);
@@ -424,16 +461,7 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
         }
         if (!ok) break;
         mma_commit(&B.str_empty[u % Cfg::ST]);
-        if (u + 1 < nb) {
-          if (Cfg::ST == 1) {
-            if (!mbar_wait(&B.str_full[0], (u + 1) & 1, guard)) { ok = false; break; }
-            tc_fence_after();
-            issue_ss(tmem, q_base, kv(u + 1), DK, IDESC_S);
-            mma_commit(B.s_full);
-          }
-          issue_ss(tmem + 128, do_base, kv(u + 1) + Cfg::TQ, DV, IDESC_S);
-          mma_commit(B.dp_full);
-        }
+        if (u + 1 < nb && !issue_dp(u + 1)) { ok = false; break; }
       }
       if (ok) mma_commit(B.acc_full);
       mma_commit(B.drain);
@@ -616,27 +644,39 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
         if (kDk && c < Cfg::CV)   // V feeds dP^T only
           tma_load_4d(res + Cfg::TQ + c * kChunk, &mapV, B.res_full, c * 64, S.k_row0 + j0, g, S.bc);
       }
-      uint32_t u = 0;
+      uint32_t u = 0, nbl = 0;
       for (; u < static_cast<uint32_t>(jobs); ++u) {
         const int st = u % Cfg::ST;
         const int hh = g * p.r + static_cast<int>(u) / nm, m = mlo + static_cast<int>(u) % nm;
         if (u >= Cfg::ST && !mbar_wait(&B.str_empty[st], ((u - Cfg::ST) / Cfg::ST) & 1, guard)) break;
-        uint8_t* dst = smem + Cfg::OFF_STR + st * Cfg::PAIR;
+        uint8_t* dst = smem + Cfg::OFF_STR + st * Cfg::A_BYTES;
         float* vec = reinterpret_cast<float*>(smem + Cfg::OFF_VEC + st * 1024);
         const int64_t vrow = ws_row0(p, b, hh) + m * kB;
-        mbar_arrive_expect_tx(&B.str_full[st], Cfg::PAIR + 1024);
+        mbar_arrive_expect_tx(&B.str_full[st], Cfg::A_BYTES + 1024);
 #pragma unroll
         for (int c = 0; c < (Cfg::CQ > Cfg::CV ? Cfg::CQ : Cfg::CV); ++c) {
           if (c < Cfg::CQ)
             tma_load_4d(dst + c * kChunk, &mapQ, &B.str_full[st], c * 64, S.q_row0 + m * kB, hh, S.bc);
-          if (c < Cfg::CV)
+          if (!Cfg::SPLIT && c < Cfg::CV)
             tma_load_4d(dst + Cfg::TQ + c * kChunk, &mapDO, &B.str_full[st], c * 64, S.q_row0 + m * kB, hh, S.bc);
         }
         bulk_load(vec, p.lse2 + vrow, 512, &B.str_full[st]);
         bulk_load(vec + 128, p.dsum + vrow, 512, &B.str_full[st]);
+        if (Cfg::SPLIT) {   // dO(u) into its own stage once dP^T(u-1) has read it
+          if (u > 0 && !mbar_wait(B.b_empty, (u - 1) & 1, guard)) { ++u; break; }
+          uint8_t* ddst = smem + Cfg::OFF_B;
+          mbar_arrive_expect_tx(B.b_full, Cfg::TV);
+#pragma unroll
+          for (int c = 0; c < Cfg::CV; ++c)
+            tma_load_4d(ddst + c * kChunk, &mapDO, B.b_full, c * 64, S.q_row0 + m * kB, hh, S.bc);
+          ++nbl;
+        }
       }
+      // drain the copies still in flight (only after an abort can any be): u
+      // stages of the ring and nbl B-tile copies were issued
       for (uint32_t x = (u > (uint32_t)Cfg::ST ? u - Cfg::ST : 0); x < u; ++x)
         drain_phase(&B.str_full[x % Cfg::ST], (x / Cfg::ST) & 1, p.timeout_ns);
+      if (Cfg::SPLIT && nbl > 0) drain_phase(B.b_full, (nbl - 1) & 1, p.timeout_ns);
       drain_phase(B.res_full, 0, p.timeout_ns);
     }
   } else if (warp == Cfg::MMA_WARP) {
@@ -647,27 +687,35 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
       // and dS^T(u) live in S's and dP's columns, which S(u+1) and dP(u+1) only
       // overwrite after dV(u) and dK(u) have read them (one thread's MMAs run
       // in order). The dV-only pass drops dP and dK, the dK-only pass dV (its
-      // S(u+1) then waits only for the warps to have read S(u)). With one stage,
-      // S(u+1) needs Q(u+1), which loads only once the job's last GEMM has
-      // released the stage: ... dK(u) | S(u+1) dP(u+1).
+      // S(u+1) then waits only for the warps to have read S(u)). With SPLIT
+      // rings, dO(u+1) loads once dP(u) has completed, before dP(u+1) is issued.
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
       constexpr uint32_t IDESC_DV = idesc_bf16_f32(kB, DV, false, true);
       constexpr uint32_t IDESC_DK = idesc_bf16_f32(kB, DK, false, true);
       constexpr uint32_t DV_COL = 256, DK_COL = (MODE == kBoth) ? 256 + DV : 256;
       const uint32_t k_base = smem_u32(smem + Cfg::OFF_RES), v_base = k_base + Cfg::TQ;
       const uint32_t nj = static_cast<uint32_t>(jobs);
-      auto qs = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * Cfg::PAIR); };
+      auto qs = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * Cfg::A_BYTES); };
+      auto dot = [&](uint32_t u) { return Cfg::SPLIT ? smem_u32(smem + Cfg::OFF_B) : qs(u) + Cfg::TQ; };
+      // dP^T(u) = V dO(u)^T, after the B stage has landed (SPLIT), released by a commit after it
+      auto issue_dp = [&](uint32_t u) -> bool {
+        if (Cfg::SPLIT) {
+          if (!mbar_wait(B.b_full, u & 1, guard)) return false;
+          tc_fence_after();
+        }
+        issue_ss(tmem + 128, v_base, dot(u), DV, IDESC_S);
+        mma_commit(B.dp_full);
+        if (Cfg::SPLIT) mma_commit(B.b_empty);
+        return true;
+      };
       bool ok = mbar_wait(B.res_full, 0, guard) && mbar_wait(&B.str_full[0], 0, guard);
       if (ok) {
         issue_ss(tmem, k_base, qs(0), DK, IDESC_S);                          // S^T  = K Q^T
         mma_commit(B.s_full);
-        if constexpr (kDk) {
-          issue_ss(tmem + 128, v_base, qs(0) + Cfg::TQ, DV, IDESC_S);        // dP^T = V dO^T
-          mma_commit(B.dp_full);
-        }
+        if constexpr (kDk) ok = issue_dp(0);                                 // dP^T = V dO^T
       }
       for (uint32_t u = 0; ok && u < nj; ++u) {
-        const uint32_t qb = qs(u), dob = qb + Cfg::TQ;
+        const uint32_t qb = qs(u), dob = dot(u);
         const bool acc = u > 0;
         for (int c = 0; c < 2; ++c) {
           if (!mbar_wait(&B.p_done[c], u & 1, guard)) { ok = false; break; }
@@ -677,7 +725,7 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
           }
         }
         if (!ok) break;
-        if (Cfg::ST > 1 && u + 1 < nj) {
+        if (u + 1 < nj) {
           if (!mbar_wait(&B.str_full[(u + 1) % Cfg::ST], ((u + 1) / Cfg::ST) & 1, guard)) { ok = false; break; }
           issue_ss(tmem, k_base, qs(u + 1), DK, IDESC_S);
           mma_commit(B.s_full);
@@ -691,17 +739,8 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
           if (!ok) break;
         }
         mma_commit(&B.str_empty[u % Cfg::ST]);
-        if (u + 1 < nj) {
-          if (Cfg::ST == 1) {
-            if (!mbar_wait(&B.str_full[0], (u + 1) & 1, guard)) { ok = false; break; }
-            tc_fence_after();
-            issue_ss(tmem, k_base, qs(u + 1), DK, IDESC_S);
-            mma_commit(B.s_full);
-          }
-          if constexpr (kDk) {
-            issue_ss(tmem + 128, v_base, qs(u + 1) + Cfg::TQ, DV, IDESC_S);
-            mma_commit(B.dp_full);
-          }
+        if constexpr (kDk) {
+          if (u + 1 < nj && !issue_dp(u + 1)) { ok = false; break; }
         }
       }
       if (ok) mma_commit(B.acc_full);
