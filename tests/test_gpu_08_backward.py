@@ -253,6 +253,27 @@ def test_full_size_causal_one_kv_group():
           compare(dv[b:b + 1, :, g:g + 1], rv, "dV"))
 
 
+@pytest.mark.slow
+def test_full_size_varlen_window_192_128_short_sequences():
+    """The varlen sliding-window workload's backward (16 sequences, Hq=Hkv=16,
+    Dqk=192, Dv=128, causal, window 1024) run at full size: every element of
+    dQ, dK and dV of its five shortest sequences (425..837 rows, all heads)."""
+    w = inputs.workload("varlen_bwd")
+    do = inputs.grad_out(w)
+    dq, dk, dv = run_bwd(w, do)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all().item()
+    cq, ck = w.cu_seqlens_q, w.cu_seqlens_k
+    lens = np.diff(cq)
+    kw = dict(scale=w.softmax_scale, causal=True, window_left=w.window_left, window_right=w.window_right)
+    for b in np.argsort(lens)[:5]:
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        rq, rk, rv = oracle.attention_backward(w.q[None, q0:q1], w.k[None, k0:k1], w.v[None, k0:k1],
+                                               do[None, q0:q1], **kw)
+        print(int(b), q1 - q0, compare(dq[q0:q1], rq[0], "dQ"), compare(dk[k0:k1], rk[0], "dK"),
+              compare(dv[k0:k1], rv[0], "dV"))
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_seqused_k_with_nan_cache_slots(d):
     """seqused_k: keys [0, seqused_k[b]) exist; the cache slots past them hold
