@@ -8,12 +8,14 @@ prefill workloads one persistent tcgen05 kernel (plus the varlen prepare
 kernel, or the combine when the library splits a small grid over the keys),
 for decode the split-KV kernel plus the combine kernel, for the backward
 workloads (`*_bwd`) one backward call (fa_bwd_two_streams: the preprocess,
-then the dK/dV kernel on a second, torch-owned stream concurrent with the dQ
-kernel; the forward's O and LSE are made once, untimed). The headline line is the causal
+then the dK/dV kernel (two passes at head dims 192/128) on a second,
+torch-owned stream concurrent with the dQ kernel; the forward's O and LSE are
+made once, untimed). The headline line is the causal
 GQA prefill (B=2, Hq=32, Hkv=4, Sq=Sk=4096, D=128) in TFLOP/s with the
 standard attention FLOP count 2*(Dqk+Dv)*#visible(i,j). The other workloads
 (the same shape without a mask, the tiny case, the large head dim, varlen,
-decode and its cache forms, chunked prefill, the backward) are measured in the
+decode and its cache forms, chunked prefill, the backward of the causal, dense
+and varlen shapes) are measured in the
 same run and listed compactly at the end of the line under "workloads" as
 [value, roofline fraction, kernel ms] (decode in GB/s of algorithmic bytes:
 Q + visible K/V rows + O + LSE; the backward in TFLOP/s of its five GEMMs,
@@ -281,7 +283,9 @@ class Runner:
             self.bws_bytes = fa.fa_bwd_workspace_size(self.args)
             self.bws = torch.empty(max(self.bws_bytes, 256), dtype=torch.uint8, device=dev)
             self.work = backward_flops(w)
-            self.launches_per_step = 3   # preprocess, dQ, dK/dV
+            # preprocess, dQ, dK/dV (a dV pass and a dK pass when both accumulators
+            # do not fit tensor memory beside S and dP: 256 + Dqk + Dv > 512 columns)
+            self.launches_per_step = 4 if 256 + w.head_dim_qk + w.head_dim_v > 512 else 3
 
     def stream_ptr(self):
         import ctypes

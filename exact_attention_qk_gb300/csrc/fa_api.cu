@@ -688,6 +688,9 @@ static int bwd_impl(const fa_fwd_args* a, const void* dout, void* dq, void* dk, 
   p.seqused_k = a->seqused_k;
   p.total_q = r.varlen ? a->total_q : 0;
   p.ws_rows = w.ws_rows;
+  // packed varlen: neighbouring tiles of one head in consecutive CTAs (the
+  // (sequence, head) index in y, whose limit is 65535)
+  p.tiles_fast = r.varlen && static_cast<int64_t>(a->batch) * a->num_heads_q <= 65535 ? 1 : 0;
   if (r.varlen) {   // batch strides are ignored in the packed layout
     p.q_bs = p.k_bs = p.v_bs = p.o_bs = 0;
   }

@@ -301,8 +301,13 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int b = blockIdx.x / p.hq, h = blockIdx.x % p.hq, g = h / p.r;
-  const int mb = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);   // longest tiles first
+  // Batched: x = (sequence, q head), y = query tile, longest tiles first. Packed
+  // varlen (tiles_fast): x = query tile, so the CTAs of neighbouring tiles of one
+  // head, which read the same K/V blocks, run together and share them in L2.
+  const int bx = p.tiles_fast ? blockIdx.y : blockIdx.x, by = p.tiles_fast ? blockIdx.x : blockIdx.y;
+  const int ny = p.tiles_fast ? static_cast<int>(gridDim.x) : static_cast<int>(gridDim.y);
+  const int b = bx / p.hq, h = bx % p.hq, g = h / p.r;
+  const int mb = ny - 1 - by;   // longest tiles first
   const BSeq S = bwd_seq(p, b);
   if (mb * kB >= S.sq) return;   // a tile past this sequence's end (whole CTA, before any barrier)
   const int off = S.sk - S.sq;
@@ -590,8 +595,13 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int b = blockIdx.x / p.hkv, g = blockIdx.x % p.hkv;
-  const int n = blockIdx.y;   // low key blocks first: under a causal mask they see the most query tiles
+  // Batched: x = (sequence, KV head), y = key block, low key blocks first (under a
+  // causal mask they see the most query tiles). Packed varlen (tiles_fast): x =
+  // key block, so neighbouring blocks of one KV head, which read the same Q and
+  // dO tiles, run together and share them in L2.
+  const int bx = p.tiles_fast ? blockIdx.y : blockIdx.x;
+  const int b = bx / p.hkv, g = bx % p.hkv;
+  const int n = p.tiles_fast ? blockIdx.x : blockIdx.y;
   const BSeq S = bwd_seq(p, b);
   if (n * kB >= S.sk) {   // a block past this sequence's keys (whole CTA, before any barrier)
     if (TAIL) {   // cache rows past seqused_k: dK = dV = 0 (this pass's accumulators)
@@ -936,7 +946,8 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtens
                                        Cfg::SMEM);
   if (e != cudaSuccess) return e;
   if ((e = set_dkdv_smem<DK, DV, TAIL>()) != cudaSuccess) return e;
-  const dim3 gq(p.batch * p.hq, mblocks), gk(p.batch * p.hkv, nblocks);
+  const dim3 gq = p.tiles_fast ? dim3(mblocks, p.batch * p.hq) : dim3(p.batch * p.hq, mblocks);
+  const dim3 gk = p.tiles_fast ? dim3(nblocks, p.batch * p.hkv) : dim3(p.batch * p.hkv, nblocks);
   if (mblocks > 0 && nblocks > 0 && side.stream != nullptr) {
     // The two kernels only share read-only inputs. dK/dV (few long CTAs under
     // a causal mask, longest first) goes on the caller's second stream, which

@@ -84,6 +84,7 @@ struct BwdParams {
   const int* seqused_k;          // int32 [batch] or NULL: keys [0, seqused_k[b]) exist
   int total_q;                   // varlen: rows of q (LSE row stride)
   int64_t ws_rows;               // varlen: workspace rows per head
+  int tiles_fast;                // grids with the tile / key-block index in x (packed varlen)
   int* status;
   unsigned long long timeout_ns;
 };
