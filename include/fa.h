@@ -207,8 +207,7 @@ int fa_combine(const float* out_partial, const float* lse_partial, int num_split
  * any entry point of this library on that device (with
  * CUDA_MODULE_LOADING=EAGER, when the library is loaded); it is held until the
  * process exits. The first call of this entry point on each device also looks
- * up the array's device address there (the device must be current); make
- * that first call before any stream capture.
+ * up the array's device address there (the device must be current).
  * The caller still passes q/k/v/out/lse in args. Only decode-shaped problems
  * (seqlen_q * Hq/Hkv <= 16) and fp8 caches are served, on the decode kernel;
  * other shapes return FA_ERR_UNSUPPORTED. args->num_splits is resolved as in
