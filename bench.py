@@ -14,8 +14,8 @@ made once, untimed). The headline line is the causal
 GQA prefill (B=2, Hq=32, Hkv=4, Sq=Sk=4096, D=128) in TFLOP/s with the
 standard attention FLOP count 2*(Dqk+Dv)*#visible(i,j). The other workloads
 (the same shape without a mask, the tiny case, the large head dim, varlen,
-decode and its cache forms, chunked prefill, the backward of the causal, dense
-and varlen shapes) are measured in the
+decode and its cache forms, chunked prefill, the backward of the causal, dense,
+varlen and large-head causal shapes) are measured in the
 same run and listed compactly at the end of the line under "workloads" as
 [value, roofline fraction, kernel ms] (decode in GB/s of algorithmic bytes:
 Q + visible K/V rows + O + LSE; the backward in TFLOP/s of its five GEMMs,
@@ -685,7 +685,8 @@ def main():
 
 
 SECONDARY = ("dense", "tiny", "large_dense", "large_causal", "varlen", "decode", "decode_fp8", "decode_paged",
-             "causal_paged", "chunk_gqa", "chunk_single", "causal_bwd", "dense_bwd", "varlen_bwd")
+             "causal_paged", "chunk_gqa", "chunk_single", "causal_bwd", "dense_bwd", "varlen_bwd",
+             "large_causal_bwd")
 DATA = "synthetic (seeded N(0,1) bf16, numpy PCG64)"
 
 

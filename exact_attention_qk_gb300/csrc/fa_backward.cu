@@ -58,7 +58,7 @@ constexpr int kB = 128;                 // rows of a query tile and of a key blo
 constexpr int kChunk = 128 * 128;       // bytes of 128 rows x 64 bf16 columns (one 128B-swizzle chunk)
 
 // Passes of the dK/dV kernel: both accumulators (head dims 64 and 128), or
-// the dV-only and dK-only passes of the (192, 128) head dims.
+// the dV-only and dK-only passes of the (192, 128) and (256, 256) head dims.
 enum : int { kBoth = 0, kDvOnly = 1, kDkOnly = 2 };
 
 template <int DK_, int DV_, int MODE_ = kBoth>
@@ -70,17 +70,30 @@ struct BwdCfg {
   static constexpr int PAIR = TQ + TV;
   // resident: Q, dO (dQ) or K, V (dK/dV; K alone in the dV-only pass)
   static constexpr int RES = (MODE == kDvOnly) ? TQ : PAIR;
-  // The streamed pair (K, V for dQ; Q, dO and lse2 / D for dK/dV) runs through
-  // two stages where two fit. Otherwise (SPLIT) its tiles get rings of their
-  // own: the A tile (K; Q with lse2 / D) two stages, the B tile (V; dO) one,
-  // which suffices since only the job's first GEMMs read it (dP = dO V^T).
-  static constexpr bool SPLIT = RES + 2 * (PAIR + 1024) + 2048 > 227 * 1024;
-  static constexpr int ST = 2;                         // stages of the pair, or of the A tile
+  // The streamed pair (K, V for dQ; Q, dO and lse2 / D for dK/dV), in the
+  // first of these layouts that fits the shared memory:
+  //   PAIR2  the pair in two stages;
+  //   SPLIT2 rings of their own: the A tile (K; Q with lse2 / D) two stages,
+  //          the B tile (V; dO) one, which suffices since only the job's
+  //          first GEMM reads it (dP = dO V^T);
+  //   PAIR1  the pair in one stage;
+  //   BHALF  the A tile one stage, the B tile in two halves (64-column
+  //          chunk pairs) through one half-tile slot: dP takes the two
+  //          halves of its contraction one after the other.
+  static constexpr int LIM = 227 * 1024 - 2048;       // tiles and lse2 / D (barriers aside)
+  static constexpr bool PAIR2 = RES + 2 * (PAIR + 1024) <= LIM;
+  static constexpr bool SPLIT2 = !PAIR2 && RES + 2 * (TQ + 1024) + TV <= LIM;
+  static constexpr bool PAIR1 = !PAIR2 && !SPLIT2 && RES + PAIR + 1024 <= LIM;
+  static constexpr bool BHALF = !PAIR2 && !SPLIT2 && !PAIR1;
+  static constexpr bool SPLIT = SPLIT2 || BHALF;      // the B tile in a ring of its own
+  static constexpr int ST = (PAIR2 || SPLIT2) ? 2 : 1; // stages of the pair, or of the A tile
   static constexpr int A_BYTES = SPLIT ? TQ : PAIR;    // one stage of that ring
+  static constexpr int B_PARTS = BHALF ? 2 : 1;        // B loads per job
+  static constexpr int B_BYTES = TV / B_PARTS;         // SPLIT: the B slot
   static constexpr int OFF_RES = 0;
   static constexpr int OFF_STR = RES;
-  static constexpr int OFF_B = OFF_STR + ST * A_BYTES; // SPLIT: the B tile's stage
-  static constexpr int OFF_VEC = OFF_B + (SPLIT ? TV : 0);   // dK/dV: lse2[128], D[128] per stage
+  static constexpr int OFF_B = OFF_STR + ST * A_BYTES; // SPLIT: the B slot
+  static constexpr int OFF_VEC = OFF_B + (SPLIT ? B_BYTES : 0);   // dK/dV: lse2[128], D[128] per stage
   static constexpr int OFF_BAR = OFF_VEC + ST * 1024;
   static constexpr int NBAR = 18;
   static constexpr int SMEM_USED = OFF_BAR + NBAR * 8 + 16;
@@ -90,7 +103,9 @@ struct BwdCfg {
   static constexpr int THREADS = 320;
   static constexpr int TMA_WARP = 8, MMA_WARP = 9;
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(OFF_STR % 1024 == 0 && PAIR % 1024 == 0, "128B-swizzled tiles start 1024-byte aligned");
+  static_assert(OFF_STR % 1024 == 0 && PAIR % 1024 == 0 && B_BYTES % 1024 == 0,
+                "128B-swizzled tiles start 1024-byte aligned");
+  static_assert(!BHALF || (RES + TQ + 1024 + TV / 2 <= LIM && CV % 2 == 0), "a layout that fits");
 };
 
 struct BBars {
@@ -164,6 +179,18 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_base, uint3
   for (int kk = 0; kk < kdim / 16; ++kk) {
     const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
     mma_bf16_ss(d_tmem, ad + off, bd + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// The 16-deep steps [kk0, kk1) of such a product, accumulating from kk0 > 0 on;
+// B's 64-column chunks sit at b_base from chunk b_chunk0 on (a half slot).
+__device__ __forceinline__ void issue_ss_part(uint32_t d_tmem, uint32_t a_base, uint32_t b_base, int kk0, int kk1,
+                                              int b_chunk0, uint32_t idesc) {
+  const uint64_t ad = sdesc_sw128(a_base, 16, 1024), bd = sdesc_sw128(b_base, 16, 1024);
+  for (int kk = kk0; kk < kk1; ++kk) {
+    const uint32_t aoff = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+    const uint32_t boff = (((kk >> 2) - b_chunk0) * kChunk + (kk & 3) * 32) >> 4;
+    mma_bf16_ss(d_tmem, ad + aoff, bd + boff, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -374,14 +401,18 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
               }
             }
             if (w) ++nka;
-            if (Cfg::SPLIT && w) {   // V(u) into its own stage once dP(u-1) has read it
-              w = u == 0 || mbar_wait(B.b_empty, (u - 1) & 1, guard);
+            // V(u) into its own slot (in two halves with BHALF), each load once dP
+            // has read the previous one
+            for (int hp = 0; Cfg::SPLIT && w && hp < Cfg::B_PARTS; ++hp) {
+              const uint32_t idx = u * Cfg::B_PARTS + hp;
+              w = idx == 0 || mbar_wait(B.b_empty, (idx - 1) & 1, guard);
               if (w) {
+                constexpr int CP = Cfg::CV / Cfg::B_PARTS;
                 uint8_t* vdst = smem + Cfg::OFF_B;
-                mbar_arrive_expect_tx(B.b_full, Cfg::TV);
+                mbar_arrive_expect_tx(B.b_full, Cfg::B_BYTES);
 #pragma unroll
-                for (int c = 0; c < Cfg::CV; ++c)
-                  tma_load_4d(vdst + c * kChunk, &mapV, B.b_full, c * 64, S.k_row0 + n * kB, g, S.bc);
+                for (int c = 0; c < CP; ++c)
+                  tma_load_4d(vdst + c * kChunk, &mapV, B.b_full, (hp * CP + c) * 64, S.k_row0 + n * kB, g, S.bc);
                 ++nbl;
               }
             }
@@ -418,21 +449,27 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
       // dP's columns, which dP(u+1) only overwrites after dQ(u) has read them
       // (the tensor pipe runs one thread's MMAs in order). With SPLIT rings,
       // V(u+1) loads once dP(u) has completed, well before dP(u+1) is issued.
+      // With one stage of K, S(u+1) needs K(u+1), which loads only once dQ(u)
+      // has released the stage: ... [dS(u)] dQ(u) | S(u+1) dP(u+1).
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
       constexpr uint32_t IDESC_DQ = idesc_bf16_f32(kB, DK, false, true);
       const uint32_t q_base = smem_u32(smem + Cfg::OFF_RES), do_base = q_base + Cfg::TQ;
       const uint32_t nb = static_cast<uint32_t>(nhi - nlo);
       auto kv = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * Cfg::A_BYTES); };
       auto vt = [&](uint32_t u) { return Cfg::SPLIT ? smem_u32(smem + Cfg::OFF_B) : kv(u) + Cfg::TQ; };
-      // dP(u) = dO V(u)^T, after the B stage has landed (SPLIT), released by a commit after it
+      // dP(u) = dO V(u)^T; with SPLIT each part of V (both halves of the
+      // contraction with BHALF) after its load landed, released by a commit after it
       auto issue_dp = [&](uint32_t u) -> bool {
-        if (Cfg::SPLIT) {
-          if (!mbar_wait(B.b_full, u & 1, guard)) return false;
-          tc_fence_after();
+        constexpr int KP = DV / 16 / Cfg::B_PARTS;   // 16-deep steps per part
+        for (int hp = 0; hp < Cfg::B_PARTS; ++hp) {
+          if (Cfg::SPLIT) {
+            if (!mbar_wait(B.b_full, (u * Cfg::B_PARTS + hp) & 1, guard)) return false;
+            tc_fence_after();
+          }
+          issue_ss_part(tmem + 128, do_base, vt(u), hp * KP, (hp + 1) * KP, hp * (Cfg::CV / Cfg::B_PARTS), IDESC_S);
+          if (Cfg::SPLIT) mma_commit(B.b_empty);
         }
-        issue_ss(tmem + 128, do_base, vt(u), DV, IDESC_S);
         mma_commit(B.dp_full);
-        if (Cfg::SPLIT) mma_commit(B.b_empty);
         return true;
       };
       bool ok = mbar_wait(B.res_full, 0, guard) && mbar_wait(&B.str_full[0], 0, guard);
@@ -443,7 +480,7 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
       }
       for (uint32_t u = 0; ok && u < nb; ++u) {
         if (!mbar_wait(&B.p_done[0], u & 1, guard) || !mbar_wait(&B.p_done[1], u & 1, guard)) { ok = false; break; }
-        if (u + 1 < nb) {
+        if (Cfg::ST > 1 && u + 1 < nb) {
           if (!mbar_wait(&B.str_full[(u + 1) % Cfg::ST], ((u + 1) / Cfg::ST) & 1, guard)) { ok = false; break; }
           tc_fence_after();
           issue_ss(tmem, q_base, kv(u + 1), DK, IDESC_S);
@@ -466,6 +503,12 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
         }
         if (!ok) break;
         mma_commit(&B.str_empty[u % Cfg::ST]);
+        if (Cfg::ST == 1 && u + 1 < nb) {
+          if (!mbar_wait(&B.str_full[0], (u + 1) & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+          issue_ss(tmem, q_base, kv(u + 1), DK, IDESC_S);
+          mma_commit(B.s_full);
+        }
         if (u + 1 < nb && !issue_dp(u + 1)) { ok = false; break; }
       }
       if (ok) mma_commit(B.acc_full);
@@ -672,15 +715,21 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
         }
         bulk_load(vec, p.lse2 + vrow, 512, &B.str_full[st]);
         bulk_load(vec + 128, p.dsum + vrow, 512, &B.str_full[st]);
-        if (Cfg::SPLIT) {   // dO(u) into its own stage once dP^T(u-1) has read it
-          if (u > 0 && !mbar_wait(B.b_empty, (u - 1) & 1, guard)) { ++u; break; }
+        // dO(u) into its own slot (in two halves with BHALF), each load once
+        // dP^T has read the previous one
+        bool bw = true;
+        for (int hp = 0; Cfg::SPLIT && hp < Cfg::B_PARTS; ++hp) {
+          const uint32_t idx = u * Cfg::B_PARTS + hp;
+          if (idx > 0 && !mbar_wait(B.b_empty, (idx - 1) & 1, guard)) { bw = false; break; }
+          constexpr int CP = Cfg::CV / Cfg::B_PARTS;
           uint8_t* ddst = smem + Cfg::OFF_B;
-          mbar_arrive_expect_tx(B.b_full, Cfg::TV);
+          mbar_arrive_expect_tx(B.b_full, Cfg::B_BYTES);
 #pragma unroll
-          for (int c = 0; c < Cfg::CV; ++c)
-            tma_load_4d(ddst + c * kChunk, &mapDO, B.b_full, c * 64, S.q_row0 + m * kB, hh, S.bc);
+          for (int c = 0; c < CP; ++c)
+            tma_load_4d(ddst + c * kChunk, &mapDO, B.b_full, (hp * CP + c) * 64, S.q_row0 + m * kB, hh, S.bc);
           ++nbl;
         }
+        if (!bw) { ++u; break; }
       }
       // drain the copies still in flight (only after an abort can any be): u
       // stages of the ring and nbl B-tile copies were issued
@@ -699,6 +748,8 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
       // in order). The dV-only pass drops dP and dK, the dK-only pass dV (its
       // S(u+1) then waits only for the warps to have read S(u)). With SPLIT
       // rings, dO(u+1) loads once dP(u) has completed, before dP(u+1) is issued.
+      // With one stage, S(u+1) needs Q(u+1), which loads only once the job's
+      // last GEMM has released the stage: ... dK(u) | S(u+1) dP(u+1).
       constexpr uint32_t IDESC_S = idesc_bf16_f32(kB, kB, false, false);
       constexpr uint32_t IDESC_DV = idesc_bf16_f32(kB, DV, false, true);
       constexpr uint32_t IDESC_DK = idesc_bf16_f32(kB, DK, false, true);
@@ -707,15 +758,19 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
       const uint32_t nj = static_cast<uint32_t>(jobs);
       auto qs = [&](uint32_t u) { return smem_u32(smem + Cfg::OFF_STR + (u % Cfg::ST) * Cfg::A_BYTES); };
       auto dot = [&](uint32_t u) { return Cfg::SPLIT ? smem_u32(smem + Cfg::OFF_B) : qs(u) + Cfg::TQ; };
-      // dP^T(u) = V dO(u)^T, after the B stage has landed (SPLIT), released by a commit after it
+      // dP^T(u) = V dO(u)^T; with SPLIT each part of dO (both halves of the
+      // contraction with BHALF) after its load landed, released by a commit after it
       auto issue_dp = [&](uint32_t u) -> bool {
-        if (Cfg::SPLIT) {
-          if (!mbar_wait(B.b_full, u & 1, guard)) return false;
-          tc_fence_after();
+        constexpr int KP = DV / 16 / Cfg::B_PARTS;   // 16-deep steps per part
+        for (int hp = 0; hp < Cfg::B_PARTS; ++hp) {
+          if (Cfg::SPLIT) {
+            if (!mbar_wait(B.b_full, (u * Cfg::B_PARTS + hp) & 1, guard)) return false;
+            tc_fence_after();
+          }
+          issue_ss_part(tmem + 128, v_base, dot(u), hp * KP, (hp + 1) * KP, hp * (Cfg::CV / Cfg::B_PARTS), IDESC_S);
+          if (Cfg::SPLIT) mma_commit(B.b_empty);
         }
-        issue_ss(tmem + 128, v_base, dot(u), DV, IDESC_S);
         mma_commit(B.dp_full);
-        if (Cfg::SPLIT) mma_commit(B.b_empty);
         return true;
       };
       bool ok = mbar_wait(B.res_full, 0, guard) && mbar_wait(&B.str_full[0], 0, guard);
@@ -735,7 +790,7 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
           }
         }
         if (!ok) break;
-        if (u + 1 < nj) {
+        if (Cfg::ST > 1 && u + 1 < nj) {
           if (!mbar_wait(&B.str_full[(u + 1) % Cfg::ST], ((u + 1) / Cfg::ST) & 1, guard)) { ok = false; break; }
           issue_ss(tmem, k_base, qs(u + 1), DK, IDESC_S);
           mma_commit(B.s_full);
@@ -749,6 +804,12 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
           if (!ok) break;
         }
         mma_commit(&B.str_empty[u % Cfg::ST]);
+        if (Cfg::ST == 1 && u + 1 < nj) {
+          if (!mbar_wait(&B.str_full[0], (u + 1) & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+          issue_ss(tmem, k_base, qs(u + 1), DK, IDESC_S);
+          mma_commit(B.s_full);
+        }
         if constexpr (kDk) {
           if (u + 1 < nj && !issue_dp(u + 1)) { ok = false; break; }
         }
@@ -975,7 +1036,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& mq, const CUtens
 }  // namespace
 
 bool bwd_supported(int dk, int dv) {
-  return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128);
+  return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 192 && dv == 128) || (dk == 256 && dv == 256);
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int dk, int dv, const CUtensorMap& mq, const CUtensorMap& mk,
@@ -991,6 +1052,9 @@ cudaError_t launch_bwd(const BwdParams& p, int dk, int dv, const CUtensorMap& mq
   if (dk == 192 && dv == 128)
     return tail ? launch_bwd_t<192, 128, true>(p, mq, mk, mv, mdo, stream, side)
                 : launch_bwd_t<192, 128, false>(p, mq, mk, mv, mdo, stream, side);
+  if (dk == 256 && dv == 256)
+    return tail ? launch_bwd_t<256, 256, true>(p, mq, mk, mv, mdo, stream, side)
+                : launch_bwd_t<256, 256, false>(p, mq, mk, mv, mdo, stream, side);
   return cudaErrorInvalidValue;
 }
 

@@ -42,6 +42,8 @@ Backward workloads (dQ, dK, dV given dO; dO is N(0,1) bf16 from its own stream):
   dense_bwd     the same shape without a mask
   varlen_bwd    the varlen sliding-window workload (Dqk=192 Dv=128; the same
                 q, k, v draws)
+  large_causal_bwd  the large-head causal shape (B=1 Hq=16 Hkv=2 S=8192 D=256;
+                the same q, k, v draws)
 """
 from __future__ import annotations
 
@@ -290,9 +292,9 @@ def workload(name: str) -> Workload:
     if name in ("causal", "dense"):
         # the causal GQA prefill and its unmasked twin (the same q, k, v draws)
         return batched(name, 2, 2, 4096, 4096, 32, 4, 128, 128, causal=(name == "causal"))
-    if name in ("large_dense", "large_causal"):
+    if name in ("large_dense", "large_causal", "large_causal_bwd"):
         return batched(name, 3, 1, 8192, 8192, 16, 2, 256, 256, scale=1.0 / 16,
-                       causal=(name == "large_causal"))
+                       causal=(name != "large_dense"))
     if name in ("varlen", "varlen_bwd"):
         lens = varlen_lengths()
         return packed(name, 4, lens, lens, 16, 16, 192, 128, causal=True,
@@ -331,4 +333,4 @@ def workload(name: str) -> Workload:
 WORKLOADS = ("tiny", "causal", "dense", "large_dense", "large_causal", "varlen", "decode", "decode_small",
              "decode_fp8", "decode_paged", "causal_paged", "chunk_gqa",
              "decode_fp8_small", "decode_paged_small", "causal_bwd", "dense_bwd", "chunk_single",
-             "varlen_bwd")
+             "varlen_bwd", "large_causal_bwd")

@@ -175,7 +175,7 @@ def test_status_strings(fa):
 @pytest.mark.parametrize("over,code", [
     (dict(page_table=0x50000, max_pages_per_seq=3, page_size=128, num_pages=6), 2),
     (dict(kv_format=1), 2),                               # fp8 cache
-    (dict(head_dim_qk=256, head_dim_v=256), 2),           # forward-only head dims
+    (dict(head_dim_qk=256, head_dim_v=128), 2),           # a forward-only head-dim pair
     (dict(num_heads_q=6, num_heads_kv=4), 1),
     (dict(out=0), 1),
     (dict(lse=0), 1),                                     # the forward's LSE is an input
@@ -187,9 +187,10 @@ def test_backward_rejections_before_launch(fa, over, code):
     assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == code
 
 
-def test_backward_accepts_head_dims_192_128(fa):
-    # (192, 128) is served; the call gets as far as the workspace check
-    a = _args(fa, lse=0x70000, head_dim_qk=192, head_dim_v=128)
+@pytest.mark.parametrize("dk,dv", [(192, 128), (256, 256)])
+def test_backward_accepts_large_head_dims(fa, dk, dv):
+    # served; the call gets as far as the workspace check
+    a = _args(fa, lse=0x70000, head_dim_qk=dk, head_dim_v=dv)
     assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 4
 
 
@@ -205,9 +206,10 @@ def test_backward_workspace(fa):
     assert fa.fa_bwd_workspace_size(a) == 2 * 2 * 8 * 384 * 4
     assert fa.lib().fa_bwd(ctypes.byref(a), 0x80000, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 4
     assert fa.lib().fa_bwd(ctypes.byref(a), 0x80008, 0x90000, 0xA0000, 0xB0000, None, 0, None) == 3
-    # (192, 128) is served (two dK/dV passes); (256, 256) is not
+    # (192, 128) and (256, 256) are served (two dK/dV passes); pairs the forward lacks are not
     assert fa.fa_bwd_workspace_size(_args(fa, head_dim_qk=192, head_dim_v=128)) == 2 * 2 * 8 * 384 * 4
-    assert fa.fa_bwd_workspace_size(_args(fa, head_dim_qk=256, head_dim_v=256)) == 0
+    assert fa.fa_bwd_workspace_size(_args(fa, head_dim_qk=256, head_dim_v=256)) == 2 * 2 * 8 * 384 * 4
+    assert fa.fa_bwd_workspace_size(_args(fa, head_dim_qk=256, head_dim_v=128)) == 0
     assert fa.lib().fa_bwd(ctypes.byref(_args(fa, batch=0)), 0, 0, 0, 0, None, 0, None) == 0
 
 

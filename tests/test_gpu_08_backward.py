@@ -1,6 +1,7 @@
 """Attention backward through the C ABI vs the fp64 oracle: dQ, dK, dV for
-head dims 64, 128 and (192, 128) (the last with its dK/dV kernel in two
-passes and single-stage rings), causal and sliding-window masks with Sq != Sk, GQA and
+head dims 64, 128, (192, 128) and 256 (the last two with the dK/dV kernel in
+two passes and the streamed tiles in rings of their own), causal and
+sliding-window masks with Sq != Sk, GQA and
 MQA, ragged tails, empty axes, determinism, and the full-size causal workload
 checked on one KV head group.
 
@@ -251,6 +252,23 @@ def test_full_size_causal_one_kv_group():
                                            do[b:b + 1, :, hs], scale=w.softmax_scale, causal=True)
     print(compare(dq[b:b + 1, :, hs], rq, "dQ"), compare(dk[b:b + 1, :, g:g + 1], rk, "dK"),
           compare(dv[b:b + 1, :, g:g + 1], rv, "dV"))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_head_dims_256(causal):
+    # D = 256: the dK/dV kernel in two passes, one stage of K / Q and V / dO in
+    # halves through one slot; 300 rows (two tiles and a tail), GQA 4/2
+    w = inputs.batched("bwd256", 490 + causal, 2, 300, 300, 4, 2, 256, 256, causal=causal)
+    print(check_bwd(w))
+
+
+def test_head_dims_256_varlen_window_and_seqused_k():
+    lens = [300, 1, 129, 400]
+    w = inputs.packed("bwd256vl", 492, lens, lens, 4, 2, 256, 256, causal=True, window_left=200)
+    print(check_bwd(w))
+    w2 = inputs.batched("bwd256su", 493, 3, 200, 768, 4, 2, 256, 256, causal=True,
+                        seqused_k=np.array([700, 1, 129], np.int32))
+    print(check_bwd(w2))
 
 
 @pytest.mark.slow
