@@ -234,10 +234,10 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
  * dout: dO, bf16, out's shape and strides (o_*_stride).
  * dq / dk / dv: written, bf16, with q's / k's / v's shapes and strides. Keys
  *   that no query sees get dK = dV = 0; rows that see no key get dQ = 0.
- * Supported: (head_dim_qk, head_dim_v) (64,64), (128,128) or (192,128) (the
- *   shape the interface page names for Blackwell; its dK/dV kernel runs as a
- *   dV pass and a dK pass, since both accumulators do not fit tensor memory
- *   beside S and dP); (256,256) gives FA_ERR_UNSUPPORTED; causal, sliding
+ * Supported: (head_dim_qk, head_dim_v) (64,64), (128,128), (192,128) (the
+ *   shape the interface page names for Blackwell) or (256,256); at the last
+ *   two the dK/dV kernel runs as a dV pass and a dK pass, since both
+ *   accumulators do not fit tensor memory beside S and dP; causal, sliding
  *   window, GQA/MQA and varlen (cu_seqlens_q / cu_seqlens_k) as in the
  *   forward; seqused_k as in the forward ("interface.py", `_flash_attn_bwd`
  *   takes seqused_q / seqused_k): only keys [0, seqused_k[b]) exist, cache
