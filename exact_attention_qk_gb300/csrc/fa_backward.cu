@@ -621,11 +621,10 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// One CTA of the dK/dV kernel (pass MODE); (xi, yi) is its grid position.
 template <int DK, int DV, bool TAIL, int MODE>
-__global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
-                    const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
-                    const BwdParams p) {
+__device__ __forceinline__ void dkdv_body(const CUtensorMap& mapQ, const CUtensorMap& mapK, const CUtensorMap& mapV,
+                                          const CUtensorMap& mapDO, const BwdParams& p, int xi, int yi) {
   using Cfg = BwdCfg<DK, DV, MODE>;
   static_assert(256 + (MODE == kBoth ? DK + DV : MODE == kDvOnly ? DV : DK) <= 512, "tensor memory budget");
   constexpr bool kDv = MODE != kDkOnly, kDk = MODE != kDvOnly;   // accumulators of this pass
@@ -642,9 +641,9 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
   // causal mask they see the most query tiles). Packed varlen (tiles_fast): x =
   // key block, so neighbouring blocks of one KV head, which read the same Q and
   // dO tiles, run together and share them in L2.
-  const int bx = p.tiles_fast ? blockIdx.y : blockIdx.x;
+  const int bx = p.tiles_fast ? yi : xi;
   const int b = bx / p.hkv, g = bx % p.hkv;
-  const int n = p.tiles_fast ? blockIdx.x : blockIdx.y;
+  const int n = p.tiles_fast ? xi : yi;
   const BSeq S = bwd_seq(p, b);
   if (n * kB >= S.sk) {   // a block past this sequence's keys (whole CTA, before any barrier)
     if (TAIL) {   // cache rows past seqused_k: dK = dV = 0 (this pass's accumulators)
@@ -953,6 +952,35 @@ __global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
 }
 
 template <int DK, int DV, bool TAIL, int MODE>
+__global__ void __launch_bounds__(BwdCfg<DK, DV, MODE>::THREADS, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                    const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
+                    const BwdParams p) {
+  dkdv_body<DK, DV, TAIL, MODE>(mapQ, mapK, mapV, mapDO, p, blockIdx.x, blockIdx.y);
+}
+
+// Both passes of the two-pass head dims in one grid: the even CTAs in x run
+// the dV pass and the odd ones the dK pass of the same (KV head, key block),
+// so that each pass's long causal CTAs share the SMs with the other's instead
+// of running after them.
+template <int DK, int DV, bool TAIL>
+__global__ void __launch_bounds__(BwdCfg<DK, DV, kDkOnly>::THREADS, 1)
+    bwd_dkdv2_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+                     const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapDO,
+                     const BwdParams p) {
+  static_assert(BwdCfg<DK, DV, kDvOnly>::THREADS == BwdCfg<DK, DV, kDkOnly>::THREADS, "one block shape");
+  const int xi = static_cast<int>(blockIdx.x >> 1), yi = static_cast<int>(blockIdx.y);
+  if (blockIdx.x & 1)
+    dkdv_body<DK, DV, TAIL, kDkOnly>(mapQ, mapK, mapV, mapDO, p, xi, yi);
+  else
+    dkdv_body<DK, DV, TAIL, kDvOnly>(mapQ, mapK, mapV, mapDO, p, xi, yi);
+}
+
+template <int DK, int DV, bool TAIL>
+constexpr int kSmem2 = BwdCfg<DK, DV, kDvOnly>::SMEM > BwdCfg<DK, DV, kDkOnly>::SMEM ? BwdCfg<DK, DV, kDvOnly>::SMEM
+                                                                                   : BwdCfg<DK, DV, kDkOnly>::SMEM;
+
+template <int DK, int DV, bool TAIL, int MODE>
 cudaError_t launch_dkdv(const BwdParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const CUtensorMap& mdo, dim3 grid, cudaStream_t stream) {
   using Cfg = BwdCfg<DK, DV, MODE>;
@@ -970,12 +998,8 @@ cudaError_t set_dkdv_smem() {   // (host calls kept ahead of the launches: they 
     return cudaFuncSetAttribute(bwd_dkdv_kernel<DK, DV, TAIL, kBoth>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 BwdCfg<DK, DV, kBoth>::SMEM);
   } else {
-    const cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<DK, DV, TAIL, kDvOnly>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               BwdCfg<DK, DV, kDvOnly>::SMEM);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(bwd_dkdv_kernel<DK, DV, TAIL, kDkOnly>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                BwdCfg<DK, DV, kDkOnly>::SMEM);
+    return cudaFuncSetAttribute(bwd_dkdv2_kernel<DK, DV, TAIL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmem2<DK, DV, TAIL>);
   }
 }
 
@@ -984,10 +1008,10 @@ cudaError_t launch_dkdv_all(const BwdParams& p, const CUtensorMap& mq, const CUt
                             const CUtensorMap& mdo, dim3 grid, cudaStream_t stream) {
   if constexpr (kOnePass<DK, DV, TAIL>) {
     return launch_dkdv<DK, DV, TAIL, kBoth>(p, mq, mk, mv, mdo, grid, stream);
-  } else {
-    const cudaError_t e = launch_dkdv<DK, DV, TAIL, kDvOnly>(p, mq, mk, mv, mdo, grid, stream);
-    if (e != cudaSuccess) return e;
-    return launch_dkdv<DK, DV, TAIL, kDkOnly>(p, mq, mk, mv, mdo, grid, stream);
+  } else {   // both passes in one grid, twice as wide in x
+    bwd_dkdv2_kernel<DK, DV, TAIL><<<dim3(2 * grid.x, grid.y), BwdCfg<DK, DV, kDkOnly>::THREADS,
+                                     kSmem2<DK, DV, TAIL>, stream>>>(mq, mk, mv, mdo, p);
+    return cudaGetLastError();
   }
 }
 
