@@ -8,7 +8,8 @@ prefill workloads one persistent tcgen05 kernel (plus the varlen prepare
 kernel, or the combine when the library splits a small grid over the keys),
 for decode the split-KV kernel plus the combine kernel, for the backward
 workloads (`*_bwd`) one backward call (fa_bwd_two_streams: the preprocess,
-then the dK/dV kernel (two passes at head dims 192/128) on a second,
+then the dK/dV kernel (a dV and a dK pass in one grid at head dims 192/128
+and 256) on a second,
 torch-owned stream concurrent with the dQ kernel; the forward's O and LSE are
 made once, untimed). The headline line is the causal
 GQA prefill (B=2, Hq=32, Hkv=4, Sq=Sk=4096, D=128) in TFLOP/s with the
@@ -283,9 +284,9 @@ class Runner:
             self.bws_bytes = fa.fa_bwd_workspace_size(self.args)
             self.bws = torch.empty(max(self.bws_bytes, 256), dtype=torch.uint8, device=dev)
             self.work = backward_flops(w)
-            # preprocess, dQ, dK/dV (a dV pass and a dK pass when both accumulators
-            # do not fit tensor memory beside S and dP: 256 + Dqk + Dv > 512 columns)
-            self.launches_per_step = 4 if 256 + w.head_dim_qk + w.head_dim_v > 512 else 3
+            # preprocess, dQ, dK/dV (its dV and dK passes share one grid at the head
+            # dims whose accumulators do not fit tensor memory together)
+            self.launches_per_step = 3
 
     def stream_ptr(self):
         import ctypes

@@ -236,7 +236,7 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
  *   that no query sees get dK = dV = 0; rows that see no key get dQ = 0.
  * Supported: (head_dim_qk, head_dim_v) (64,64), (128,128), (192,128) (the
  *   shape the interface page names for Blackwell) or (256,256); at the last
- *   two the dK/dV kernel runs as a dV pass and a dK pass, since both
+ *   two the dK/dV kernel runs a dV pass and a dK pass in one grid, since both
  *   accumulators do not fit tensor memory beside S and dP; causal, sliding
  *   window, GQA/MQA and varlen (cu_seqlens_q / cu_seqlens_k) as in the
  *   forward; seqused_k as in the forward ("interface.py", `_flash_attn_bwd`
@@ -247,8 +247,7 @@ int fa_fwd_decode_noalloc(const fa_fwd_args* args, void* stream);
  * workspace: at least fa_bwd_workspace_size(args) bytes, 256-byte aligned
  *   (fp32 LSE * log2(e) and D for every padded query row). The call is
  *   deterministic: no atomics, the same inputs give the same bits.
- * Every kernel runs on `stream`, one after the other (preprocess, dK/dV (one or
- * two launches), dQ).
+ * Every kernel runs on `stream`, one after the other (preprocess, dK/dV, dQ).
  */
 int fa_bwd(const fa_fwd_args* args, const void* dout, void* dq, void* dk, void* dv, void* workspace,
            size_t workspace_bytes, void* stream);
